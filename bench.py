@@ -1,0 +1,460 @@
+"""Benchmark: EAGLE draft-tree verify steps per second on one GB300 (or N replicas).
+
+A step is one pass of the verify hot path over one batch: tree attention for
+every layer, acceptance, KV commit (eagle_tree_attn x L, eagle_accept,
+eagle_kv_commit), captured in one CUDA graph and replayed.  The default workload
+is the LLaMA-3.1-8B-shaped one at 8K context (32 q / 8 kv heads x 128, vocab
+128256, 61-row dynamic tree, 32 layers); --config picks another.
+
+Output: one JSON line (rank 0).  `value` is whole-job verify steps/s with inputs
+resident in HBM; `e2e` is the same metric through the C ABI with the step's
+inputs copied from pinned host memory and its result read back inside the timed
+region; `roofline` rates the tree-attention launch against the measured HBM
+bandwidth; `cpu_baseline` times the CPU oracle on a bounded sample.
+
+--impl reference times the CPU oracle itself (as it stands, on the host cores) on
+the same workload, one bounded sample per step.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "traffic.json")
+L2_BYTES = 129 * 1024 * 1024
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            m = json.load(f)
+        return float(m["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def _workload_desc(w, batch):
+    return {"workload": f"{w.name}: {w.n_q_heads}q/{w.n_kv_heads}kv x {w.head_dim} {w.dtype}, vocab {w.vocab}, "
+                        f"prefix {w.prefix_min if w.prefix_min != w.prefix else w.prefix}"
+                        f"{'-' + str(w.prefix) if w.prefix_min != w.prefix else ''}, "
+                        f"{w.tree_mode} tree {w.rows} rows depth {w.depth}, T={w.temperature}, batch {batch}, "
+                        f"{w.layers} layers",
+            "batch": batch, "layers": w.layers, "tree_rows": w.rows, "prefix": int(w.prefix),
+            "vocab": w.vocab, "heads": f"{w.n_q_heads}/{w.n_kv_heads}x{w.head_dim}"}
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out" if os.path.isdir(os.path.join(ROOT, "gpurun_out")) else ".",
+                                 f".clocks_{os.getpid()}.csv")
+
+    def __enter__(self):
+        q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={q}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            time.sleep(0.2)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"]}
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            p = [x.strip() for x in line.split(",")]
+            if len(p) < 9:
+                continue
+            try:
+                sm.append(float(p[1]))
+                mx.append(float(p[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, p[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        try:
+            os.remove(self.path)
+        except OSError:
+            pass
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": float(max(mx)), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+def _traffic_for(kernel_src: str, workload: str):
+    """dram bytes per launch from the committed ncu summary, if the kernel is unchanged."""
+    try:
+        with open(PROFILE_TRAFFIC) as f:
+            t = json.load(f)
+        sha = hashlib.sha256(open(kernel_src, "rb").read()).hexdigest()
+        e = t.get(workload)
+        if e and e.get("source_sha256") == sha:
+            return float(e["dram_bytes_per_launch"])
+    except Exception:
+        pass
+    return None
+
+
+# ----------------------------------------------------------------------------- CPU oracle timing
+def oracle_sample(w, st_host, reps: int = 1):
+    """Time the CPU oracle on a bounded sample of one verify step: tree attention for
+    one KV head of one layer, plus the whole acceptance and commit.  Returns
+    (seconds per full step extrapolated, description, seconds spent)."""
+    import oracle
+    q, kc, vc, tk, tv, seq_len, parent, target, draft, tokens, ua, uf, max_path, n_acc, path = st_host
+    G = w.group
+    Bn = q.shape[0]
+    t0 = time.perf_counter()
+    for _ in range(reps):
+        oracle.tree_attn(np.ascontiguousarray(q[:, :, :G]), np.ascontiguousarray(kc[:, :1]),
+                         np.ascontiguousarray(vc[:, :1]), np.ascontiguousarray(tk[:, :1]),
+                         np.ascontiguousarray(tv[:, :1]), seq_len, parent, 1.0 / math.sqrt(w.head_dim))
+    t_attn = (time.perf_counter() - t0) / reps
+    t0 = time.perf_counter()
+    prop = oracle.SAMPLED if w.proposal == "sampled" else oracle.DELTA
+    res = oracle.accept(target, tokens, parent, ua, uf, w.temperature, prop, max_path, draft=draft)
+    t_acc = time.perf_counter() - t0
+    # commit: L layers of path-row copies (one layer's caches stand in for each layer)
+    t0 = time.perf_counter()
+    kcw, vcw = kc[None].copy(), vc[None].copy()
+    oracle.kv_commit(kcw, vcw, tk[None], tv[None], res["n_acc"], res["path"], seq_len)
+    t_com = (time.perf_counter() - t0) * w.layers
+    per_step = t_attn * w.n_kv_heads * w.layers + t_acc + t_com
+    desc = (f"oracle tree attention on 1 of {w.n_kv_heads} KV heads of 1 of {w.layers} layers "
+            f"(x{w.n_kv_heads * w.layers}), plus acceptance and commit for batch {Bn}; single thread")
+    return per_step, desc, t_attn * reps + t_acc + t_com / w.layers
+
+
+def host_inputs(st):
+    """Host copies of one layer's tensors and the step's acceptance inputs (for the oracle)."""
+    import torch
+    to_np = (lambda t: t.view(torch.int16).cpu().numpy().view(np.uint16)) if st.w.dtype == "bf16" else \
+        (lambda t: t.cpu().numpy())
+    parent = st.parent.cpu().numpy()
+    return (to_np(st.q[0]), to_np(st.kc[0]), to_np(st.vc[0]), to_np(st.tk[0]), to_np(st.tv[0]),
+            st.seq_len_init.cpu().numpy(), parent, st.target_host, st.draft_host, st.tokens.cpu().numpy(),
+            st.u_accept.cpu().numpy(), st.u_final.cpu().numpy(), st.max_depth + 1, None, None)
+
+
+# ----------------------------------------------------------------------------- main arms
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    from eagle_speculative_decoding_tree_gb300 import binding as B
+    from eagle_speculative_decoding_tree_gb300 import synth
+    from eagle_speculative_decoding_tree_gb300.step import VerifyStep
+
+    ws, rank, local = _dist()
+    torch.cuda.set_device(local)
+    if ws > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    w = synth.WORKLOADS[args.config]
+    batch = args.batch or w.batch
+    w = w.with_(batch=batch)
+    B.load()
+    t_setup = time.perf_counter()
+    st = VerifyStep(w, batch=batch)
+    torch.cuda.synchronize()
+    t_setup = time.perf_counter() - t_setup
+
+    stream = torch.cuda.Stream()
+    g = None
+    with torch.cuda.stream(stream):
+        for _ in range(2):  # warm the launch path before capture
+            st.run(stream)
+        stream.synchronize()
+        if not args.no_graph:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                st.run(stream)
+    step = (lambda: g.replay()) if g is not None else (lambda: st.run(stream))
+    splits = B.workspace_size(B.EAGLE_WS_TREE_ATTN, st.attn_desc)  # noqa: F841 (plan is fixed per desc)
+    per_layer_launches = 1 if st.attn_ws.numel() <= 16 else 2
+    launches_per_step = st.L * per_layer_launches + 2 + 2
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            step()
+    stream.synchronize()
+    kv_total = st.kv_bytes_per_layer() * st.L
+    l2_note = (f"inputs larger than L2: {kv_total / 1e9:.2f} GB of K/V read per step" if kv_total > L2_BYTES else
+               "L2 flushed between steps")
+    flush = None if kv_total > L2_BYTES else torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device="cuda")
+
+    # ---- timed region: K graph replays
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if ws > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            if flush is None:
+                for _ in range(args.steps):
+                    step()
+            else:
+                # L2 flush between steps is timed separately and subtracted
+                for _ in range(args.steps):
+                    flush.zero_()
+                    step()
+            e1.record(stream)
+        torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1)
+    if flush is not None:
+        f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            f0.record(stream)
+            for _ in range(args.steps):
+                flush.zero_()
+            f1.record(stream)
+        torch.cuda.synchronize()
+        ms -= f0.elapsed_time(f1)
+    if ws > 1:
+        dist.barrier()
+        t = torch.tensor([ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    clocks = clk.summary()
+    ms_per_step = ms / args.steps
+    value = ws * args.steps / (ms / 1e3)
+    n_acc = st.acc.n_acc.cpu().numpy()
+
+    # ---- roofline of the dominant kernel: tree attention, timed alone (graph of L layers)
+    ga = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        st.reset()
+        for l in range(st.L):
+            st.attn_layer(l, stream)
+        stream.synchronize()
+        with torch.cuda.graph(ga, stream=stream):
+            for l in range(st.L):
+                st.attn_layer(l, stream)
+        for _ in range(3):
+            ga.replay()
+        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        reps = max(5, args.steps // 4)
+        a0.record(stream)
+        for _ in range(reps):
+            ga.replay()
+        a1.record(stream)
+    torch.cuda.synchronize()
+    attn_ms = a0.elapsed_time(a1) / (reps * st.L)
+    peak, peak_kind = _peaks()
+    bytes_layer = st.kv_bytes_per_layer()
+    achieved = bytes_layer / (attn_ms / 1e3) / 1e9
+    traffic = _traffic_for(os.path.join(ROOT, "eagle_speculative_decoding_tree_gb300", "csrc", "tree_attn.cu"),
+                           args.config)
+    roofline = {"kernel": "tree_attn (split + combine launches, one layer)", "bound": "hbm",
+                "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
+                "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
+                else "fallback 6.8 TB/s", "traffic": traffic, "algorithmic_bytes_per_launch": bytes_layer,
+                "us_per_launch": round(attn_ms * 1e3, 2)}
+    step_bytes = kv_total + st.logit_bytes_visited(n_acc)
+    step_frac = step_bytes / (ms_per_step / 1e3) / 1e9 / peak
+
+    # ---- e2e through the C ABI with host buffers (pinned), copies inside the timed region
+    e2e = e2e_run(st, stream, args, ws)
+
+    line = {"metric": "verify steps/s (tree attention x L + accept + commit), 1 GB300", "value": round(value, 2),
+            "unit": "steps/s", "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(ms_per_step, 5), "us_per_step": round(ms_per_step * 1e3, 2),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+            "config": {**_workload_desc(w, batch), "l2": l2_note, "graph": g is not None,
+                       "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU"},
+            "step_roofline_frac": round(step_frac, 4), "step_algorithmic_bytes": int(step_bytes),
+            "mean_accept_length": float(np.mean(n_acc + 1)), "roofline": roofline, "e2e": e2e,
+            "gpu_launches": int(launches_per_step * args.steps), "clocks": clocks,
+            "setup_s": round(t_setup, 1)}
+    if rank == 0 and not args.skip_cpu_baseline:
+        per_step, desc, spent = oracle_sample(w, host_inputs(st))
+        line["cpu_baseline"] = {"value": round(1.0 / per_step, 6), "unit": "steps/s", "cores": 1, "kind": "oracle",
+                                "sample": desc, "seconds": round(spent, 1)}
+    if ws > 1:
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def e2e_run(st, stream, args, ws):
+    """The same step through the public API with host inputs: every step copies the
+    step's inputs (queries and tree K/V of all layers, logits, uniforms, tree) from
+    pinned host memory, runs the step, and reads the accepted tokens back."""
+    import torch
+    ins = [*st.q, *st.tk, *st.tv, st.target, st.u_accept, st.u_final, st.tokens, st.parent, st.anc_mask]
+    if st.draft is not None:
+        ins.append(st.draft)
+    host = [t.cpu().pin_memory() for t in ins]
+    outs = [st.acc.n_acc, st.acc.out_tok]
+    host_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs]
+    h2d = sum(t.numel() * t.element_size() for t in ins)
+    d2h = sum(t.numel() * t.element_size() for t in outs)
+    n = max(3, args.steps // 4)
+
+    def one():
+        for d, h in zip(ins, host):
+            d.copy_(h, non_blocking=True)
+        st.run(stream)
+        for h, d in zip(host_out, outs):
+            h.copy_(d, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            one()
+        stream.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(n):
+            one()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1)
+    return {"value": round(ws * n / (ms / 1e3), 2), "unit": "steps/s", "h2d_bytes_per_step": int(h2d),
+            "d2h_bytes_per_step": int(d2h), "steps": n, "ms_per_step": round(ms / n, 5)}
+
+
+def run_reference(args):
+    """The CPU oracle timed as the reference arm (rank 0 only)."""
+    ws, rank, local = _dist()
+    if rank != 0:
+        return
+    from eagle_speculative_decoding_tree_gb300 import synth
+    import oracle
+    oracle.build()
+    w = synth.WORKLOADS[args.config]
+    batch = args.batch or w.batch
+    w = w.with_(batch=batch)
+    st_host = reference_inputs(w, batch)
+    for _ in range(args.warmup):
+        oracle_sample(w, st_host)
+    per = []
+    desc = ""
+    t_all = time.perf_counter()
+    for _ in range(args.steps):
+        p, desc, _ = oracle_sample(w, st_host)
+        per.append(p)
+    spent = time.perf_counter() - t_all
+    sec = float(np.mean(per))
+    value = 1.0 / sec
+    line = {"impl": "reference", "metric": "verify steps/s (tree attention x L + accept + commit), 1 GB300",
+            "value": round(value, 6), "unit": "steps/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(sec * 1e3, 3), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": w.dtype, "data": "synthetic", "config": _workload_desc(w, batch),
+            "cpu_baseline": {"value": round(value, 6), "unit": "steps/s", "cores": 1, "kind": "oracle",
+                             "sample": desc, "seconds": round(spent, 1)},
+            "e2e": {"value": round(value, 6), "unit": "steps/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def reference_inputs(w, batch):
+    """Host inputs for the reference arm: one layer of attention tensors and a tree of
+    the workload's shape (the oracle builds it), logits at its nodes."""
+    import oracle
+    from eagle_speculative_decoding_tree_gb300 import synth
+    seq_len = synth.prefix_lengths(w, batch)
+    root_tok = synth.root_tokens(w, batch)
+    root_h = [synth.root_hash(w.config_id, b) for b in range(batch)]
+    lm = synth.hash_lm(w)
+    ua, uf, ud = synth.step_uniforms(w, batch, w.rows)
+    if w.tree_mode == "dynamic":
+        t = oracle.DynamicTree(batch, w.vocab, w.depth, w.top_k, w.total_tokens)
+        front = [[h] for h in root_h]
+        for level in range(1, w.depth + 1):
+            rows = synth.as_dtype_bytes(np.stack([lm.rows(front[b], "draft") for b in range(batch)]), w.dtype)
+            prev = None if level == 1 else t.frontier.copy()
+            t.expand(rows)
+            slot = t.frontier_parent_slot(prev)
+            tok = t.frontier_tokens()
+            front = [[synth.child_hash(front[b][int(slot[b, j])], int(tok[b, j])) for j in range(tok.shape[1])]
+                     for b in range(batch)]
+        tree = t.finalize(root_tok, seq_len)
+    else:
+        par = synth.static_parents(w.static_choices)
+        t = oracle.StaticTree(batch, w.vocab, par, w.tree_mode == "static_sampled", w.temperature)
+        hs = [[h] + [0] * (len(par) - 1) for h in root_h]
+        for level in range(1, int(t.depths.max()) + 1):
+            nodes = t.frontier_nodes(level)
+            rows = synth.as_dtype_bytes(np.stack([[lm.draft_row(hs[b][n]) for n in nodes] for b in range(batch)]),
+                                        w.dtype)
+            t.expand(rows, ud)
+            for b in range(batch):
+                for i in np.nonzero(t.depths == level)[0]:
+                    hs[b][i] = synth.child_hash(hs[b][par[i]], int(t.tokens[b, i]))
+        tree = t.finalize(root_tok, seq_len)
+    hs = []
+    for b in range(batch):
+        h = [root_h[b]]
+        for i in range(1, tree["tokens"].shape[1]):
+            h.append(synth.child_hash(h[tree["parent"][b, i]], int(tree["tokens"][b, i])))
+        hs.append(h)
+    target = synth.as_dtype_bytes(np.stack([lm.rows(hs[b], "target") for b in range(batch)]), w.dtype)
+    draft = synth.as_dtype_bytes(np.stack([lm.rows(hs[b], "draft") for b in range(batch)]), w.dtype) \
+        if w.proposal == "sampled" else None
+    R = tree["tokens"].shape[1]
+    q, kc, vc, tk, tv = synth.attn_tensors(w, 0, batch, seq_len, R)
+    return (q, kc, vc, tk, tv, seq_len, tree["parent"], target, draft, tree["tokens"], ua, uf,
+            int(tree["depth"].max()) + 1, None, None)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", default="llama8b",
+                    choices=["tiny", "vicuna7b", "llama8b", "long128k", "concurrency"])
+    ap.add_argument("--batch", type=int, default=0, help="override the workload's batch (concurrency: 1/8/32)")
+    ap.add_argument("--no-graph", action="store_true")
+    ap.add_argument("--skip-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

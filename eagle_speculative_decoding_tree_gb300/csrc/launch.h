@@ -1,0 +1,78 @@
+// launch.h -- internal launcher interface between the C-ABI layer (abi.cu) and the
+// kernel files.  Launchers assume arguments were validated on the host.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/eagle.h"
+
+namespace eagle {
+
+// ------------------------------------------------------------------ tree build
+struct StaticShape {
+  int32_t rows;
+  int8_t parent[128];
+  int8_t depth[128];
+};
+
+struct TreeBuildPlan {
+  int B, V, mode, depth, k, N, R, W, dtype;
+  float temperature;
+  int n_chunks;   // vocabulary chunks per row
+  int f_max;      // widest frontier
+  int pool_cap;   // dynamic pool capacity per request
+  StaticShape shape;
+  // workspace carve-up (byte offsets)
+  size_t off_pool_tok, off_pool_par, off_pool_score, off_pool_depth, off_state, off_front,
+      off_part, off_node_tok, off_node_score, total;
+};
+void plan_tree_build(const eagle_tree_desc* d, TreeBuildPlan* p);
+int frontier_rows(const TreeBuildPlan& p, int level);
+cudaError_t launch_tree_build(const TreeBuildPlan& p, int level, const void* logits, const float* u_draft,
+                              const int32_t* root_tok, const int32_t* seq_len, void* ws, const eagle_tree& out,
+                              cudaStream_t s);
+
+// ------------------------------------------------------------------ tree attention
+struct AttnPlan {
+  int B, R, Hq, Hkv, G, D, P, dtype, W, out_dtype;
+  bool precise;
+  float scale;
+  int rows_per_cta;  // query rows (node x head-in-group) per CTA
+  int row_blocks;
+  int splits;
+  int rows_pad;      // row_blocks * rows_per_cta
+  size_t off_o, off_ml, total;
+};
+void plan_tree_attn(const eagle_attn_desc* d, int num_sms, AttnPlan* p);
+cudaError_t launch_tree_attn(const AttnPlan& p, const void* q, const void* k_cache, const void* v_cache,
+                             const void* tree_k, const void* tree_v, const int32_t* seq_len,
+                             const uint64_t* anc_mask, void* out, float* lse, void* ws, cudaStream_t s);
+
+// ------------------------------------------------------------------ accept
+struct AcceptPlan {
+  int B, R, V, dtype, proposal, max_depth;
+  float temperature;
+  int n_chunks;
+  int n_sources;  // 1 (target) or 2 (target + draft)
+  size_t off_part, total;
+};
+void plan_accept(const eagle_accept_desc* d, AcceptPlan* p);
+cudaError_t launch_accept(const AcceptPlan& p, const void* target, const void* draft, const int32_t* tokens,
+                          const int32_t* parent, const float* u_accept, const float* u_final,
+                          const eagle_accept_out& out, void* ws, cudaStream_t s);
+
+// ------------------------------------------------------------------ commit
+constexpr int kMaxLayers = 128;
+struct CommitArgs {
+  void* k_cache[kMaxLayers];
+  void* v_cache[kMaxLayers];
+  const void* tree_k[kMaxLayers];
+  const void* tree_v[kMaxLayers];
+};
+cudaError_t launch_kv_commit(const eagle_commit_desc* d, const CommitArgs& a, const int32_t* n_acc,
+                             const int32_t* path, int32_t* seq_len, int32_t* commit_pos, void* feat_cache,
+                             const void* tree_feat, uint32_t* status, cudaStream_t s);
+
+}  // namespace eagle

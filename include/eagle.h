@@ -1,0 +1,268 @@
+/*
+ * eagle.h -- C ABI of the EAGLE draft-tree verify step on one GB300 (sm_103a).
+ *
+ * One verify step of EAGLE-style lossless speculative decoding has four stages,
+ * one entry point each:
+ *
+ *   eagle_tree_build  draft-tree construction, one draft level per call
+ *                     (EAGLE review (zenmind), section 3.1 and appendix A.1:
+ *                     top-k children per node, k = 4 at the root, static tree;
+ *                     EAGLE-3 visual reading, "EAGLE-2": dynamic tree that keeps
+ *                     the most confident candidates, draft confidence tracking
+ *                     acceptance, Figures 4 and 6).
+ *   eagle_tree_attn   attention of every tree node over the prefix KV cache and
+ *                     its own ancestors in the tree (EAGLE review, terms "tree
+ *                     attention" and section 3.3; lesson "Speculative decoding
+ *                     and EAGLE-3", glossary "Tree attention": a flash-attention
+ *                     call with a tree mask).
+ *   eagle_accept      multi-round speculative sampling down the tree, greedy
+ *                     argmax matching at temperature 0 (EAGLE review, section 3.3
+ *                     and appendix A.2 / Algorithm 1; lesson steps 1-2, "bonus
+ *                     token").
+ *   eagle_kv_commit   compaction of the accepted path's K/V (and feature rows)
+ *                     into the contiguous cache (EAGLE review, section 3.3 and
+ *                     data path step 7; lesson "KV cache rollback", step 4).
+ *
+ * Conventions shared by every call
+ *   - All buffer pointers are DEVICE pointers unless the comment says HOST.
+ *     The caller owns every buffer; the library allocates nothing, keeps no
+ *     state between calls and is reentrant.  Scratch memory comes from the
+ *     caller's `ws` buffer, sized by eagle_workspace_size().
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Every call
+ *     only enqueues work on it and returns; nothing synchronises.  Outputs are
+ *     valid once the stream has reached the call's work.  No call does a
+ *     device-to-host copy, so a whole verify step can be captured in one graph.
+ *   - Argument errors are detected on the host before anything is enqueued and
+ *     returned as EAGLE_ERR_*; nothing is launched in that case.  Conditions that
+ *     depend on device data (a malformed tree, a full cache) set bits in a device
+ *     status word that the caller reads after the stream completes.  No call
+ *     traps, asserts or prints on the device.
+ *   - Element types: EAGLE_F32 or EAGLE_BF16.  Every accumulation is fp32.
+ *   - Device buffers must be 16-byte aligned (EAGLE_ERR_ALIGNMENT otherwise).
+ *
+ * Shapes (B batch, R tree rows including the root, V vocabulary, Hq / Hkv query /
+ * KV heads, G = Hq / Hkv, D head dim, P cache capacity per request, W = ceil(R/64))
+ *   tree tokens / parent / depth / pos_id   int32  [B][R]   row 0 = root, parent[0] = -1,
+ *                                                           parent[i] < i (parents first)
+ *   ancestor mask                           uint64 [B][R][W] bit j of row i set iff node j
+ *                                                           is node i or an ancestor of i
+ *   q, attention out                        [B][R][Hq][D]
+ *   KV cache (per layer)                    [B][Hkv][P][D]
+ *   tree K/V (per layer)                    [B][Hkv][R][D]
+ *   logits                                  [B][R][V]
+ */
+#ifndef EAGLE_H
+#define EAGLE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---------------------------------------------------------------- status codes */
+enum {
+  EAGLE_OK = 0,
+  EAGLE_ERR_INVALID_ARG = 1, /* NULL pointer, non-positive size, inconsistent shape */
+  EAGLE_ERR_UNSUPPORTED = 2, /* outside the supported envelope (see each call) */
+  EAGLE_ERR_ALIGNMENT = 3,   /* a device buffer is not 16-byte aligned */
+  EAGLE_ERR_WORKSPACE = 4,   /* ws is NULL or smaller than eagle_workspace_size() */
+  EAGLE_ERR_CUDA = 5         /* a kernel launch failed; cudaGetLastError() has the cause */
+};
+
+/* Bits of the device status word written by eagle_accept / eagle_kv_commit.
+ * The caller zeroes the word; the library only ORs bits into it. */
+#define EAGLE_STATUS_BAD_TREE 0x1u      /* a row's parent is not an earlier row, or a path node is out of range */
+#define EAGLE_STATUS_PATH_OVERFLOW 0x2u /* accepted path deeper than max_depth: truncated */
+#define EAGLE_STATUS_CACHE_FULL 0x4u    /* seq_len + n_acc + 1 > max_seq: that request was not committed */
+#define EAGLE_STATUS_BAD_TOKEN 0x8u     /* a draft token outside [0, V): treated as rejected */
+
+/* Element types */
+enum { EAGLE_F32 = 0, EAGLE_BF16 = 1 };
+
+/* Tree modes */
+enum {
+  EAGLE_TREE_DYNAMIC = 0,       /* EAGLE-2: top-k per frontier node, rerank by cumulative confidence */
+  EAGLE_TREE_STATIC_TOPK = 1,   /* fixed shape; a node's children are its best tokens in rank order */
+  EAGLE_TREE_STATIC_SAMPLED = 2 /* fixed shape; children drawn i.i.d. from the draft distribution */
+};
+
+/* What distribution a draft candidate was proposed from (used by eagle_accept). */
+enum {
+  EAGLE_PROPOSAL_DELTA = 0,  /* deterministic candidates (top-k / dynamic trees): q = point mass */
+  EAGLE_PROPOSAL_SAMPLED = 1 /* candidates drawn from softmax(draft / T): q = that softmax */
+};
+
+/* Precision of the attention PV product (bf16 path) */
+enum {
+  EAGLE_ATTN_STANDARD = 0, /* P rounded to bf16 (8 significant bits), as flash attention does */
+  EAGLE_ATTN_PRECISE = 1   /* P split into two bf16 terms (hi + lo, ~16 bits): one extra MMA per PV
+                              step; for sharply peaked rows where bf16 rounding of P shows */
+};
+
+/* Workspace kinds for eagle_workspace_size() */
+enum { EAGLE_WS_TREE_BUILD = 1, EAGLE_WS_TREE_ATTN = 2, EAGLE_WS_ACCEPT = 3 };
+
+/* ---------------------------------------------------------------- tree build */
+typedef struct {
+  int32_t batch;              /* B >= 1 */
+  int32_t vocab;              /* V >= 1 */
+  int32_t mode;               /* EAGLE_TREE_* */
+  int32_t depth;              /* draft levels D, 1..16 (dynamic), or the static shape's depth */
+  int32_t top_k;              /* dynamic: children per frontier node and frontier width, 1..16 */
+  int32_t total_tokens;       /* dynamic: drafts kept N; rows R = N + 1 <= 128 and N <= the pool size */
+  int32_t n_static;           /* static: number of draft nodes; R = n_static + 1 <= 128 */
+  const int32_t* static_parent; /* static: HOST array [R], parent[0] = -1, parent[i] < i, nodes
+                                   ordered by depth; at most 16 children per node */
+  int32_t dtype;              /* element type of the draft logits */
+  float temperature;          /* STATIC_SAMPLED: draw temperature (> 0) */
+} eagle_tree_desc;
+
+typedef struct {             /* all DEVICE pointers, caller-allocated */
+  int32_t* tokens;           /* [B][R]   written after the last level */
+  int32_t* parent;           /* [B][R]   written after the last level */
+  int32_t* depth;            /* [B][R]   written after the last level */
+  int32_t* pos_id;           /* [B][R]   = seq_len[b] + depth, written after the last level */
+  uint64_t* anc_mask;        /* [B][R][W] written after the last level */
+  float* score;              /* [B][R]   cumulative ln draft confidence (root 0) */
+  int32_t* frontier_tok;     /* [B][F_max] tokens of the nodes whose draft rows feed the next level */
+  int32_t* frontier_slot;    /* [B][F_max] each such node's parent row in this level's input */
+  int32_t* near_tie;         /* [B]      selection or draw decisions within 1e-5 of a boundary */
+} eagle_tree;
+
+/* Rows the frontier_logits of `level` must have: 1 at level 1; then top_k (dynamic)
+ * or the number of depth level-1 nodes (static).  -1 on a bad argument. */
+int eagle_tree_frontier_rows(const eagle_tree_desc* d, int level);
+
+/* Widest frontier over all levels (the F_max of eagle_tree.frontier_*). */
+int eagle_tree_max_frontier(const eagle_tree_desc* d);
+
+/* Run draft level `level` (1..depth) of the tree build.
+ *   frontier_logits  [B][F][V] draft logits of the current frontier rows, in the
+ *                    order eagle_tree.frontier_tok listed them after the previous
+ *                    level (level 1: the root row).
+ *   u_draft          [B][R] fp32 uniforms in [0,1), one per node (STATIC_SAMPLED;
+ *                    else may be NULL).  Node i's token is drawn with u_draft[b][i].
+ *   root_tok, seq_len [B] int32: the pending token and the prefix length (used by
+ *                    the last level).
+ *   ws               scratch of eagle_workspace_size(EAGLE_WS_TREE_BUILD, d) bytes.
+ *                    It carries the candidate pool from level to level: pass the
+ *                    same ws, untouched, to levels 1..depth of one build.
+ * After each level frontier_tok / frontier_slot name the next level's rows.  The
+ * last level writes the tree.  Ties inside a row go to the lower token id;
+ * scores are compared in fp32 with the pool index breaking ties. */
+int eagle_tree_build(const eagle_tree_desc* d, int level, const void* frontier_logits,
+                     const float* u_draft, const int32_t* root_tok, const int32_t* seq_len,
+                     void* ws, size_t ws_bytes, const eagle_tree* out, void* stream);
+
+/* ---------------------------------------------------------------- tree attention */
+typedef struct {
+  int32_t batch;       /* B */
+  int32_t rows;        /* R = tree rows incl. root, 1..128 */
+  int32_t n_q_heads;   /* Hq, a multiple of n_kv_heads */
+  int32_t n_kv_heads;  /* Hkv */
+  int32_t head_dim;    /* D: 64 or 128 */
+  int32_t max_seq;     /* P: cache capacity per request (rows of the K/V cache) */
+  float scale;         /* softmax scale, usually 1/sqrt(D) */
+  int32_t dtype;       /* element type of q, caches and tree K/V */
+  int32_t num_splits;  /* prefix splits per (request, KV head); 0 = choose from the SM count */
+  int32_t out_dtype;   /* element type of out: EAGLE_F32, or EAGLE_BF16 when dtype is EAGLE_BF16 */
+  int32_t precision;   /* EAGLE_ATTN_STANDARD or EAGLE_ATTN_PRECISE (ignored for fp32 inputs) */
+} eagle_attn_desc;
+
+/* One layer of tree attention.  Row i of request b, query head hq attends to the
+ * prefix keys j < seq_len[b] of KV head hq / G and to the tree keys a whose bit is
+ * set in anc_mask[b][i]:
+ *     out = softmax(scale * q k^T) v,   lse = ln sum exp(scale * q k^T)  (natural log)
+ *   q [B][R][Hq][D]; k_cache, v_cache [B][Hkv][P][D]; tree_k, tree_v [B][Hkv][R][D];
+ *   seq_len [B] int32 (0 <= seq_len <= P); anc_mask [B][R][W]; out [B][R][Hq][D];
+ *   lse [B][R][Hq] fp32, may be NULL.
+ * ws: eagle_workspace_size(EAGLE_WS_TREE_ATTN, d) bytes (split partials).
+ * Unsupported: head_dim not 64/128, R > 128, Hq % Hkv != 0, bf16 out with fp32 inputs. */
+int eagle_tree_attn(const eagle_attn_desc* d, const void* q, const void* k_cache, const void* v_cache,
+                    const void* tree_k, const void* tree_v, const int32_t* seq_len,
+                    const uint64_t* anc_mask, void* out, float* lse, void* ws, size_t ws_bytes,
+                    void* stream);
+
+/* ---------------------------------------------------------------- acceptance */
+typedef struct {
+  int32_t batch;       /* B */
+  int32_t rows;        /* R, 1..128 */
+  int32_t vocab;       /* V */
+  float temperature;   /* T; 0 = greedy argmax matching */
+  int32_t proposal;    /* EAGLE_PROPOSAL_* (ignored when T == 0) */
+  int32_t dtype;       /* element type of the logits */
+  int32_t max_depth;   /* path arrays hold max_depth + 1 entries */
+} eagle_accept_desc;
+
+typedef struct {       /* all DEVICE pointers, caller-allocated */
+  int32_t* n_acc;      /* [B] accepted drafts */
+  int32_t* path;       /* [B][max_depth+1] accepted node rows, root first, -1 padded */
+  int32_t* out_tok;    /* [B][max_depth+1] accepted tokens then the emitted token, -1 padded */
+  int32_t* near_tie;   /* [B] 1 if a decision had |u - p/q| < 1e-5 or a draw landed within
+                          1e-5 of a bin edge */
+  uint32_t* status;    /* [1] EAGLE_STATUS_* bits (ORed) */
+} eagle_accept_out;
+
+/* Walk the tree from the root.  T == 0: the child whose token is the target argmax
+ * (lowest id on ties) is accepted, else the argmax is emitted.  T > 0: with
+ * p = softmax(target[cur] / T), the children of cur are tried in row order:
+ * child d is accepted iff u_accept[b][child] < p(d) / q(d); otherwise
+ * p <- norm(max(0, p - q)) and the next child is tried; when all are rejected, or
+ * cur is a leaf, icdf(p, u_final[b]) is emitted (the smallest index whose running
+ * sum exceeds u * sum).  q is a point mass on d for EAGLE_PROPOSAL_DELTA and
+ * softmax(draft[cur] / T) for EAGLE_PROPOSAL_SAMPLED.
+ *   target_logits, draft_logits [B][R][V] (draft only for SAMPLED, else NULL);
+ *   tree_tokens, tree_parent [B][R]; u_accept [B][R]; u_final [B] (fp32 in [0,1)).
+ * ws: eagle_workspace_size(EAGLE_WS_ACCEPT, d) bytes. */
+int eagle_accept(const eagle_accept_desc* d, const void* target_logits, const void* draft_logits,
+                 const int32_t* tree_tokens, const int32_t* tree_parent, const float* u_accept,
+                 const float* u_final, const eagle_accept_out* out, void* ws, size_t ws_bytes,
+                 void* stream);
+
+/* ---------------------------------------------------------------- KV commit */
+typedef struct {
+  int32_t layers;      /* L, 1..128 */
+  int32_t batch;       /* B */
+  int32_t n_kv_heads;  /* Hkv */
+  int32_t head_dim;    /* D (any, with D * element size a multiple of 16 bytes) */
+  int32_t rows;        /* R */
+  int32_t max_seq;     /* P */
+  int32_t max_depth;   /* path arrays hold max_depth + 1 entries */
+  int32_t dtype;       /* K/V element type */
+  int32_t feat_dim;    /* feature row width; 0 = no feature rows */
+  int32_t feat_dtype;  /* feature element type */
+} eagle_commit_desc;
+
+/* For every layer l, request b, KV head h and m = 0..n_acc[b]: copy tree row
+ * path[b][m] of tree_k/v_layers[l] to cache row seq_len[b] + m of
+ * k/v_cache_layers[l]; copy feature row path[b][m] of tree_feat [B][R][F] to
+ * feat_cache [B][P][F] row seq_len[b] + m; set commit_pos[b][m] = seq_len[b] + m
+ * (-1 beyond n_acc); then seq_len[b] += n_acc[b] + 1.  A request whose commit
+ * would pass max_seq is left untouched and flagged EAGLE_STATUS_CACHE_FULL.
+ *   k_cache_layers, v_cache_layers, tree_k_layers, tree_v_layers: HOST arrays of
+ *   `layers` DEVICE pointers; each cache [B][Hkv][P][D], each tree [B][Hkv][R][D].
+ *   n_acc [B], path [B][max_depth+1] as written by eagle_accept; seq_len [B] in/out;
+ *   commit_pos [B][max_depth+1]; feat_cache / tree_feat may be NULL (feat_dim 0).
+ * Source and destination never overlap (tree K/V is its own buffer). */
+int eagle_kv_commit(const eagle_commit_desc* d, void* const* k_cache_layers, void* const* v_cache_layers,
+                    const void* const* tree_k_layers, const void* const* tree_v_layers,
+                    const int32_t* n_acc, const int32_t* path, int32_t* seq_len, int32_t* commit_pos,
+                    void* feat_cache, const void* tree_feat, uint32_t* status, void* stream);
+
+/* ---------------------------------------------------------------- misc */
+/* Scratch bytes a call needs (which = EAGLE_WS_*, desc = the matching desc); 0 on a
+ * bad argument. */
+size_t eagle_workspace_size(int which, const void* desc);
+
+/* A static string naming a status code. */
+const char* eagle_status_string(int status);
+
+/* Library version string. */
+const char* eagle_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* EAGLE_H */

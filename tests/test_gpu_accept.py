@@ -1,0 +1,158 @@
+"""GPU parity: eagle_accept against the oracle's acceptance.
+
+Trees come from the oracle's builder on the synthetic path-keyed LM; target (and
+draft) rows are that LM's rows at the tree's nodes; uniforms are seeded.  The GPU
+must reproduce the oracle's accepted lengths, paths and emitted tokens bit for
+bit, except for requests where either side reports a near-tie (|u - p/q| < 1e-5,
+or a draw within 1e-5 of a bin edge), which are counted.  A GPU-side chi-square
+check repeats the losslessness test on the kernels themselves.
+"""
+import numpy as np
+import pytest
+import torch
+from scipy.special import softmax
+
+import oracle
+from eagle_speculative_decoding_tree_gb300 import binding as B
+from eagle_speculative_decoding_tree_gb300 import synth
+from gpu_helpers import dev
+from spec_helpers import OracleDynamicBuilder, OracleStaticBuilder, build_tree_bigram, chisquare_pvalue, \
+    drive_tree_build, node_hashes
+
+pytestmark = pytest.mark.gpu
+
+W = synth.WORKLOADS
+
+
+def gpu_accept(w, tree, target, draft, ua, uf, proposal, T, max_depth):
+    Bn, R = tree["tokens"].shape
+    dt = B.EAGLE_F32 if w.dtype == "f32" else B.EAGLE_BF16
+    desc = B.AcceptDesc(Bn, R, target.shape[-1], float(T), proposal, dt, max_depth)
+    ws = torch.zeros(B.workspace_size(B.EAGLE_WS_ACCEPT, desc), dtype=torch.uint8, device="cuda")
+    out = B.AcceptBuffers.allocate(Bn, max_depth)
+    i32 = lambda a: torch.from_numpy(np.ascontiguousarray(a, np.int32)).cuda()
+    B.eagle_accept(desc, dev(target, w.dtype), None if draft is None else dev(draft, w.dtype), i32(tree["tokens"]),
+                   i32(tree["parent"]), torch.from_numpy(ua).cuda(), torch.from_numpy(uf).cuda(), out, ws)
+    torch.cuda.synchronize()
+    return {k: getattr(out, k).cpu().numpy() for k in ("n_acc", "path", "out_tok", "near_tie", "status")}
+
+
+def compare(g, r, max_near):
+    near = (g["near_tie"] > 0) | (r["near_tie"] > 0)
+    ok = ~near
+    for key in ("n_acc", "path", "out_tok"):
+        bad = np.nonzero(ok & np.any(np.atleast_2d(g[key].reshape(len(near), -1) != r[key].reshape(len(near), -1)),
+                                     axis=1))[0]
+        assert len(bad) == 0, f"{key} differs for requests {bad[:8]}: gpu {g[key][bad[:2]]} oracle {r[key][bad[:2]]}"
+    assert g["status"][0] == 0
+    assert near.sum() <= max_near, near.sum()
+    return int(near.sum())
+
+
+def case(w, batch, seed, T=None, proposal=None):
+    T = w.temperature if T is None else T
+    proposal = proposal if proposal is not None else (oracle.SAMPLED if w.proposal == "sampled" else oracle.DELTA)
+    lm = synth.hash_lm(w)
+    root_tok = synth.rng(w.config_id, 41, seed).integers(0, w.vocab, batch).astype(np.int32)
+    root_h = [synth.root_hash(w.config_id, b, 100 + seed) for b in range(batch)]
+    seq_len = synth.prefix_lengths(w, batch)
+    if w.tree_mode == "dynamic":
+        bld = OracleDynamicBuilder(batch, w.vocab, w.depth, w.top_k, w.total_tokens)
+        depth = w.depth
+    else:
+        par = synth.static_parents(w.static_choices)
+        bld = OracleStaticBuilder(batch, w.vocab, par, w.tree_mode == "static_sampled", T if T > 0 else 1.0)
+        depth = int(max(len(c) for c in w.static_choices))
+    ud = synth.uniforms(synth.rng(w.config_id, 42, seed), (batch, w.rows))
+    tree = drive_tree_build(bld, lm, depth, root_tok, root_h, seq_len, u_draft=ud)
+    hs = node_hashes(tree, root_h)
+    target = synth.as_dtype_bytes(np.stack([lm.rows(hs[b], "target") for b in range(batch)]), w.dtype)
+    draft = synth.as_dtype_bytes(np.stack([lm.rows(hs[b], "draft") for b in range(batch)]), w.dtype) \
+        if proposal == oracle.SAMPLED else None
+    ua = synth.uniforms(synth.rng(w.config_id, 43, seed), (batch, tree["tokens"].shape[1]))
+    uf = synth.uniforms(synth.rng(w.config_id, 44, seed), (batch,))
+    max_depth = int(tree["depth"].max())
+    r = oracle.accept(target, tree["tokens"], tree["parent"], ua, uf, T, proposal, max_depth + 1, draft=draft)
+    g = gpu_accept(w, tree, target, draft, ua, uf, proposal, T, max_depth)
+    return g, r
+
+
+@pytest.mark.parametrize("name,batch,T", [
+    ("vicuna7b", 8, 0.0), ("vicuna7b", 8, 1.0), ("llama8b", 8, 1.0), ("tiny", 64, 1.0), ("long128k", 8, 1.0),
+])
+def test_accept_workloads(name, batch, T):
+    g, r = case(W[name], batch, seed=1, T=T)
+    compare(g, r, max_near=max(1, batch // 8))
+
+
+def test_accept_concurrency_batch32():
+    w = W["concurrency"].with_(batch=32, vocab=32768)
+    g, r = case(w, 32, seed=2)
+    compare(g, r, max_near=4)
+
+
+def test_accept_temperature_07_delta():
+    w = W["vicuna7b"].with_(vocab=5000, temperature=0.7)
+    g, r = case(w, 32, seed=3)
+    compare(g, r, max_near=4)
+
+
+def test_accept_sampled_static_multi_sibling_residuals():
+    w = W["tiny"].with_(vocab=5000, dtype="bf16", temperature=0.8, draft_sigma=2.0)
+    g, r = case(w, 64, seed=4)
+    compare(g, r, max_near=8)
+    assert (r["n_acc"] < 3).sum() > 10  # rejections (and residual passes) happened
+
+
+def test_accept_delta_with_duplicate_siblings():
+    # children drawn with replacement, judged as point-mass proposals: a duplicate of a
+    # rejected token has zero residual mass and must be rejected too
+    w = W["tiny"].with_(vocab=40, dtype="f32", temperature=1.0, sigma=1.0)
+    g, r = case(w, 128, seed=5, proposal=oracle.DELTA)
+    compare(g, r, max_near=8)
+
+
+def test_accept_gpu_chisquare_first_token():
+    """Losslessness on the GPU: 2e5 independent requests in one call, first emitted
+    token against the target distribution (dynamic top-k tree, point-mass proposals)."""
+    V, n = 16, 200_000
+    lm = synth.BigramLM(V, sigma=1.5, draft_sigma=0.7, seed_key=1)
+    root = 3
+    tree = build_tree_bigram(lm, np.array([root], np.int32), "dynamic", depth=3, top_k=4, total_tokens=10)
+    tree = {k: np.broadcast_to(v, (n,) + v.shape[1:]).copy() for k, v in tree.items()}
+    target = lm.target[tree["tokens"]]
+    g = synth.rng(0, 7777)
+    ua, uf = synth.uniforms(g, (n, 11)), synth.uniforms(g, (n,))
+    w = synth.WORKLOADS["tiny"]
+    out = gpu_accept(w, tree, target, None, ua, uf, oracle.DELTA, 1.0, int(tree["depth"].max()))
+    c1 = np.bincount(out["out_tok"][:, 0], minlength=V)
+    p = softmax(lm.target[root].astype(np.float64))
+    assert chisquare_pvalue(c1, p) > 1e-3
+
+
+def test_accept_gpu_chisquare_sampled_static():
+    V, n = 16, 100_000
+    lm = synth.BigramLM(V, sigma=1.5, draft_sigma=0.7, seed_key=1)
+    g = synth.rng(0, 7778)
+    par = synth.static_parents(synth.TINY_STATIC_CHOICES)
+    tree = build_tree_bigram(lm, np.full(n, 3, np.int32), "static_sampled", static_parent=par,
+                             u_draft=synth.uniforms(g, (n, 11)))
+    target, draft = lm.target[tree["tokens"]], lm.draft[tree["tokens"]]
+    ua, uf = synth.uniforms(g, (n, 11)), synth.uniforms(g, (n,))
+    out = gpu_accept(synth.WORKLOADS["tiny"], tree, target, draft, ua, uf, oracle.SAMPLED, 1.0, 3)
+    c1 = np.bincount(out["out_tok"][:, 0], minlength=V)
+    p = softmax(lm.target[3].astype(np.float64))
+    assert chisquare_pvalue(c1, p) > 1e-3
+    r = oracle.accept(target[:2000], tree["tokens"][:2000], tree["parent"][:2000], ua[:2000], uf[:2000], 1.0,
+                      oracle.SAMPLED, 4, draft=draft[:2000])
+    compare({k: v[:2000] if k != "status" else v for k, v in out.items()}, r, max_near=4)
+
+
+def test_accept_bad_token_is_flagged_and_rejected():
+    w = W["tiny"].with_(vocab=50, dtype="f32")
+    tree = {"tokens": np.array([[1, 60, 3]], np.int32), "parent": np.array([[-1, 0, 0]], np.int32)}
+    target = np.zeros((1, 3, 50), np.float32)
+    target[0, 0, 3] = 10.0
+    g = gpu_accept(w, tree, target, None, np.zeros((1, 3), np.float32), np.zeros(1, np.float32), oracle.DELTA, 1.0, 1)
+    assert g["status"][0] & B.EAGLE_STATUS_BAD_TOKEN
+    assert g["n_acc"][0] == 1 and g["out_tok"][0, 0] == 3
