@@ -30,7 +30,7 @@ int num_sms() {
 int check_tree_desc(const eagle_tree_desc* d) {
   if (!d) return EAGLE_ERR_INVALID_ARG;
   if (d->batch < 1 || d->vocab < 1) return EAGLE_ERR_INVALID_ARG;
-  if (!dtype_ok(d->dtype)) return EAGLE_ERR_UNSUPPORTED;
+  if (!dtype_ok(d->dtype) || d->vocab > kMaxVocabTiles * kVocabChunk) return EAGLE_ERR_UNSUPPORTED;
   if (d->mode == EAGLE_TREE_DYNAMIC) {
     if (d->depth < 1 || d->top_k < 1 || d->total_tokens < 1) return EAGLE_ERR_INVALID_ARG;
     if (d->depth > kMaxDepth || d->top_k > kMaxTopK || d->top_k > d->vocab) return EAGLE_ERR_UNSUPPORTED;
@@ -67,6 +67,7 @@ int check_attn_desc(const eagle_attn_desc* d) {
     return EAGLE_ERR_INVALID_ARG;
   if (d->num_splits < 0 || !(d->scale > 0.f) || !isfinite(d->scale)) return EAGLE_ERR_INVALID_ARG;
   if (d->n_q_heads % d->n_kv_heads) return EAGLE_ERR_UNSUPPORTED;
+  if (static_cast<long long>(d->batch) * d->n_kv_heads > 65535) return EAGLE_ERR_UNSUPPORTED;  // grid z
   if (d->head_dim != 64 && d->head_dim != 128) return EAGLE_ERR_UNSUPPORTED;
   if (d->rows > kMaxRows || !dtype_ok(d->dtype) || !dtype_ok(d->out_dtype)) return EAGLE_ERR_UNSUPPORTED;
   if (d->dtype == EAGLE_F32 && d->out_dtype != EAGLE_F32) return EAGLE_ERR_UNSUPPORTED;
@@ -80,6 +81,7 @@ int check_accept_desc(const eagle_accept_desc* d) {
   if (!(d->temperature >= 0.f) || !isfinite(d->temperature)) return EAGLE_ERR_INVALID_ARG;
   if (d->proposal != EAGLE_PROPOSAL_DELTA && d->proposal != EAGLE_PROPOSAL_SAMPLED) return EAGLE_ERR_INVALID_ARG;
   if (d->rows > kMaxRows || d->max_depth >= kMaxRows || !dtype_ok(d->dtype)) return EAGLE_ERR_UNSUPPORTED;
+  if (d->vocab > kMaxVocabTiles * kVocabChunk) return EAGLE_ERR_UNSUPPORTED;
   return EAGLE_OK;
 }
 

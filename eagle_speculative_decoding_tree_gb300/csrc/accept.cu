@@ -11,7 +11,7 @@
 // ones.
 //
 // Kernels
-//   accept_rowstats_kernel  one CTA per (4096-token chunk, tree row, source): chunk
+//   accept_rowstats_kernel  one CTA per (tree row, 4096-token chunk, source): chunk
 //                           max, sum exp((x - m) / T) and argmax -- a single
 //                           streaming pass over every target (and draft) row.
 //   accept_walk_kernel      one CTA per request: merges the chunk statistics of the
@@ -19,6 +19,11 @@
 //                           token by inverse CDF.  Point-mass residuals only zero a
 //                           few tokens, so the draw skips to the chunk that holds
 //                           the crossing; drawn-proposal residuals take full passes.
+//
+// Precision: weights are expf((x - m) / T) in fp32; per-thread sums are compensated
+// (Neumaier) and every sum across threads, chunks or tiles is taken in double, so a
+// running sum is within about 2e-7 of the total mass of its exact value.  Draws are
+// reported as near-ties when they land within 1e-7 of the mass of a bin edge.
 #include <limits.h>
 
 #include "common.cuh"
@@ -29,12 +34,14 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kPer = kVocabChunk / kThreads;  // 16 elements per thread per tile
+constexpr double kIcdfNearEps = 1e-7;
 
 struct RowPart {
   float m;    // chunk max
-  float s;    // sum exp2((x - m) * cT)
   float av;   // chunk argmax value
   int ai;     // chunk argmax index (lowest on ties)
+  int pad;
+  double s;   // sum exp((x - m) / T)
 };
 
 struct WalkArgs {
@@ -50,89 +57,93 @@ struct WalkArgs {
 
 __global__ void __launch_bounds__(kThreads) accept_rowstats_kernel(const AcceptPlan p, const void* target,
                                                                    const void* draft, RowPart* part) {
-  const int c = blockIdx.x, row = blockIdx.y, src = blockIdx.z;
+  const int row = blockIdx.x, c = blockIdx.y, src = blockIdx.z;
+  const int rows = gridDim.x, n_chunks = gridDim.y;
   const void* base = src == 0 ? target : draft;
   const size_t off = static_cast<size_t>(row) * p.V;
   const int lo = c * kVocabChunk, hi = min(p.V, lo + kVocabChunk);
-  const float cT = kLog2e / (p.temperature > 0.f ? p.temperature : 1.f);
-  float m = -INFINITY, s = 0.f, av = -INFINITY;
+  const float invT = 1.f / (p.temperature > 0.f ? p.temperature : 1.f);
+  float m = -INFINITY, av = -INFINITY;
   int ai = INT_MAX;
+  CSum acc;
   for (int v = lo + threadIdx.x; v < hi; v += kThreads) {
     const float x = load_elem(base, off + v, p.dtype);
     if (x > m) {
-      if (m != -INFINITY) s *= exp2f((m - x) * cT);
+      if (m != -INFINITY) acc.scale(expf((m - x) * invT));
       m = x;
     }
-    s += exp2f((x - m) * cT);
+    acc.add(expf((x - m) * invT));
     if (before(x, v, av, ai)) {
       av = x;
       ai = v;
     }
   }
+  // warp max / argmax, then the sums rescaled to the warp max, in double
+  double s = acc.total();
+  float M = m;
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
-    const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
-    const float s2 = __shfl_xor_sync(0xffffffffu, s, o);
+    M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
     const float v2 = __shfl_xor_sync(0xffffffffu, av, o);
     const int i2 = __shfl_xor_sync(0xffffffffu, ai, o);
-    const float M = fmaxf(m, m2);
-    if (M != -INFINITY) s = s * exp2f((m - M) * cT) + s2 * exp2f((m2 - M) * cT);
-    m = M;
     if (before(v2, i2, av, ai)) {
       av = v2;
       ai = i2;
     }
   }
+  s = (m == -INFINITY) ? 0.0 : s * static_cast<double>(expf((m - M) * invT));
+  s = warp_sum_d(s);
   __shared__ RowPart wp[kThreads / 32];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (lane == 0) wp[warp] = RowPart{m, s, av, ai};
+  if (lane == 0) wp[warp] = RowPart{M, av, ai, 0, s};
   __syncthreads();
   if (threadIdx.x == 0) {
     RowPart r = wp[0];
-    for (int w = 1; w < kThreads / 32; ++w) {
-      const RowPart q = wp[w];
-      const float M = fmaxf(r.m, q.m);
-      if (M != -INFINITY) r.s = r.s * exp2f((r.m - M) * cT) + q.s * exp2f((q.m - M) * cT);
-      r.m = M;
-      if (before(q.av, q.ai, r.av, r.ai)) {
-        r.av = q.av;
-        r.ai = q.ai;
+    for (int w = 1; w < kThreads / 32; ++w) r.m = fmaxf(r.m, wp[w].m);
+    double t = 0.0;
+    for (int w = 0; w < kThreads / 32; ++w) {
+      if (wp[w].m != -INFINITY) t += wp[w].s * static_cast<double>(expf((wp[w].m - r.m) * invT));
+      if (w > 0 && before(wp[w].av, wp[w].ai, r.av, r.ai)) {
+        r.av = wp[w].av;
+        r.ai = wp[w].ai;
       }
     }
-    part[(static_cast<size_t>(src) * gridDim.y + row) * gridDim.x + c] = r;
+    r.s = t;
+    part[(static_cast<size_t>(src) * rows + row) * n_chunks + c] = r;
   }
 }
 
 // ------------------------------------------------------------------ block helpers
 struct DrawScratch {
-  float wsum[kThreads / 32];
+  double wsum[kThreads / 32];
   int found;
   int last;
-  float prev_edge, next_edge, total;
+  double prev_edge, next_edge, total;
 };
 
-// One tile of an inverse-CDF draw: elements [lo, hi) (hi - lo <= 4096), running sum
-// `base` before lo.  Sets ds.found to the first index whose running sum exceeds
-// `target` (INT_MAX if none), ds.last to the last index with positive weight
-// (-1 if none) and ds.total to the tile's weight sum.
+// One tile of an inverse-CDF draw: elements [lo, hi) (hi - lo <= 4096), running mass
+// `base` before lo.  Each thread takes 16 consecutive elements; its running sum and
+// the thread offsets are taken in double.  Sets ds.found to the first index whose running mass
+// exceeds `target` (INT_MAX if none), ds.last to the last index with positive
+// weight (-1 if none) and ds.total to the tile's mass.
 template <class WF>
-__device__ void block_draw_tile(int lo, int hi, float base, float target, WF wf, DrawScratch& ds) {
+__device__ void block_draw_tile(int lo, int hi, double base, double target, WF wf, DrawScratch& ds) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int a0 = lo + threadIdx.x * kPer;
   float w[kPer];
-  float mine = 0.f;
+  double my = 0.0;
   int last = -1;
 #pragma unroll
   for (int e = 0; e < kPer; ++e) {
     const int v = a0 + e;
     w[e] = (v < hi) ? wf(v) : 0.f;
-    mine += w[e];
+    my += static_cast<double>(w[e]);
     if (w[e] > 0.f) last = v;
   }
-  float incl = mine;
+  double incl = my;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    const float t = __shfl_up_sync(0xffffffffu, incl, o);
+    const double t = __shfl_up_sync(0xffffffffu, incl, o);
     if (lane >= o) incl += t;
   }
   __syncthreads();  // earlier readers of ds are done
@@ -142,23 +153,27 @@ __device__ void block_draw_tile(int lo, int hi, float base, float target, WF wf,
   }
   if (lane == 31) ds.wsum[warp] = incl;
   __syncthreads();
-  float wbase = 0.f, tot = 0.f;
+  double wbase = 0.0, tot = 0.0;
   for (int i = 0; i < kThreads / 32; ++i) {
     if (i < warp) wbase += ds.wsum[i];
     tot += ds.wsum[i];
   }
-  float cum = base + wbase + incl - mine;
+  const double tbase = base + wbase + incl - my;  // mass before this thread's first element
+  const double rel = target - tbase;
   int found = INT_MAX;
-  float pe = 0.f, ne = 0.f;
+  double pe = 0.0, ne = 0.0;
+  {
+    double cum = 0.0;
 #pragma unroll
-  for (int e = 0; e < kPer; ++e) {
-    const float nc = cum + w[e];
-    if (found == INT_MAX && a0 + e < hi && nc > target) {
-      found = a0 + e;
-      pe = cum;
-      ne = nc;
+    for (int e = 0; e < kPer; ++e) {
+      const double nc = cum + static_cast<double>(w[e]);
+      if (found == INT_MAX && a0 + e < hi && w[e] > 0.f && nc > rel) {
+        found = a0 + e;
+        pe = tbase + cum;
+        ne = tbase + nc;
+      }
+      cum = nc;
     }
-    cum = nc;
   }
   if (found != INT_MAX) atomicMin(&ds.found, found);
   if (last >= 0) atomicMax(&ds.last, last);
@@ -171,17 +186,17 @@ __device__ void block_draw_tile(int lo, int hi, float base, float target, WF wf,
   __syncthreads();
 }
 
-// Block sum of wf(v) over [0, V).
+// Block sum of wf(v) over [lo, hi): compensated per thread, double across threads.
 template <class WF>
-__device__ float block_sum(int V, WF wf, float* red) {
-  float s = 0.f;
-  for (int v = threadIdx.x; v < V; v += kThreads) s += wf(v);
-  s = warp_sum(s);
+__device__ double block_sum(int lo, int hi, WF wf, double* red) {
+  CSum acc;
+  for (int v = lo + threadIdx.x; v < hi; v += kThreads) acc.add(wf(v));
+  double s = warp_sum_d(acc.total());
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   __syncthreads();
   if (lane == 0) red[warp] = s;
   __syncthreads();
-  float t = 0.f;
+  double t = 0.0;
   for (int i = 0; i < kThreads / 32; ++i) t += red[i];
   __syncthreads();
   return t;
@@ -192,23 +207,27 @@ __global__ void __launch_bounds__(kThreads) accept_walk_kernel(const AcceptPlan 
   const int R = p.R, V = p.V, C = p.n_chunks;
   const bool greedy = !(p.temperature > 0.f);
   const bool sampled = !greedy && p.proposal == EAGLE_PROPOSAL_SAMPLED;
-  const float cT = kLog2e / (greedy ? 1.f : p.temperature);
+  const float invT = 1.f / (greedy ? 1.f : p.temperature);
   const int32_t* tok = a.tokens + static_cast<size_t>(b) * R;
   const int32_t* par = a.parent + static_cast<size_t>(b) * R;
   const int maxp = p.max_depth + 1;
 
   __shared__ int s_path[kMaxRows + 1];
   __shared__ int s_kids[kMaxRows];
-  __shared__ int s_nk, s_len, s_cur, s_next, s_emit, s_done, s_near;
+  __shared__ int s_nk, s_len, s_cur, s_next, s_emit, s_done, s_near, s_flag;
   __shared__ unsigned s_status;
   __shared__ int s_rej[kMaxRows];
   __shared__ int s_nrej;
-  __shared__ float s_Z[kMaxRows];
+  __shared__ double s_Z[kMaxRows];
   __shared__ int s_nz;
-  __shared__ float s_M, s_Zt, s_Mq, s_Zq, s_rejmass;
+  __shared__ float s_M, s_Mq;
+  __shared__ double s_Zt, s_Zq, s_rejmass;
   __shared__ int s_amax;
-  __shared__ float red[kThreads / 32];
+  __shared__ double red[kThreads / 32];
   __shared__ DrawScratch ds;
+  __shared__ int s_chunk, s_fallback;
+  __shared__ double s_base, s_W;
+  __shared__ double s_tile[kMaxVocabTiles];
 
   if (threadIdx.x == 0) {
     s_len = 1;
@@ -229,7 +248,7 @@ __global__ void __launch_bounds__(kThreads) accept_walk_kernel(const AcceptPlan 
       int nk = 0;
       for (int c = cur + 1; c < R; ++c) {
         const int pc = par[c];
-        if (pc >= c || pc < -1 || (c > 0 && pc < 0)) s_status |= EAGLE_STATUS_BAD_TREE;
+        if (pc >= c || pc < 0) s_status |= EAGLE_STATUS_BAD_TREE;
         if (pc == cur) s_kids[nk++] = c;
       }
       s_nk = nk;
@@ -244,9 +263,9 @@ __global__ void __launch_bounds__(kThreads) accept_walk_kernel(const AcceptPlan 
           ai = rp[c].ai;
         }
       }
-      float Z = 0.f;
+      double Z = 0.0;
       for (int c = 0; c < C; ++c)
-        if (rp[c].m != -INFINITY) Z += rp[c].s * exp2f((rp[c].m - M) * cT);
+        if (rp[c].m != -INFINITY) Z += rp[c].s * static_cast<double>(expf((rp[c].m - M) * invT));
       s_M = M;
       s_Zt = Z;
       s_amax = ai;
@@ -254,28 +273,30 @@ __global__ void __launch_bounds__(kThreads) accept_walk_kernel(const AcceptPlan 
         const RowPart* dp = a.part + (static_cast<size_t>(p.B) * R + row_base + cur) * C;
         float Mq = -INFINITY;
         for (int c = 0; c < C; ++c) Mq = fmaxf(Mq, dp[c].m);
-        float Zq = 0.f;
+        double Zq = 0.0;
         for (int c = 0; c < C; ++c)
-          if (dp[c].m != -INFINITY) Zq += dp[c].s * exp2f((dp[c].m - Mq) * cT);
+          if (dp[c].m != -INFINITY) Zq += dp[c].s * static_cast<double>(expf((dp[c].m - Mq) * invT));
         s_Mq = Mq;
         s_Zq = Zq;
       }
       s_next = -1;
       s_nrej = 0;
       s_nz = 0;
-      s_rejmass = 0.f;
+      s_rejmass = 0.0;
     }
     __syncthreads();
-    const float M = s_M, Zt = s_Zt;
-    const float Mq = s_Mq, Zq = s_Zq;
-    auto p_of = [&](int v) { return exp2f((load_elem(a.target, xrow + v, p.dtype) - M) * cT) / Zt; };
-    auto q_of = [&](int v) { return exp2f((load_elem(a.draft, xrow + v, p.dtype) - Mq) * cT) / Zq; };
+    const float M = s_M, Mq = s_Mq;
+    const float invZt = static_cast<float>(1.0 / s_Zt);
+    const float invZq = sampled ? static_cast<float>(1.0 / s_Zq) : 0.f;
+    auto w_target = [&](int v) { return expf((load_elem(a.target, xrow + v, p.dtype) - M) * invT); };
+    auto p_of = [&](int v) { return w_target(v) * invZt; };
+    auto q_of = [&](int v) { return expf((load_elem(a.draft, xrow + v, p.dtype) - Mq) * invT) * invZq; };
     // residual chain for drawn proposals: p_j = max(0, p_{j-1} - q) / Z_j
     auto pres_of = [&](int v, int nz) {
       float pv = p_of(v);
       if (nz == 0) return pv;
       const float qv = q_of(v);
-      for (int i = 0; i < nz; ++i) pv = fmaxf(pv - qv, 0.f) / s_Z[i];
+      for (int i = 0; i < nz; ++i) pv = static_cast<float>(fmaxf(pv - qv, 0.f) / s_Z[i]);
       return pv;
     };
 
@@ -305,11 +326,11 @@ __global__ void __launch_bounds__(kThreads) accept_walk_kernel(const AcceptPlan 
           }
           bool dup = false;
           for (int r = 0; r < s_nrej; ++r) dup |= (s_rej[r] == d);
-          const float pd = dup ? 0.f : p_of(d);
-          const float denom = 1.f - s_rejmass;
-          const float ratio = denom > 0.f ? pd / denom : 0.f;
-          const float u = a.u_accept[row_base + c];
-          if (fabsf(u - ratio) < kNearTieEps) s_near = 1;
+          const double pd = dup ? 0.0 : static_cast<double>(w_target(d)) / s_Zt;
+          const double denom = 1.0 - s_rejmass;
+          const double ratio = denom > 0.0 ? pd / denom : 0.0;
+          const double u = a.u_accept[row_base + c];
+          if (fabs(u - ratio) < static_cast<double>(kNearTieEps)) s_near = 1;
           if (u < ratio) {
             s_next = c;
             break;
@@ -328,26 +349,26 @@ __global__ void __launch_bounds__(kThreads) accept_walk_kernel(const AcceptPlan 
         const int nz = s_nz;
         if (threadIdx.x == 0) {
           const int d = tok[c];
-          s_rej[0] = 0;  // flag: 1 = rejected, residual needed
+          s_flag = 0;  // 1: rejected, residual needed
           if (d < 0 || d >= V) {
             s_status |= EAGLE_STATUS_BAD_TOKEN;
           } else {
-            const float qd = q_of(d);
-            const float pd = pres_of(d, nz);
-            const float ratio = qd > 0.f ? pd / qd : INFINITY;
-            const float u = a.u_accept[row_base + c];
-            if (qd > 0.f && fabsf(u - ratio) < kNearTieEps) s_near = 1;
-            if (!(qd > 0.f) || u < ratio)
+            const double qd = q_of(d);
+            const double pd = pres_of(d, nz);
+            const double ratio = qd > 0.0 ? pd / qd : INFINITY;
+            const double u = a.u_accept[row_base + c];
+            if (qd > 0.0 && fabs(u - ratio) < static_cast<double>(kNearTieEps)) s_near = 1;
+            if (!(qd > 0.0) || u < ratio)
               s_next = c;
             else
-              s_rej[0] = 1;
+              s_flag = 1;
           }
         }
         __syncthreads();
         if (s_next >= 0) break;
-        if (s_rej[0]) {
-          const float z = block_sum(V, [&](int v) { return fmaxf(pres_of(v, nz) - q_of(v), 0.f); }, red);
-          if (threadIdx.x == 0 && z > 0.f) s_Z[s_nz++] = z;
+        if (s_flag) {
+          const double z = block_sum(0, V, [&](int v) { return fmaxf(pres_of(v, nz) - q_of(v), 0.f); }, red);
+          if (threadIdx.x == 0 && z > 0.0) s_Z[s_nz++] = z;
         }
         __syncthreads();
       }
@@ -370,33 +391,47 @@ __global__ void __launch_bounds__(kThreads) accept_walk_kernel(const AcceptPlan 
     if (s_done) break;
 
     // ---- draw the emitted token from the (residual) target distribution
-    const float u = a.u_final[b];
+    const double u = a.u_final[b];
     if (sampled && s_nz > 0) {
+      // residual of drawn proposals: a mass per 4096-token tile, then the crossing
+      // tile is scanned element by element
       const int nz = s_nz;
-      // full passes, tile by tile; W = the residual's sum, taken in the same pass order
-      float W = 0.f;
-      for (int lo = 0; lo < V; lo += kVocabChunk) {
-        block_draw_tile(lo, min(V, lo + kVocabChunk), W, INFINITY, [&](int v) { return pres_of(v, nz); }, ds);
-        W += ds.total;
-      }
-      const float target = u * W;
-      float run = 0.f;
-      int emit = -1, last = -1;
-      for (int lo = 0; lo < V; lo += kVocabChunk) {
-        block_draw_tile(lo, min(V, lo + kVocabChunk), run, target, [&](int v) { return pres_of(v, nz); }, ds);
-        if (ds.last >= 0) last = ds.last;
-        if (ds.found != INT_MAX) {
-          emit = ds.found;
-          if (threadIdx.x == 0 &&
-              (target - ds.prev_edge < kNearTieEps * W || ds.next_edge - target < kNearTieEps * W))
-            s_near = 1;
-          break;
-        }
-        run += ds.total;
+      auto wres = [&](int v) { return pres_of(v, nz); };
+      const int n_tiles = (V + kVocabChunk - 1) / kVocabChunk;
+      for (int t = 0; t < n_tiles; ++t) {
+        const double m = block_sum(t * kVocabChunk, min(V, (t + 1) * kVocabChunk), wres, red);
+        if (threadIdx.x == 0) s_tile[t] = m;
       }
       if (threadIdx.x == 0) {
-        if (emit < 0) {
-          emit = last < 0 ? 0 : last;
+        double W = 0.0;
+        for (int t = 0; t < n_tiles; ++t) W += s_tile[t];
+        const double target = u * W;
+        double cum = 0.0, bs = 0.0;
+        int ts = -1, lastt = -1;
+        for (int t = 0; t < n_tiles; ++t) {
+          if (s_tile[t] > 0.0) lastt = t;
+          if (ts < 0 && cum + s_tile[t] > target) {
+            ts = t;
+            bs = cum;
+          }
+          cum += s_tile[t];
+        }
+        s_fallback = ts < 0;
+        if (ts < 0) ts = lastt < 0 ? 0 : lastt;
+        s_chunk = ts;
+        s_base = bs;
+        s_W = W;
+      }
+      __syncthreads();
+      const int lo = s_chunk * kVocabChunk;
+      const double W = s_W, target = s_fallback ? INFINITY : u * W;
+      block_draw_tile(lo, min(V, lo + kVocabChunk), s_base, target, wres, ds);
+      if (threadIdx.x == 0) {
+        int emit = ds.found;
+        if (emit == INT_MAX) {
+          emit = ds.last < 0 ? lo : ds.last;
+          s_near = 1;
+        } else if (target - ds.prev_edge < kIcdfNearEps * W || ds.next_edge - target < kIcdfNearEps * W) {
           s_near = 1;
         }
         s_emit = emit;
@@ -407,26 +442,22 @@ __global__ void __launch_bounds__(kThreads) accept_walk_kernel(const AcceptPlan 
       auto w_of = [&](int v) {
         for (int r = 0; r < nrej; ++r)
           if (s_rej[r] == v) return 0.f;
-        return exp2f((load_elem(a.target, xrow + v, p.dtype) - M) * cT);
+        return w_target(v);
       };
-      __shared__ int s_chunk, s_fallback;
-      __shared__ float s_base, s_W;
       if (threadIdx.x == 0) {
         const RowPart* rp = a.part + (row_base + cur) * C;
-        float W = 0.f;
+        double W = 0.0;
         for (int c = 0; c < C; ++c)
-          if (rp[c].m != -INFINITY) W += rp[c].s * exp2f((rp[c].m - M) * cT);
-        for (int r = 0; r < nrej; ++r) W -= exp2f((load_elem(a.target, xrow + s_rej[r], p.dtype) - M) * cT);
-        const float target = u * W;
-        float cum = 0.f;
+          if (rp[c].m != -INFINITY) W += rp[c].s * static_cast<double>(expf((rp[c].m - M) * invT));
+        for (int r = 0; r < nrej; ++r) W -= static_cast<double>(w_target(s_rej[r]));
+        const double target = u * W;
+        double cum = 0.0, bs = 0.0;
         int cs = -1, lastc = -1;
-        float bs = 0.f;
         for (int c = 0; c < C; ++c) {
-          float wc = (rp[c].m == -INFINITY) ? 0.f : rp[c].s * exp2f((rp[c].m - M) * cT);
+          double wc = (rp[c].m == -INFINITY) ? 0.0 : rp[c].s * static_cast<double>(expf((rp[c].m - M) * invT));
           for (int r = 0; r < nrej; ++r)
-            if (s_rej[r] / kVocabChunk == c)
-              wc -= exp2f((load_elem(a.target, xrow + s_rej[r], p.dtype) - M) * cT);
-          if (wc > 0.f) lastc = c;
+            if (s_rej[r] / kVocabChunk == c) wc -= static_cast<double>(w_target(s_rej[r]));
+          if (wc > 0.0) lastc = c;
           if (cs < 0 && cum + wc > target) {
             cs = c;
             bs = cum;
@@ -441,14 +472,14 @@ __global__ void __launch_bounds__(kThreads) accept_walk_kernel(const AcceptPlan 
       }
       __syncthreads();
       const int lo = s_chunk * kVocabChunk;
-      const float W = s_W, target = s_fallback ? INFINITY : u * W;
+      const double W = s_W, target = s_fallback ? INFINITY : u * W;
       block_draw_tile(lo, min(V, lo + kVocabChunk), s_base, target, w_of, ds);
       if (threadIdx.x == 0) {
         int emit = ds.found;
         if (emit == INT_MAX) {
           emit = ds.last < 0 ? lo : ds.last;
           s_near = 1;
-        } else if (target - ds.prev_edge < kNearTieEps * W || ds.next_edge - target < kNearTieEps * W) {
+        } else if (target - ds.prev_edge < kIcdfNearEps * W || ds.next_edge - target < kIcdfNearEps * W) {
           s_near = 1;
         }
         s_emit = emit;
@@ -494,7 +525,7 @@ cudaError_t launch_accept(const AcceptPlan& p, const void* target, const void* d
                           const int32_t* parent, const float* u_accept, const float* u_final,
                           const eagle_accept_out& out, void* ws, cudaStream_t s) {
   RowPart* part = reinterpret_cast<RowPart*>(static_cast<uint8_t*>(ws) + p.off_part);
-  dim3 grid(p.n_chunks, p.B * p.R, p.n_sources);
+  dim3 grid(p.B * p.R, p.n_chunks, p.n_sources);
   accept_rowstats_kernel<<<grid, kThreads, 0, s>>>(p, target, draft, part);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;

@@ -9,7 +9,7 @@
 // next root; its K/V comes from the next verify pass.
 //
 // Kernels
-//   kv_commit_copy_kernel      one CTA per (path position m, request, layer): 16-byte
+//   kv_commit_copy_kernel      one CTA per (request, path position m, layer): 16-byte
 //                              vector copies of the K and V rows of every KV head.
 //   kv_commit_finalize_kernel  one thread per request: commit positions, seq_len
 //                              update, cache-full check.  A separate launch so the
@@ -31,7 +31,7 @@ __global__ void __launch_bounds__(128) kv_commit_copy_kernel(const eagle_commit_
                                                              const int32_t* n_acc, const int32_t* path,
                                                              const int32_t* seq_len, void* feat_cache,
                                                              const void* tree_feat) {
-  const int m = blockIdx.x, b = blockIdx.y, l = blockIdx.z;
+  const int b = blockIdx.x, m = blockIdx.y, l = blockIdx.z;
   if (!commit_ok(d, n_acc, seq_len, b) || m > n_acc[b]) return;
   const int node = path[static_cast<size_t>(b) * (d.max_depth + 1) + m];
   if (node < 0 || node >= d.rows) return;  // flagged by the finalize kernel
@@ -91,7 +91,7 @@ __global__ void kv_commit_finalize_kernel(const eagle_commit_desc d, const int32
 cudaError_t launch_kv_commit(const eagle_commit_desc* d, const CommitArgs& a, const int32_t* n_acc,
                              const int32_t* path, int32_t* seq_len, int32_t* commit_pos, void* feat_cache,
                              const void* tree_feat, uint32_t* status, cudaStream_t s) {
-  dim3 grid(d->max_depth + 1, d->batch, d->layers);
+  dim3 grid(d->batch, d->max_depth + 1, d->layers);
   kv_commit_copy_kernel<<<grid, 128, 0, s>>>(*d, a, n_acc, path, seq_len, feat_cache, tree_feat);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;

@@ -14,12 +14,16 @@
 // softmax(row / T) (non-greedy).
 //
 // Kernels
-//   tree_chunk_kernel   one CTA per (request, frontier row, 4096-token chunk):
+//   tree_chunk_kernel   one CTA per (request x frontier row, 4096-token chunk):
 //                       chunk max, sum exp (T = 1 and T), and the chunk's top-16 by
 //                       (logit desc, id asc) -- one streaming pass over the logits.
 //   tree_select_kernel  one CTA per request: merges the chunk results per row,
 //                       extends the pool, picks the frontier (bitonic sort in shared
 //                       memory) and, at the last level, emits the tree arrays.
+//
+// Precision: chunk sums are compensated fp32, merged in double; cumulative scores
+// are kept in double so that fp32 and fp64 selections agree unless two scores at a
+// boundary are within 1e-5 (reported as a near-tie).
 #include <limits.h>
 
 #include "common.cuh"
@@ -30,12 +34,13 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int K = kMaxTopK;
+constexpr double kIcdfNearEps = 1e-7;
 
 struct ChunkPart {
   float m;        // chunk max logit
-  float s1;       // sum exp(x - m)
-  float sT;       // sum exp((x - m) / T)
   float pad;
+  double s1;      // sum exp(x - m)
+  double sT;      // sum exp((x - m) / T)
   float tv[K];    // top-K logits of the chunk, best first
   int ti[K];      // their token ids (INT_MAX = empty)
 };
@@ -57,13 +62,15 @@ __device__ __forceinline__ ChunkPart* parts(const TreeBuildPlan& p, uint8_t* ws)
 // ------------------------------------------------------------------ chunk pass
 template <bool TOPK>
 __global__ void __launch_bounds__(kThreads) tree_chunk_kernel(const TreeBuildPlan p, const BuildArgs a) {
-  const int c = blockIdx.x, f = blockIdx.y, b = blockIdx.z;
+  const int bf = blockIdx.x, c = blockIdx.y;
+  const int b = bf / a.F, f = bf % a.F;
   const int lo = c * kVocabChunk;
   const int hi = min(p.V, lo + kVocabChunk);
-  const size_t row = (static_cast<size_t>(b) * a.F + f) * p.V;
-  const float c1 = kLog2e, cT = kLog2e / (p.temperature > 0.f ? p.temperature : 1.f);
+  const size_t row = static_cast<size_t>(bf) * p.V;
+  const float invT = 1.f / (p.temperature > 0.f ? p.temperature : 1.f);
 
-  float m = -INFINITY, s1 = 0.f, sT = 0.f;
+  float m = -INFINITY;
+  CSum s1, sT;
   float tv[K];
   int ti[K];
 #pragma unroll
@@ -75,13 +82,13 @@ __global__ void __launch_bounds__(kThreads) tree_chunk_kernel(const TreeBuildPla
     const float x = load_elem(a.logits, row + v, p.dtype);
     if (x > m) {
       if (m != -INFINITY) {
-        s1 *= exp2f((m - x) * c1);
-        sT *= exp2f((m - x) * cT);
+        s1.scale(expf(m - x));
+        sT.scale(expf((m - x) * invT));
       }
       m = x;
     }
-    s1 += exp2f((x - m) * c1);
-    sT += exp2f((x - m) * cT);
+    s1.add(expf(x - m));
+    sT.add(expf((x - m) * invT));
     if (TOPK && before(x, v, tv[K - 1], ti[K - 1])) {
       float cv = x;
       int ci = v;
@@ -97,89 +104,84 @@ __global__ void __launch_bounds__(kThreads) tree_chunk_kernel(const TreeBuildPla
       }
     }
   }
-  // block reduction of (m, s1, sT)
-  __shared__ float sm[kThreads / 32], ss1[kThreads / 32], ssT[kThreads / 32];
+  // block reduction of (m, s1, sT): sums rescaled to the warp max, in double
+  __shared__ float sm[kThreads / 32];
+  __shared__ double ss1[kThreads / 32], ssT[kThreads / 32];
   __shared__ float wv[kThreads / 32];
   __shared__ int wi[kThreads / 32];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
-    const float a1 = __shfl_xor_sync(0xffffffffu, s1, o);
-    const float aT = __shfl_xor_sync(0xffffffffu, sT, o);
-    const float M = fmaxf(m, m2);
-    if (M != -INFINITY) {
-      s1 = s1 * exp2f((m - M) * c1) + a1 * exp2f((m2 - M) * c1);
-      sT = sT * exp2f((m - M) * cT) + aT * exp2f((m2 - M) * cT);
-    }
-    m = M;
-  }
+  const float M = warp_max(m);
+  double d1 = (m == -INFINITY) ? 0.0 : s1.total() * static_cast<double>(expf(m - M));
+  double dT = (m == -INFINITY) ? 0.0 : sT.total() * static_cast<double>(expf((m - M) * invT));
+  d1 = warp_sum_d(d1);
+  dT = warp_sum_d(dT);
   if (lane == 0) {
-    sm[warp] = m;
-    ss1[warp] = s1;
-    ssT[warp] = sT;
+    sm[warp] = M;
+    ss1[warp] = d1;
+    ssT[warp] = dT;
   }
   __syncthreads();
   ChunkPart* out = parts(p, a.ws) + (static_cast<size_t>(b) * p.f_max + f) * p.n_chunks + c;
   if (threadIdx.x == 0) {
-    float M = -INFINITY;
-    for (int w = 0; w < kThreads / 32; ++w) M = fmaxf(M, sm[w]);
-    float t1 = 0.f, tT = 0.f;
+    float BM = -INFINITY;
+    for (int w = 0; w < kThreads / 32; ++w) BM = fmaxf(BM, sm[w]);
+    double t1 = 0.0, tT = 0.0;
     for (int w = 0; w < kThreads / 32; ++w) {
       if (sm[w] == -INFINITY) continue;
-      t1 += ss1[w] * exp2f((sm[w] - M) * c1);
-      tT += ssT[w] * exp2f((sm[w] - M) * cT);
+      t1 += ss1[w] * static_cast<double>(expf(sm[w] - BM));
+      tT += ssT[w] * static_cast<double>(expf((sm[w] - BM) * invT));
     }
-    out->m = M;
+    out->m = BM;
     out->s1 = t1;
     out->sT = tT;
   }
-  if constexpr (!TOPK) return;
-  // block top-K: K rounds of block argmax over the threads' list heads
-  for (int r = 0; r < K; ++r) {
-    float bv = tv[0];
-    int bi = ti[0];
+  if constexpr (TOPK) {
+    // block top-K: K rounds of block argmax over the threads' list heads
+    for (int r = 0; r < K; ++r) {
+      float bv = tv[0];
+      int bi = ti[0];
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float v2 = __shfl_xor_sync(0xffffffffu, bv, o);
-      const int i2 = __shfl_xor_sync(0xffffffffu, bi, o);
-      if (before(v2, i2, bv, bi)) {
-        bv = v2;
-        bi = i2;
+      for (int o = 16; o > 0; o >>= 1) {
+        const float v2 = __shfl_xor_sync(0xffffffffu, bv, o);
+        const int i2 = __shfl_xor_sync(0xffffffffu, bi, o);
+        if (before(v2, i2, bv, bi)) {
+          bv = v2;
+          bi = i2;
+        }
       }
-    }
-    __syncthreads();
-    if (lane == 0) {
-      wv[warp] = bv;
-      wi[warp] = bi;
-    }
-    __syncthreads();
-    bv = wv[0];
-    bi = wi[0];
-    for (int w = 1; w < kThreads / 32; ++w)
-      if (before(wv[w], wi[w], bv, bi)) {
-        bv = wv[w];
-        bi = wi[w];
+      __syncthreads();
+      if (lane == 0) {
+        wv[warp] = bv;
+        wi[warp] = bi;
       }
-    if (threadIdx.x == 0) {
-      out->tv[r] = bv;
-      out->ti[r] = bi;
-    }
-    if (bi != INT_MAX && ti[0] == bi) {  // the owner pops its head
+      __syncthreads();
+      bv = wv[0];
+      bi = wi[0];
+      for (int w = 1; w < kThreads / 32; ++w)
+        if (before(wv[w], wi[w], bv, bi)) {
+          bv = wv[w];
+          bi = wi[w];
+        }
+      if (threadIdx.x == 0) {
+        out->tv[r] = bv;
+        out->ti[r] = bi;
+      }
+      if (bi != INT_MAX && ti[0] == bi) {  // the owner pops its head
 #pragma unroll
-      for (int j = 0; j < K - 1; ++j) {
-        tv[j] = tv[j + 1];
-        ti[j] = ti[j + 1];
+        for (int j = 0; j < K - 1; ++j) {
+          tv[j] = tv[j + 1];
+          ti[j] = ti[j + 1];
+        }
+        tv[K - 1] = -INFINITY;
+        ti[K - 1] = INT_MAX;
       }
-      tv[K - 1] = -INFINITY;
-      ti[K - 1] = INT_MAX;
     }
   }
 }
 
 // ------------------------------------------------------------------ select helpers
 // Block bitonic sort of n2 (power of two) entries, best first by (key desc, idx asc).
-__device__ void bitonic_sort(float* key, int* idx, int n2) {
+__device__ void bitonic_sort(double* key, int* idx, int n2) {
   for (int k = 2; k <= n2; k <<= 1) {
     for (int j = k >> 1; j > 0; j >>= 1) {
       for (int i = threadIdx.x; i < n2; i += blockDim.x) {
@@ -188,7 +190,7 @@ __device__ void bitonic_sort(float* key, int* idx, int n2) {
           const bool up = (i & k) == 0;
           const bool sw = up ? before(key[ixj], idx[ixj], key[i], idx[i]) : before(key[i], idx[i], key[ixj], idx[ixj]);
           if (sw) {
-            const float tk = key[i];
+            const double tk = key[i];
             key[i] = key[ixj];
             key[ixj] = tk;
             const int t = idx[i];
@@ -202,26 +204,27 @@ __device__ void bitonic_sort(float* key, int* idx, int n2) {
   }
 }
 
-// Row statistics merged over chunks by one warp: M, ln Z (T = 1) and the chunk
-// weights at temperature T (for draws).
+// Row statistics merged over chunks by one warp: M, ln Z (T = 1) and the mass at
+// temperature T (for draws), in double.
 struct RowStats {
-  float M, lnZ1, WT;
+  float M;
+  double lnZ1, WT;
 };
 
-__device__ RowStats row_stats(const ChunkPart* cp, int n_chunks, float cT) {
+__device__ RowStats row_stats(const ChunkPart* cp, int n_chunks, float invT) {
   float M = -INFINITY;
   for (int c = threadIdx.x & 31; c < n_chunks; c += 32) M = fmaxf(M, cp[c].m);
   M = warp_max(M);
-  float z1 = 0.f, zT = 0.f;
+  double z1 = 0.0, zT = 0.0;
   for (int c = threadIdx.x & 31; c < n_chunks; c += 32) {
     if (cp[c].m == -INFINITY) continue;
-    z1 += cp[c].s1 * exp2f((cp[c].m - M) * kLog2e);
-    zT += cp[c].sT * exp2f((cp[c].m - M) * cT);
+    z1 += cp[c].s1 * static_cast<double>(expf(cp[c].m - M));
+    zT += cp[c].sT * static_cast<double>(expf((cp[c].m - M) * invT));
   }
   RowStats r;
   r.M = M;
-  r.lnZ1 = logf(warp_sum(z1));
-  r.WT = warp_sum(zT);
+  r.lnZ1 = log(warp_sum_d(z1));
+  r.WT = warp_sum_d(zT);
   return r;
 }
 
@@ -265,22 +268,22 @@ __device__ void merge_topk(const ChunkPart* cp, int n_chunks, int cnt, int* tok,
   __syncwarp();
 }
 
-// Warp inverse-CDF draw over one logit row with weights exp((x - M) / T), using the
-// chunk totals to skip to the chunk that holds the crossing.  Returns the token;
-// *near = 1 when the draw lands within 1e-5 * W of a bin edge.
+// Warp inverse-CDF draw over one logit row with weights exp((x - M) / T): the chunk
+// masses pick the chunk that holds the crossing, then the lanes scan that chunk
+// (lane offsets in double, local running sums in fp32).  Returns the token; *near =
+// 1 when the draw lands within 1e-7 of the mass of a bin edge.
 __device__ int warp_draw(const void* logits, size_t row, int dtype, int V, const ChunkPart* cp, int n_chunks, float M,
-                         float cT, float W, float u, int* near) {
+                         float invT, double W, float u, int* near) {
   const int lane = threadIdx.x & 31;
-  const float target = u * W;
-  // chunk holding the crossing (sequential over chunks, lane 0; broadcast)
-  int cstar = -1;
-  float base = 0.f;
+  const double target = static_cast<double>(u) * W;
+  int cstar = -1, fallback = 0;
+  double base = 0.0;
   if (lane == 0) {
-    float cum = 0.f;
+    double cum = 0.0;
     int last_pos = -1;
     for (int c = 0; c < n_chunks; ++c) {
-      const float w = (cp[c].m == -INFINITY) ? 0.f : cp[c].sT * exp2f((cp[c].m - M) * cT);
-      if (w > 0.f) last_pos = c;
+      const double w = (cp[c].m == -INFINITY) ? 0.0 : cp[c].sT * static_cast<double>(expf((cp[c].m - M) * invT));
+      if (w > 0.0) last_pos = c;
       if (cum + w > target) {
         cstar = c;
         base = cum;
@@ -288,37 +291,40 @@ __device__ int warp_draw(const void* logits, size_t row, int dtype, int V, const
       }
       cum += w;
     }
-    if (cstar < 0) {
+    if (cstar < 0) {  // nothing crosses (rounding): the last positive weight
       cstar = last_pos < 0 ? 0 : last_pos;
-      base = cum - ((cp[cstar].m == -INFINITY) ? 0.f : cp[cstar].sT * exp2f((cp[cstar].m - M) * cT));
+      fallback = 1;
     }
   }
   cstar = __shfl_sync(0xffffffffu, cstar, 0);
+  fallback = __shfl_sync(0xffffffffu, fallback, 0);
   base = __shfl_sync(0xffffffffu, base, 0);
   const int lo = cstar * kVocabChunk, hi = min(V, lo + kVocabChunk);
   const int n = hi - lo;
   const int seg = (n + 31) / 32;
   const int a0 = lo + lane * seg, a1 = min(hi, a0 + seg);
-  float mine = 0.f;
-  for (int v = a0; v < a1; ++v) mine += exp2f((load_elem(logits, row + v, dtype) - M) * cT);
-  float incl = mine;
+  double my = 0.0;
+  for (int v = a0; v < a1; ++v) my += static_cast<double>(expf((load_elem(logits, row + v, dtype) - M) * invT));
+  double incl = my;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    const float t = __shfl_up_sync(0xffffffffu, incl, o);
+    const double t = __shfl_up_sync(0xffffffffu, incl, o);
     if (lane >= o) incl += t;
   }
-  float cum = base + incl - mine;
+  const double lbase = base + incl - my;
+  const double rel = fallback ? INFINITY : target - lbase;
+  double cum = 0.0;
   int found = -1;
-  float prev_edge = 0.f, next_edge = 0.f;
+  double prev_edge = 0.0, next_edge = 0.0;
   int last_pos = -1;
   for (int v = a0; v < a1; ++v) {
-    const float w = exp2f((load_elem(logits, row + v, dtype) - M) * cT);
+    const float w = expf((load_elem(logits, row + v, dtype) - M) * invT);
     if (w > 0.f) last_pos = v;
-    const float nc = cum + w;
-    if (found < 0 && nc > target) {
+    const double nc = cum + static_cast<double>(w);
+    if (found < 0 && w > 0.f && nc > rel) {
       found = v;
-      prev_edge = cum;
-      next_edge = nc;
+      prev_edge = lbase + cum;
+      next_edge = lbase + nc;
     }
     cum = nc;
   }
@@ -328,9 +334,9 @@ __device__ int warp_draw(const void* logits, size_t row, int dtype, int V, const
   if (ball) {
     const int src = __ffs(ball) - 1;
     tok = __shfl_sync(0xffffffffu, found, src);
-    const float pe = __shfl_sync(0xffffffffu, prev_edge, src);
-    const float ne = __shfl_sync(0xffffffffu, next_edge, src);
-    nr = (target - pe < kNearTieEps * W || ne - target < kNearTieEps * W) ? 1 : 0;
+    const double pe = __shfl_sync(0xffffffffu, prev_edge, src);
+    const double ne = __shfl_sync(0xffffffffu, next_edge, src);
+    nr = (target - pe < kIcdfNearEps * W || ne - target < kIcdfNearEps * W) ? 1 : 0;
   } else {
     const unsigned bl = __ballot_sync(0xffffffffu, last_pos >= 0);
     const int src = bl ? 31 - __clz(bl) : 0;
@@ -342,7 +348,6 @@ __device__ int warp_draw(const void* logits, size_t row, int dtype, int V, const
   return tok;
 }
 
-// ------------------------------------------------------------------ select / finalize
 __global__ void __launch_bounds__(kThreads) tree_select_kernel(const TreeBuildPlan p, const BuildArgs a) {
   const int b = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -350,9 +355,9 @@ __global__ void __launch_bounds__(kThreads) tree_select_kernel(const TreeBuildPl
   uint8_t* ws = a.ws;
   int32_t* state = reinterpret_cast<int32_t*>(ws + p.off_state) + b * 4;  // [0] n_pool, [1] near
   const ChunkPart* cps = parts(p, ws) + static_cast<size_t>(b) * p.f_max * p.n_chunks;
-  const float cT = kLog2e / (p.temperature > 0.f ? p.temperature : 1.f);
+  const float invT = 1.f / (p.temperature > 0.f ? p.temperature : 1.f);
 
-  __shared__ float skey[kMaxPool];
+  __shared__ double skey[kMaxPool];
   __shared__ int sidx[kMaxPool];
   __shared__ int srow[kMaxPool];
   __shared__ int stok[NW][K];
@@ -373,7 +378,7 @@ __global__ void __launch_bounds__(kThreads) tree_select_kernel(const TreeBuildPl
   if (p.mode == EAGLE_TREE_DYNAMIC) {
     int32_t* ptok = reinterpret_cast<int32_t*>(ws + p.off_pool_tok) + static_cast<size_t>(b) * p.pool_cap;
     int32_t* ppar = reinterpret_cast<int32_t*>(ws + p.off_pool_par) + static_cast<size_t>(b) * p.pool_cap;
-    float* psc = reinterpret_cast<float*>(ws + p.off_pool_score) + static_cast<size_t>(b) * p.pool_cap;
+    double* psc = reinterpret_cast<double*>(ws + p.off_pool_score) + static_cast<size_t>(b) * p.pool_cap;
     int32_t* pdep = reinterpret_cast<int32_t*>(ws + p.off_pool_depth) + static_cast<size_t>(b) * p.pool_cap;
     int32_t* front = reinterpret_cast<int32_t*>(ws + p.off_front) + static_cast<size_t>(b) * K;
     const int base = state[0];
@@ -381,15 +386,15 @@ __global__ void __launch_bounds__(kThreads) tree_select_kernel(const TreeBuildPl
     // extend the pool: one warp per frontier row
     for (int f = warp; f < a.F; f += NW) {
       const ChunkPart* cp = cps + static_cast<size_t>(f) * p.n_chunks;
-      const RowStats rs = row_stats(cp, p.n_chunks, cT);
+      const RowStats rs = row_stats(cp, p.n_chunks, invT);
       merge_topk(cp, p.n_chunks, k, stok[warp], sval[warp]);
       const int pidx = (a.level == 1) ? -1 : front[f];
-      const float spar_score = (pidx < 0) ? 0.f : psc[pidx];
+      const double spar_score = (pidx < 0) ? 0.0 : psc[pidx];
       if (lane < k) {
         const int i = base + f * k + lane;
         ptok[i] = stok[warp][lane];
         ppar[i] = pidx;
-        psc[i] = spar_score + ((sval[warp][lane] - rs.M) - rs.lnZ1);
+        psc[i] = spar_score + (static_cast<double>(sval[warp][lane] - rs.M) - rs.lnZ1);
         pdep[i] = a.level;
       }
       __syncwarp();
@@ -405,7 +410,11 @@ __global__ void __launch_bounds__(kThreads) tree_select_kernel(const TreeBuildPl
     }
     __syncthreads();
     bitonic_sort(skey, sidx, n2);
-    if (threadIdx.x == 0 && n_new > k && skey[k - 1] - skey[k] < kNearTieEps) s_near += 1;
+    // a near-tie at the boundary, unless it is an exact tie between siblings (same
+    // parent, same logit), which both fp32 and fp64 break by pool index
+    if (threadIdx.x == 0 && n_new > k && skey[k - 1] - skey[k] < kNearTieEps &&
+        !(skey[k - 1] == skey[k] && ppar[sidx[k - 1]] == ppar[sidx[k]]))
+      s_near += 1;
     for (int j = threadIdx.x; j < n_new; j += kThreads) srow[j] = 0;
     __syncthreads();
     for (int j = threadIdx.x; j < k; j += kThreads) srow[sidx[j] - base] = 1;
@@ -437,7 +446,9 @@ __global__ void __launch_bounds__(kThreads) tree_select_kernel(const TreeBuildPl
     }
     __syncthreads();
     bitonic_sort(skey, sidx, n2);
-    if (threadIdx.x == 0 && np > N && skey[N - 1] - skey[N] < kNearTieEps) state[1] += 1;
+    if (threadIdx.x == 0 && np > N && skey[N - 1] - skey[N] < kNearTieEps &&
+        !(skey[N - 1] == skey[N] && ppar[sidx[N - 1]] == ppar[sidx[N]]))
+      state[1] += 1;
     for (int j = threadIdx.x; j < np; j += kThreads) srow[j] = 0;
     __syncthreads();
     for (int j = threadIdx.x; j < N; j += kThreads) srow[sidx[j]] = 1;
@@ -459,7 +470,7 @@ __global__ void __launch_bounds__(kThreads) tree_select_kernel(const TreeBuildPl
       a.out.parent[ob + r] = pr;
       a.out.depth[ob + r] = pdep[j];
       a.out.pos_id[ob + r] = L + pdep[j];
-      a.out.score[ob + r] = psc[j];
+      a.out.score[ob + r] = static_cast<float>(psc[j]);
     }
     if (threadIdx.x == 0) {
       spar[0] = -1;
@@ -473,11 +484,11 @@ __global__ void __launch_bounds__(kThreads) tree_select_kernel(const TreeBuildPl
   } else {
     // ---- static shape
     int32_t* ntok = reinterpret_cast<int32_t*>(ws + p.off_node_tok) + static_cast<size_t>(b) * p.R;
-    float* nsc = reinterpret_cast<float*>(ws + p.off_node_score) + static_cast<size_t>(b) * p.R;
+    double* nsc = reinterpret_cast<double*>(ws + p.off_node_score) + static_cast<size_t>(b) * p.R;
     const bool sampled = p.mode == EAGLE_TREE_STATIC_SAMPLED;
     if (a.level == 1 && threadIdx.x == 0) {
       ntok[0] = a.root_tok[b];
-      nsc[0] = 0.f;
+      nsc[0] = 0.0;
     }
     __syncthreads();
     // frontier row f = the f-th node of depth level-1; one warp per row
@@ -494,7 +505,7 @@ __global__ void __launch_bounds__(kThreads) tree_select_kernel(const TreeBuildPl
       for (int i = n + 1; i < p.R; ++i) kids += (p.shape.parent[i] == n);
       if (kids == 0) continue;
       const ChunkPart* cp = cps + static_cast<size_t>(f) * p.n_chunks;
-      const RowStats rs = row_stats(cp, p.n_chunks, cT);
+      const RowStats rs = row_stats(cp, p.n_chunks, invT);
       const size_t row = (static_cast<size_t>(b) * a.F + f) * p.V;
       if (!sampled) merge_topk(cp, p.n_chunks, kids, stok[warp], sval[warp]);
       int j = 0;
@@ -505,13 +516,13 @@ __global__ void __launch_bounds__(kThreads) tree_select_kernel(const TreeBuildPl
           tok = stok[warp][j];
         } else {
           int nr = 0;
-          tok = warp_draw(a.logits, row, p.dtype, p.V, cp, p.n_chunks, rs.M, cT, rs.WT,
+          tok = warp_draw(a.logits, row, p.dtype, p.V, cp, p.n_chunks, rs.M, invT, rs.WT,
                           a.u_draft[static_cast<size_t>(b) * p.R + ch], &nr);
           near_local += nr;
         }
         if (lane == 0) {
           ntok[ch] = tok;
-          nsc[ch] = nsc[n] + ((load_elem(a.logits, row + tok, p.dtype) - rs.M) - rs.lnZ1);
+          nsc[ch] = nsc[n] + (static_cast<double>(load_elem(a.logits, row + tok, p.dtype) - rs.M) - rs.lnZ1);
         }
         ++j;
       }
@@ -543,7 +554,7 @@ __global__ void __launch_bounds__(kThreads) tree_select_kernel(const TreeBuildPl
       a.out.parent[ob + i] = p.shape.parent[i];
       a.out.depth[ob + i] = p.shape.depth[i];
       a.out.pos_id[ob + i] = L + p.shape.depth[i];
-      a.out.score[ob + i] = nsc[i];
+      a.out.score[ob + i] = static_cast<float>(nsc[i]);
     }
     __syncthreads();
   }
@@ -620,7 +631,7 @@ void plan_tree_build(const eagle_tree_desc* d, TreeBuildPlan* p) {
   p->off_pool_par = off;
   off = align256(off + cap * 4);
   p->off_pool_score = off;
-  off = align256(off + cap * 4);
+  off = align256(off + cap * 8);
   p->off_pool_depth = off;
   off = align256(off + cap * 4);
   p->off_state = off;
@@ -632,7 +643,7 @@ void plan_tree_build(const eagle_tree_desc* d, TreeBuildPlan* p) {
   p->off_node_tok = off;
   off = align256(off + static_cast<size_t>(p->B) * p->R * 4);
   p->off_node_score = off;
-  off = align256(off + static_cast<size_t>(p->B) * p->R * 4);
+  off = align256(off + static_cast<size_t>(p->B) * p->R * 8);
   p->total = off;
 }
 
@@ -656,7 +667,7 @@ cudaError_t launch_tree_build(const TreeBuildPlan& p, int level, const void* log
   a.out = out;
   a.level = level;
   a.F = frontier_rows(p, level);
-  dim3 grid(p.n_chunks, a.F, p.B);
+  dim3 grid(p.B * a.F, p.n_chunks);
   if (p.mode == EAGLE_TREE_STATIC_SAMPLED)
     tree_chunk_kernel<false><<<grid, kThreads, 0, s>>>(p, a);
   else

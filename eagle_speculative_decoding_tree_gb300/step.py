@@ -66,10 +66,14 @@ class GpuTreeBuilder:
         lg = _to_dev(logits, self.w.dtype, self.device)
         ud = None if u_draft is None else torch.from_numpy(np.asarray(u_draft, np.float32)).to(self.device)
         B.eagle_tree_build(self.desc, level, lg, ud, self.root_tok, self.seq_len, self.ws, self.out)
-        F = B.tree_frontier_rows(self.desc, level + 1) if level < self.depth else \
-            (0 if self.w.tree_mode != "dynamic" else self.w.top_k)
-        if F <= 0:
-            F = 0
+        if self.w.tree_mode == "dynamic":
+            F = self.w.top_k
+        else:  # the nodes created at this level (depth == level), in row order
+            par = synth.static_parents(self.w.static_choices)
+            dep = np.zeros(len(par), np.int32)
+            for i in range(1, len(par)):
+                dep[i] = dep[par[i]] + 1
+            F = int((dep == level).sum())
         tok = self.out.frontier_tok[:, :F].cpu().numpy()
         slot = self.out.frontier_slot[:, :F].cpu().numpy()
         return tok, slot

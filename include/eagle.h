@@ -179,7 +179,8 @@ typedef struct {
  *   seq_len [B] int32 (0 <= seq_len <= P); anc_mask [B][R][W]; out [B][R][Hq][D];
  *   lse [B][R][Hq] fp32, may be NULL.
  * ws: eagle_workspace_size(EAGLE_WS_TREE_ATTN, d) bytes (split partials).
- * Unsupported: head_dim not 64/128, R > 128, Hq % Hkv != 0, bf16 out with fp32 inputs. */
+ * Unsupported: head_dim not 64/128, R > 128, Hq % Hkv != 0, B * Hkv > 65535, bf16 out
+ * with fp32 inputs. */
 int eagle_tree_attn(const eagle_attn_desc* d, const void* q, const void* k_cache, const void* v_cache,
                     const void* tree_k, const void* tree_v, const int32_t* seq_len,
                     const uint64_t* anc_mask, void* out, float* lse, void* ws, size_t ws_bytes,

@@ -38,7 +38,13 @@
 #define OR_BAD_ARG 1
 #define OR_NO_MEM 2
 
+/* A decision is a near-tie when fp32 and fp64 arithmetic could resolve it
+ * differently: |u - p/q| < 1e-5 for an accept test; a draw landing within
+ * 1e-7 * sum(w) of a bin edge; two scores at a selection boundary closer than
+ * 1e-5 (unless they are siblings with the same logit, an exact tie both sides
+ * break by pool index). */
 #define NEAR_TIE_EPS 1e-5
+#define ICDF_NEAR_EPS 1e-7
 
 /* Element types of the input buffers. */
 #define OR_F32 0
@@ -84,7 +90,7 @@ static void log_softmax(const void* row, size_t off, int V, int dtype, double* o
 
 /* Inverse CDF: smallest i with w_0 + ... + w_i > u * sum(w).  If rounding leaves
  * no such i, the last i with w_i > 0.  *near is set when u*sum(w) lies within
- * 1e-5 * sum(w) of either edge of the chosen bin. */
+ * 1e-7 * sum(w) of either edge of the chosen bin. */
 static int icdf(const double* w, int V, double u, int* near) {
   double W = 0.0;
   for (int v = 0; v < V; ++v) W += w[v];
@@ -93,7 +99,7 @@ static int icdf(const double* w, int V, double u, int* near) {
     double prev = c;
     c += w[v];
     if (c > target) {
-      if (near && (target - prev < NEAR_TIE_EPS * W || c - target < NEAR_TIE_EPS * W)) *near = 1;
+      if (near && (target - prev < ICDF_NEAR_EPS * W || c - target < ICDF_NEAR_EPS * W)) *near = 1;
       return v;
     }
   }
@@ -400,7 +406,9 @@ int oracle_tree_level_dynamic(int B, int V, int dtype, int k, int level, const v
       cand[j].id = base + j;
     }
     qsort(cand, (size_t)F * k, sizeof(vid_t), cmp_score);
-    if (F * k > k && fabs(cand[k - 1].val - cand[k].val) < NEAR_TIE_EPS) near_tie[b] += 1;
+    if (F * k > k && fabs(cand[k - 1].val - cand[k].val) < NEAR_TIE_EPS &&
+        !(cand[k - 1].val == cand[k].val && ppar[cand[k - 1].id] == ppar[cand[k].id]))
+      near_tie[b] += 1;
     for (int j = 0; j < k; ++j) fr[j] = cand[j].id;
     for (int a = 1; a < k; ++a) /* insertion sort by pool index */
       for (int j = a; j > 0 && fr[j - 1] > fr[j]; --j) {
@@ -449,7 +457,10 @@ int oracle_tree_finalize_dynamic(int B, int N, int pool_cap, const int32_t* pool
       tree_of[j] = -1;
     }
     qsort(cand, (size_t)np, sizeof(vid_t), cmp_score);
-    if (np > N && fabs(cand[N - 1].val - cand[N].val) < NEAR_TIE_EPS) near_tie[b] += 1;
+    if (np > N && fabs(cand[N - 1].val - cand[N].val) < NEAR_TIE_EPS &&
+        !(cand[N - 1].val == cand[N].val &&
+          pool_parent[po + cand[N - 1].id] == pool_parent[po + cand[N].id]))
+      near_tie[b] += 1;
     for (int j = 0; j < N; ++j) sel[j] = cand[j].id;
     for (int a = 1; a < N; ++a)
       for (int j = a; j > 0 && sel[j - 1] > sel[j]; --j) {

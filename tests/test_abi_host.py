@@ -106,7 +106,7 @@ def test_accept_validation(lib):
     assert _call_acc(lib, _acc(), out_ok=False) == B.EAGLE_ERR_INVALID_ARG
     d = _acc()
     need = B.workspace_size(B.EAGLE_WS_ACCEPT, d)
-    assert need == 61 * 32 * 16  # one 16-byte record per (row, 4096-token chunk)
+    assert need == 61 * 32 * 24  # one 24-byte record per (row, 4096-token chunk)
     assert _call_acc(lib, d, ws_bytes=need - 1) == B.EAGLE_ERR_WORKSPACE
     ds = _acc(proposal=1)
     assert B.workspace_size(B.EAGLE_WS_ACCEPT, ds) == 2 * need

@@ -4,7 +4,7 @@ Trees come from the oracle's builder on the synthetic path-keyed LM; target (and
 draft) rows are that LM's rows at the tree's nodes; uniforms are seeded.  The GPU
 must reproduce the oracle's accepted lengths, paths and emitted tokens bit for
 bit, except for requests where either side reports a near-tie (|u - p/q| < 1e-5,
-or a draw within 1e-5 of a bin edge), which are counted.  A GPU-side chi-square
+or a draw within 1e-7 of the mass of a bin edge), which are counted.  A GPU-side chi-square
 check repeats the losslessness test on the kernels themselves.
 """
 import numpy as np
@@ -82,7 +82,7 @@ def case(w, batch, seed, T=None, proposal=None):
 ])
 def test_accept_workloads(name, batch, T):
     g, r = case(W[name], batch, seed=1, T=T)
-    compare(g, r, max_near=max(1, batch // 8))
+    compare(g, r, max_near=max(2, batch // 4))
 
 
 def test_accept_concurrency_batch32():
@@ -156,3 +156,33 @@ def test_accept_bad_token_is_flagged_and_rejected():
     g = gpu_accept(w, tree, target, None, np.zeros((1, 3), np.float32), np.zeros(1, np.float32), oracle.DELTA, 1.0, 1)
     assert g["status"][0] & B.EAGLE_STATUS_BAD_TOKEN
     assert g["n_acc"][0] == 1 and g["out_tok"][0, 0] == 3
+
+
+@pytest.mark.parametrize("proposal", [oracle.DELTA, oracle.SAMPLED])
+def test_accept_agreement_many_requests_128k(proposal):
+    """Many requests over a 128K vocabulary: outside the requests either side reports as
+    near-ties, the GPU and the oracle never disagree; near-ties stay rare."""
+    from gpu_helpers import random_tree
+    Bn, R, V, n_rows = 128, 12, 128256, 24
+    g = synth.rng(0, 7900, proposal)
+    pool_t = np.stack([synth.zipf_row(g, V) for _ in range(n_rows)])
+    pool_d = (pool_t + synth.normal_row(g, pool_t.shape, 0.5)).astype(np.float32)
+    which = g.integers(0, n_rows, (Bn, R))
+    target = synth.bf16_bits(pool_t[which])
+    draft = synth.bf16_bits(pool_d[which]) if proposal == oracle.SAMPLED else None
+    tokens = np.zeros((Bn, R), np.int32)
+    parent = np.zeros((Bn, R), np.int32)
+    for b in range(Bn):
+        par, _ = random_tree(R, seed=1000 + b)
+        parent[b] = par
+        for i in range(1, R):  # one of the parent row's three most likely tokens
+            tokens[b, i] = np.argsort(-pool_d[which[b, par[i]]])[g.integers(0, 3)]
+    ua, uf = synth.uniforms(g, (Bn, R)), synth.uniforms(g, (Bn,))
+    max_depth = R - 1
+    tree = {"tokens": tokens, "parent": parent}
+    w = W["llama8b"]
+    r = oracle.accept(target, tokens, parent, ua, uf, 1.0, proposal, max_depth + 1, draft=draft)
+    out = gpu_accept(w, tree, target, draft, ua, uf, proposal, 1.0, max_depth)
+    near = compare(out, r, max_near=Bn // 8)
+    assert (r["n_acc"] > 0).sum() > Bn // 10
+    print(f"near-ties: {near} of {Bn}")

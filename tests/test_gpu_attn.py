@@ -19,12 +19,7 @@ pytestmark = pytest.mark.gpu
 W = synth.WORKLOADS
 
 
-def _check(w, batch, seq_len, rows, par, mask, heads, q_scale=1.0, num_splits=0, out_f32=False,
-           precision=B.EAGLE_ATTN_STANDARD, derived_tol=False):
-    """derived_tol: the standard path on sharply peaked rows, where the bound comes
-    from the arithmetic instead of the fixed 2e-3: P rounded to bf16 (unit roundoff
-    u = 2^-8) moves O by at most u/(1-u) * max_j |v_j - O|, and a bf16 output adds
-    u * |O|."""
+def _run_one(w, batch, seq_len, rows, par, mask, heads, q_scale, num_splits, out_f32, precision, bound_fn):
     inputs, out, lse = run_attn(w, batch, seq_len, rows, par, mask, q_scale=q_scale, num_splits=num_splits,
                                 out_f32=out_f32, precision=precision)
     G = w.group
@@ -33,21 +28,43 @@ def _check(w, batch, seq_len, rows, par, mask, heads, q_scale=1.0, num_splits=0,
     for b, h in heads:
         sub = head_slice(inputs, h, G, b)
         ref, ref_lse = oracle.tree_attn(*sub, seq_len[b:b + 1], par[None], 1.0 / np.sqrt(w.head_dim))
-        got = out[b:b + 1, :, h * G:(h + 1) * G]
-        err_el = np.abs(got - ref)
-        if derived_tol:
-            u = 2.0 ** -8
-            vmax = max(np.abs(synth.bf16_value(sub[2]) if w.dtype == "bf16" else sub[2]).max(),
-                       np.abs(synth.bf16_value(sub[4]) if w.dtype == "bf16" else sub[4]).max())
-            bound = tol + u / (1 - u) * 2 * vmax + (0 if out_f32 else u * np.abs(ref))
-            assert (err_el <= bound).all(), f"b={b} h={h}: error {err_el.max()} above the derived bound"
-        else:
-            err = float(err_el.max())
-            assert err < tol, f"b={b} h={h}: max abs error {err}"
-        worst = max(worst, float(err_el.max()))
+        err = np.abs(out[b:b + 1, :, h * G:(h + 1) * G] - ref)
+        bound = bound_fn(ref, sub)
+        assert (err <= bound).all(), (f"b={b} h={h} precision={precision} out_f32={out_f32}: max abs error "
+                                      f"{err.max():.3e}, worst excess {(err - bound).max():.3e}")
+        worst = max(worst, float(err.max()))
         lerr = float(np.abs(lse[b:b + 1, :, h * G:(h + 1) * G] - ref_lse).max())
         assert lerr < tol, f"b={b} h={h}: lse max abs error {lerr}"
     return worst
+
+
+def _check(w, batch, seq_len, rows, par, mask, heads, q_scale=1.0, num_splits=0, strict_standard=False):
+    """Check one case against the oracle.
+
+    fp32 inputs: max abs error < 1e-5.
+    bf16 inputs, two launches:
+      * precise PV path with fp32 output: max abs error < 2e-3 (the stated bound);
+      * the benchmark's launch (standard PV path, bf16 output): P rounded to bf16
+        (unit roundoff u = 2^-8) moves O by at most u/(1-u) * max_j |v_j - O| <=
+        u/(1-u) * 2 max|v|, and rounding O to bf16 adds up to u * |O|; with
+        strict_standard the case must instead meet 2e-3 + u * |O| (the workloads'
+        shapes, whose rows are not sharply peaked).
+    """
+    if w.dtype == "f32":
+        return _run_one(w, batch, seq_len, rows, par, mask, heads, q_scale, num_splits, True,
+                        B.EAGLE_ATTN_STANDARD, lambda ref, sub: F32_TOL)
+    _run_one(w, batch, seq_len, rows, par, mask, heads, q_scale, num_splits, True, B.EAGLE_ATTN_PRECISE,
+             lambda ref, sub: BF16_TOL)
+    u = 2.0 ** -8
+
+    def derived(ref, sub):
+        vmax = max(np.abs(synth.bf16_value(sub[2])).max(), np.abs(synth.bf16_value(sub[4])).max())
+        if strict_standard:
+            return BF16_TOL + u * np.abs(ref)
+        return BF16_TOL + u / (1 - u) * 2 * vmax + u * np.abs(ref)
+
+    return _run_one(w, batch, seq_len, rows, par, mask, heads, q_scale, num_splits, False, B.EAGLE_ATTN_STANDARD,
+                    derived)
 
 
 @pytest.mark.parametrize("name,kw,prefix,rows,q_scale,splits", [
@@ -73,22 +90,11 @@ def test_tree_attention_small(name, kw, prefix, rows, q_scale, splits):
 
 
 @pytest.mark.parametrize("head_dim", [128, 64])
-def test_tree_attention_peaked_rows_precise_path(head_dim):
-    """Q scaled by 4: sharply peaked softmax rows that exercise the online rescaling.
-    The precise PV path with fp32 output meets the 2e-3 bound; the standard path is
-    held to the bound derived from bf16 rounding of P and of the output."""
+def test_tree_attention_peaked_rows(head_dim):
+    """Q scaled by 4: sharply peaked softmax rows that exercise the online rescaling."""
     w = W["llama8b"].with_(prefix=500, prefix_min=500, head_dim=head_dim)
     par, mask = random_tree(61, seed=9)
-    sl = np.array([500], np.int32)
-    _check(w, 1, sl, 61, par, mask, [(0, 0), (0, 7)], q_scale=4.0, out_f32=True, precision=B.EAGLE_ATTN_PRECISE)
-    _check(w, 1, sl, 61, par, mask, [(0, 0), (0, 7)], q_scale=4.0, derived_tol=True)
-    _check(w, 1, sl, 61, par, mask, [(0, 3)], q_scale=4.0, out_f32=True, derived_tol=True)
-
-
-def test_tree_attention_precise_path_normal_rows():
-    w = W["vicuna7b"].with_(prefix=900, prefix_min=900)
-    par, mask = random_tree(61, seed=10)
-    _check(w, 1, np.array([900], np.int32), 61, par, mask, [(0, 0), (0, 31)], precision=B.EAGLE_ATTN_PRECISE)
+    _check(w, 1, np.array([500], np.int32), 61, par, mask, [(0, 0), (0, 3), (0, 7)], q_scale=4.0)
 
 
 def test_tree_attention_head_dim_64():
@@ -113,11 +119,11 @@ def test_tree_attention_full_size(name):
     par, mask = random_tree(rows, seed=11, chain=(name == "long128k"))
     seq_len = synth.prefix_lengths(w, 1)
     heads = [(0, 0)] if name == "long128k" else [(0, 0), (0, w.n_kv_heads - 1)]
-    _check(w, 1, seq_len, rows, par, mask, heads)
+    _check(w, 1, seq_len, rows, par, mask, heads, strict_standard=True)
 
 
 def test_tree_attention_full_size_concurrency_batch8():
     w = W["concurrency"].with_(batch=8)
     seq_len = synth.prefix_lengths(w, 8)
     par, mask = random_tree(w.rows, seed=12)
-    _check(w, 8, seq_len, w.rows, par, mask, [(0, 0), (7, 7), (3, 2)])
+    _check(w, 8, seq_len, w.rows, par, mask, [(0, 0), (7, 7), (3, 2)], strict_standard=True)

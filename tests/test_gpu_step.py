@@ -98,8 +98,10 @@ def test_chained_verify_steps(name, kw, batch, layers):
             torch.cuda.synchronize()
             ref, _ = oracle.tree_attn(q, host_k[l], host_v[l], tk, tv, seq_len, tree["parent"],
                                       1.0 / math.sqrt(w.head_dim))
-            err = np.abs(out.float().cpu().numpy() - ref).max()
-            assert err < (F32_TOL if w.dtype == "f32" else BF16_TOL), (s, l, err)
+            err = np.abs(out.float().cpu().numpy() - ref)
+            # bf16 output: the 2e-3 bound plus one bf16 rounding of O (u = 2^-8)
+            bound = F32_TOL if w.dtype == "f32" else BF16_TOL + 2.0 ** -8 * np.abs(ref)
+            assert (err <= bound).all(), (s, l, float(err.max()))
         # ---- acceptance
         hs = node_hashes(tree, root_h)
         target = synth.as_dtype_bytes(np.stack([lm.rows(hs[b], "target") for b in range(batch)]), w.dtype)

@@ -4,7 +4,8 @@ Both builders receive the same draft rows at every level (rows of the synthetic
 path-keyed LM at the oracle's frontier), and must agree bit for bit on each
 level's frontier tokens and parent slots and on the final tree (tokens, parents,
 depths, position ids, ancestor masks).  A request whose selection boundary or
-draw landed within 1e-5 of a tie (reported by either side) is excluded from the
+draw landed near a tie (selection scores within 1e-5, a draw within 1e-7 of the
+mass of a bin edge; reported by either side) is excluded from the
 comparison from that level on and counted.  Cumulative scores agree within 1e-4.
 """
 import numpy as np
@@ -64,9 +65,11 @@ def build_both(w, batch, seed, lm=None, max_excluded=None):
     return int(excluded.sum())
 
 
-@pytest.mark.parametrize("name,batch", [("vicuna7b", 4), ("llama8b", 2), ("tiny", 16), ("long128k", 4)])
-def test_tree_build_workloads(name, batch):
-    build_both(W[name], batch, seed=1)
+@pytest.mark.parametrize("name,batch,max_excluded", [("vicuna7b", 4, 1), ("llama8b", 2, 1), ("tiny", 16, 2),
+                                                     ("long128k", 8, 3)])
+def test_tree_build_workloads(name, batch, max_excluded):
+    # a 128K-token draw lands within 1e-7 of the mass of a bin edge ~1-3% of the time
+    build_both(W[name], batch, seed=1, max_excluded=max_excluded)
 
 
 def test_tree_build_concurrency_batch8():

@@ -201,7 +201,7 @@ def test_temperature_is_logit_scaling():
 def test_near_tie_is_reported():
     target = np.log(np.array([[[0.25, 0.75], [0.5, 0.5]]], np.float32))
     p0 = softmax(target[0, 0].astype(np.float64))[0]
-    for du, near in ((0.0, 1), (3e-6, 1), (5e-5, 0)):
+    for du, near in ((0.0, 1), (3e-6, 1), (5e-5, 0)):  # accept test: |u - p/q| < 1e-5
         res = oracle.accept(target, np.array([[1, 0]], np.int32), np.array([[-1, 0]], np.int32),
                             np.array([[0.0, p0 + du]], np.float32), np.array([0.9], np.float32), 1.0, oracle.DELTA, 2)
         assert res["near_tie"][0] == near, du
