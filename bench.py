@@ -51,6 +51,22 @@ def _dist():
     return ws, rank, local
 
 
+def reduce_max(value: float, world_size: int, device: str = "cpu") -> float:
+    """Max of a per-rank value over all ranks of the current process group."""
+    if world_size <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_value(world_size: int, steps: int, ms: float) -> float:
+    """Whole-job steps/s: every rank runs `steps` steps of its own replica in `ms` (max over ranks)."""
+    return world_size * steps / (ms / 1e3)
+
+
 def _workload_desc(w, batch):
     return {"workload": f"{w.name}: {w.n_q_heads}q/{w.n_kv_heads}kv x {w.head_dim} {w.dtype}, vocab {w.vocab}, "
                         f"prefix {w.prefix_min if w.prefix_min != w.prefix else w.prefix}"
@@ -191,7 +207,7 @@ def run_ours(args):
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     w = synth.WORKLOADS[args.config]
     batch = args.batch or w.batch
-    w = w.with_(batch=batch)
+    w = w.with_(batch=batch, layers=args.layers or w.layers)
     B.load()
     t_setup = time.perf_counter()
     st = VerifyStep(w, batch=batch)
@@ -252,12 +268,10 @@ def run_ours(args):
         ms -= f0.elapsed_time(f1)
     if ws > 1:
         dist.barrier()
-        t = torch.tensor([ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = reduce_max(ms, ws, "cuda")
     clocks = clk.summary()
     ms_per_step = ms / args.steps
-    value = ws * args.steps / (ms / 1e3)
+    value = job_value(ws, args.steps, ms)
     n_acc = st.acc.n_acc.cpu().numpy()
 
     # ---- roofline of the dominant kernel: tree attention, timed alone (graph of L layers)
@@ -445,6 +459,7 @@ def main():
     ap.add_argument("--config", default="llama8b",
                     choices=["tiny", "vicuna7b", "llama8b", "long128k", "concurrency"])
     ap.add_argument("--batch", type=int, default=0, help="override the workload's batch (concurrency: 1/8/32)")
+    ap.add_argument("--layers", type=int, default=0, help="override the layer count (small profiling cases)")
     ap.add_argument("--no-graph", action="store_true")
     ap.add_argument("--skip-cpu-baseline", action="store_true")
     args = ap.parse_args()
