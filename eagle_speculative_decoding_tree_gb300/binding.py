@@ -25,11 +25,13 @@ EAGLE_TREE_DYNAMIC, EAGLE_TREE_STATIC_TOPK, EAGLE_TREE_STATIC_SAMPLED = 0, 1, 2
 EAGLE_PROPOSAL_DELTA, EAGLE_PROPOSAL_SAMPLED = 0, 1
 EAGLE_WS_TREE_BUILD, EAGLE_WS_TREE_ATTN, EAGLE_WS_ACCEPT = 1, 2, 3
 EAGLE_ATTN_STANDARD, EAGLE_ATTN_PRECISE = 0, 1
+EAGLE_ENGINE_AUTO, EAGLE_ENGINE_MMA_SYNC = 0, 1
 EAGLE_STATUS_BAD_TREE, EAGLE_STATUS_PATH_OVERFLOW, EAGLE_STATUS_CACHE_FULL, EAGLE_STATUS_BAD_TOKEN = 1, 2, 4, 8
 
 EXPORTED_SYMBOLS = ("eagle_tree_build", "eagle_tree_attn", "eagle_accept", "eagle_kv_commit",
                     "eagle_workspace_size", "eagle_status_string", "eagle_version",
-                    "eagle_tree_frontier_rows", "eagle_tree_max_frontier")
+                    "eagle_tree_frontier_rows", "eagle_tree_max_frontier", "eagle_last_cuda_error",
+                    "eagle_last_cuda_error_string")
 
 
 class TreeDesc(ctypes.Structure):
@@ -48,7 +50,7 @@ class AttnDesc(ctypes.Structure):
     _fields_ = [("batch", ctypes.c_int32), ("rows", ctypes.c_int32), ("n_q_heads", ctypes.c_int32),
                 ("n_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32), ("max_seq", ctypes.c_int32),
                 ("scale", ctypes.c_float), ("dtype", ctypes.c_int32), ("num_splits", ctypes.c_int32),
-                ("out_dtype", ctypes.c_int32), ("precision", ctypes.c_int32)]
+                ("out_dtype", ctypes.c_int32), ("precision", ctypes.c_int32), ("engine", ctypes.c_int32)]
 
 
 class AcceptDesc(ctypes.Structure):
@@ -93,6 +95,8 @@ def load() -> ctypes.CDLL:
         L.eagle_status_string.argtypes = [i32]
         L.eagle_status_string.restype = ctypes.c_char_p
         L.eagle_version.restype = ctypes.c_char_p
+        L.eagle_last_cuda_error.restype = ctypes.c_int
+        L.eagle_last_cuda_error_string.restype = ctypes.c_char_p
         L.eagle_tree_frontier_rows.argtypes = [ctypes.POINTER(TreeDesc), i32]
         L.eagle_tree_max_frontier.argtypes = [ctypes.POINTER(TreeDesc)]
         for f in (L.eagle_tree_build, L.eagle_tree_attn, L.eagle_accept, L.eagle_kv_commit,
@@ -104,7 +108,10 @@ def load() -> ctypes.CDLL:
 
 class EagleError(RuntimeError):
     def __init__(self, fn: str, status: int):
-        super().__init__(f"{fn}: {load().eagle_status_string(status).decode()} (status {status})")
+        msg = f"{fn}: {load().eagle_status_string(status).decode()} (status {status})"
+        if status == EAGLE_ERR_CUDA:
+            msg += f": {load().eagle_last_cuda_error_string().decode()}"
+        super().__init__(msg)
         self.status = status
 
 

@@ -11,6 +11,14 @@ using namespace eagle;
 
 namespace {
 
+thread_local cudaError_t t_last_cuda = cudaSuccess;
+
+int cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return EAGLE_OK;
+  t_last_cuda = e;
+  return EAGLE_ERR_CUDA;
+}
+
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 bool dtype_ok(int t) { return t == EAGLE_F32 || t == EAGLE_BF16; }
 
@@ -91,6 +99,10 @@ extern "C" {
 
 const char* eagle_version(void) { return "eagle-tree-gb300 0.1 (sm_103a)"; }
 
+int eagle_last_cuda_error(void) { return static_cast<int>(t_last_cuda); }
+
+const char* eagle_last_cuda_error_string(void) { return cudaGetErrorName(t_last_cuda); }
+
 const char* eagle_status_string(int status) {
   switch (status) {
     case EAGLE_OK: return "EAGLE_OK";
@@ -162,10 +174,8 @@ int eagle_tree_build(const eagle_tree_desc* d, int level, const void* frontier_l
       (u_draft && !aligned(u_draft, 4)))
     return EAGLE_ERR_ALIGNMENT;
   if (!ws || ws_bytes < p.total) return EAGLE_ERR_WORKSPACE;
-  return launch_tree_build(p, level, frontier_logits, u_draft, root_tok, seq_len, ws, *out,
-                           static_cast<cudaStream_t>(stream)) == cudaSuccess
-             ? EAGLE_OK
-             : EAGLE_ERR_CUDA;
+  return cuda_status(launch_tree_build(p, level, frontier_logits, u_draft, root_tok, seq_len, ws, *out,
+                           static_cast<cudaStream_t>(stream)));
 }
 
 int eagle_tree_attn(const eagle_attn_desc* d, const void* q, const void* k_cache, const void* v_cache,
@@ -182,10 +192,8 @@ int eagle_tree_attn(const eagle_attn_desc* d, const void* q, const void* k_cache
   AttnPlan p;
   plan_tree_attn(d, num_sms(), &p);
   if (p.total > 0 && (!ws || ws_bytes < p.total)) return EAGLE_ERR_WORKSPACE;
-  return launch_tree_attn(p, q, k_cache, v_cache, tree_k, tree_v, seq_len, anc_mask, out, lse, ws,
-                          static_cast<cudaStream_t>(stream)) == cudaSuccess
-             ? EAGLE_OK
-             : EAGLE_ERR_CUDA;
+  return cuda_status(launch_tree_attn(p, q, k_cache, v_cache, tree_k, tree_v, seq_len, anc_mask, out, lse, ws,
+                          static_cast<cudaStream_t>(stream)));
 }
 
 int eagle_accept(const eagle_accept_desc* d, const void* target_logits, const void* draft_logits,
@@ -203,10 +211,8 @@ int eagle_accept(const eagle_accept_desc* d, const void* target_logits, const vo
   AcceptPlan p;
   plan_accept(d, &p);
   if (!ws || ws_bytes < p.total) return EAGLE_ERR_WORKSPACE;
-  return launch_accept(p, target_logits, need_draft ? draft_logits : nullptr, tree_tokens, tree_parent, u_accept,
-                       u_final, *out, ws, static_cast<cudaStream_t>(stream)) == cudaSuccess
-             ? EAGLE_OK
-             : EAGLE_ERR_CUDA;
+  return cuda_status(launch_accept(p, target_logits, need_draft ? draft_logits : nullptr, tree_tokens, tree_parent, u_accept,
+                       u_final, *out, ws, static_cast<cudaStream_t>(stream)));
 }
 
 int eagle_kv_commit(const eagle_commit_desc* d, void* const* k_cache_layers, void* const* v_cache_layers,
@@ -243,10 +249,8 @@ int eagle_kv_commit(const eagle_commit_desc* d, void* const* k_cache_layers, voi
     const size_t rb = static_cast<size_t>(d->feat_dim) * fsz;
     if (rb % 16 == 0 && (!aligned(feat_cache, 16) || !aligned(tree_feat, 16))) return EAGLE_ERR_ALIGNMENT;
   }
-  return launch_kv_commit(d, a, n_acc, path, seq_len, commit_pos, feat_cache, tree_feat, status,
-                          static_cast<cudaStream_t>(stream)) == cudaSuccess
-             ? EAGLE_OK
-             : EAGLE_ERR_CUDA;
+  return cuda_status(launch_kv_commit(d, a, n_acc, path, seq_len, commit_pos, feat_cache, tree_feat, status,
+                          static_cast<cudaStream_t>(stream)));
 }
 
 }  // extern "C"

@@ -38,14 +38,22 @@ cudaError_t launch_tree_build(const TreeBuildPlan& p, int level, const void* log
 struct AttnPlan {
   int B, R, Hq, Hkv, G, D, P, dtype, W, out_dtype;
   bool precise;
+  bool tc;           // tcgen05 kernel
   float scale;
   int rows_per_cta;  // query rows (node x head-in-group) per CTA
   int row_blocks;
   int splits;
   int rows_pad;      // row_blocks * rows_per_cta
-  size_t off_o, off_ml, total;
+  size_t off_err, off_o, off_ml, total;
 };
 void plan_tree_attn(const eagle_attn_desc* d, int num_sms, AttnPlan* p);
+// Merge split partials into out / lse (shared by the mma.sync and tcgen05 kernels).
+cudaError_t launch_tree_attn_combine(const AttnPlan& p, void* out, float* lse, const float* part_o,
+                                     const float* part_ml, cudaStream_t s);
+// The tcgen05 kernel (plan.tc); ws holds the error word and the partials.
+cudaError_t launch_tree_attn_tc(const AttnPlan& p, const void* q, const void* k_cache, const void* v_cache,
+                                const void* tree_k, const void* tree_v, const int32_t* seq_len,
+                                const uint64_t* anc_mask, void* out, float* lse, void* ws, cudaStream_t s);
 cudaError_t launch_tree_attn(const AttnPlan& p, const void* q, const void* k_cache, const void* v_cache,
                              const void* tree_k, const void* tree_v, const int32_t* seq_len,
                              const uint64_t* anc_mask, void* out, float* lse, void* ws, cudaStream_t s);

@@ -476,43 +476,83 @@ void plan_tree_attn(const eagle_attn_desc* d, int num_sms, AttnPlan* p) {
   p->scale = d->scale;
   p->out_dtype = d->out_dtype;
   p->precise = d->precision == EAGLE_ATTN_PRECISE;
+  p->off_err = p->off_o = p->off_ml = p->total = 0;
+  p->tc = false;
   const int RG = p->R * p->G;
   if (p->dtype == EAGLE_F32) {
     p->rows_per_cta = 4;
     p->row_blocks = 1;
     p->splits = 1;
     p->rows_pad = RG;
-    p->off_o = p->off_ml = p->total = 0;
     return;
   }
-  const int nw = (RG <= 64) ? 4 : 8;
-  p->rows_per_cta = nw * 16;
+  // tcgen05 kernel: bf16, D = 128, M-tiles of 128 rows that hold whole nodes.
+  p->tc = d->engine == EAGLE_ENGINE_AUTO && p->D == 128 && (128 % p->G) == 0;
+  int key_tile, slots_per_sm;
+  if (p->tc) {
+    p->rows_per_cta = (RG <= 128) ? 128 : 256;
+    key_tile = 128;
+    slots_per_sm = 1;  // one CTA per SM: it holds all 512 TMEM columns
+  } else {
+    const int nw = (RG <= 64) ? 4 : 8;
+    p->rows_per_cta = nw * 16;
+    key_tile = BN;
+    slots_per_sm = (nw == 4) ? 2 : 1;
+  }
   p->row_blocks = (RG + p->rows_per_cta - 1) / p->rows_per_cta;
   p->rows_pad = p->row_blocks * p->rows_per_cta;
-  const int max_tiles = (p->P + BN - 1) / BN;
+  const int max_tiles = (p->P + key_tile - 1) / key_tile;
   int splits = d->num_splits;
   if (splits <= 0) {
-    const int slots = num_sms * ((nw == 4) ? 2 : 1);
     const int base = p->B * p->Hkv * p->row_blocks;
-    splits = slots / (base > 0 ? base : 1);
+    splits = num_sms * slots_per_sm / (base > 0 ? base : 1);
   }
   if (splits > max_tiles) splits = max_tiles;
   if (splits > 64) splits = 64;
   if (splits < 1) splits = 1;
   p->splits = splits;
-  if (splits == 1) {
-    p->off_o = p->off_ml = p->total = 0;
-    return;
+  size_t off = p->tc ? 256 : 0;  // tcgen05: error word first
+  if (splits > 1) {
+    const size_t rows = static_cast<size_t>(p->B) * p->Hkv * splits * p->rows_pad;
+    p->off_o = off;
+    off += ((rows * p->D * 4) + 255) / 256 * 256;
+    p->off_ml = off;
+    off += rows * 2 * 4;
   }
-  const size_t rows = static_cast<size_t>(p->B) * p->Hkv * splits * p->rows_pad;
-  p->off_o = 0;
-  p->off_ml = ((rows * p->D * 4) + 255) / 256 * 256;
-  p->total = p->off_ml + rows * 2 * 4;
+  p->total = off;
+}
+
+cudaError_t launch_tree_attn_combine(const AttnPlan& p, void* out, float* lse, const float* part_o,
+                                     const float* part_ml, cudaStream_t s) {
+  AttnArgs a{};
+  a.out = out;
+  a.lse = lse;
+  a.part_o = const_cast<float*>(part_o);
+  a.part_ml = const_cast<float*>(part_ml);
+  a.B = p.B;
+  a.R = p.R;
+  a.Hq = p.Hq;
+  a.Hkv = p.Hkv;
+  a.G = p.G;
+  a.P = p.P;
+  a.W = p.W;
+  a.splits = p.splits;
+  a.rows_pad = p.rows_pad;
+  a.out_f32 = p.out_dtype == EAGLE_F32;
+  a.scale = p.scale;
+  a.scale_log2 = p.scale * kLog2e;
+  dim3 cgrid((p.R * p.G + 3) / 4, p.B * p.Hkv);
+  if (p.D == 64)
+    tree_attn_combine_kernel<64><<<cgrid, 128, 0, s>>>(a);
+  else
+    tree_attn_combine_kernel<128><<<cgrid, 128, 0, s>>>(a);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_tree_attn(const AttnPlan& p, const void* q, const void* k_cache, const void* v_cache,
                              const void* tree_k, const void* tree_v, const int32_t* seq_len,
                              const uint64_t* anc_mask, void* out, float* lse, void* ws, cudaStream_t s) {
+  if (p.tc) return launch_tree_attn_tc(p, q, k_cache, v_cache, tree_k, tree_v, seq_len, anc_mask, out, lse, ws, s);
   if (p.dtype == EAGLE_F32) {
     const long long rows = static_cast<long long>(p.B) * p.R * p.Hq;
     const int grid = static_cast<int>((rows + 3) / 4);

@@ -1,0 +1,517 @@
+// tree_attn_tc.cu -- tree attention on the tcgen05 tensor cores (bf16, head_dim 128).
+//
+// Same operation as tree_attn.cu (EAGLE review, terms "tree attention": each
+// candidate attends only to its ancestors; lesson glossary "Tree attention"): row i
+// of a request attends to the prefix keys j < seq_len and to the tree keys whose bit
+// is set in its ancestor words.
+//
+// One CTA per (request, KV head, split, row block), 320 threads, warp-specialised:
+//   warp 8        TMA producer: Q once (one box per 128-row M-tile and 64-dim half),
+//                 then K and V tiles of 128 keys through two-stage rings.
+//   warp 9        allocates all 512 TMEM columns; lane 0 issues tcgen05.mma:
+//                 S_i = Q_i K^T (Q, K K-major, 128-byte swizzle) and O_i += P_i V (P from
+//                 TMEM, V MN-major); the warp zeroes V rows past the last valid key so
+//                 that masked keys contribute exactly 0.
+//   warps 0-3     online softmax of M-tile 0 (thread = row = TMEM lane),
+//   warps 4-7     of M-tile 1: read S_i, mask, running max, P = 2^((s - m) c) written
+//                 back into S_i's columns as packed bf16 (the PV A operand).  O is
+//                 rescaled in TMEM only when the row max grows by more than 2^8.
+// MMA issue order QK0 QK1 | PV0 QK0' PV1 QK1' | ... lets one warpgroup's softmax
+// overlap the other's MMAs.  TMEM columns: S0 [0,128) S1 [128,256) O0 [256,384)
+// O1 [384,512).  Splits write unnormalised partials (O, m, l) merged by the shared
+// combine kernel; a single split writes the output directly.
+//
+// Every mbarrier wait is bounded; a timeout ORs a bit into an error word at the
+// start of the workspace and the roles stop, so the kernel ends instead of hanging.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "common.cuh"
+#include "launch.h"
+#include "sm100.cuh"
+
+namespace eagle {
+namespace {
+
+using namespace sm100;
+
+constexpr int KT = 128;                   // keys per tile
+constexpr int HALF = 16384;               // one 64-dim half of a 128-row tile (bytes)
+constexpr int TILE = 2 * HALF;            // one K or V tile
+constexpr int NTHREADS = 320;
+constexpr int SM_Q = 0;                   // 2 M-tiles x 32 KB
+constexpr int SM_K = 2 * TILE;            // 2 stages
+constexpr int SM_V = 4 * TILE;            // 2 stages
+constexpr int SMEM_BYTES = 6 * TILE + 1024;
+__device__ __forceinline__ uint32_t col_s(int i) { return static_cast<uint32_t>(i) * 128u; }          // S_i / P_i
+__device__ __forceinline__ uint32_t col_o(int i) { return 256u + static_cast<uint32_t>(i) * 128u; }  // O_i
+constexpr float kRescaleLog2 = 8.f;       // lazy rescale threshold (log2 units)
+
+enum : int { ERR_Q = 1, ERR_KFULL = 2, ERR_KEMPTY = 4, ERR_VFULL = 8, ERR_VEMPTY = 16, ERR_S = 32, ERR_P = 64, ERR_O = 128 };
+
+struct TcArgs {
+  const int32_t* seq_len;
+  const uint64_t* anc_mask;
+  void* out;
+  float* lse;
+  float* part_o;   // [B*Hkv][splits][rows_pad][128]
+  float* part_ml;  // [B*Hkv][splits][rows_pad][2]
+  int* err;
+  int B, R, Hq, Hkv, G, P, W, splits, rows_pad, rows_per_cta, n_mt, out_f32;
+  float scale, scale_log2;
+};
+
+struct Tmaps {
+  CUtensorMap q;   // [B*R][Hq][128] bf16, box {64, G, 128/G}
+  CUtensorMap kc;  // [B*Hkv*P][128], box {64, 128}
+  CUtensorMap vc;
+  CUtensorMap tk;  // [B*Hkv*R][128], box {64, 128}
+  CUtensorMap tv;
+};
+
+struct TileInfo {
+  int n_pt, t_begin, n_tiles, L;
+};
+
+__device__ __forceinline__ TileInfo tile_info(const TcArgs& a, int b, int split) {
+  TileInfo ti;
+  int L = a.seq_len[b];
+  L = L < 0 ? 0 : (L > a.P ? a.P : L);
+  const int n_pref = (L + KT - 1) / KT;
+  ti.t_begin = static_cast<int>(static_cast<long long>(n_pref) * split / a.splits);
+  const int t_end = static_cast<int>(static_cast<long long>(n_pref) * (split + 1) / a.splits);
+  ti.n_pt = t_end - ti.t_begin;
+  ti.n_tiles = ti.n_pt + (split == a.splits - 1 ? 1 : 0);
+  ti.L = L;
+  return ti;
+}
+
+// Valid keys of tile t (prefix keys before L; tree rows before R).
+__device__ __forceinline__ int tile_valid(const TcArgs& a, const TileInfo& ti, int t) {
+  if (t < ti.n_pt) return min(KT, ti.L - (ti.t_begin + t) * KT);
+  return a.R;
+}
+
+template <bool PRECISE>
+__device__ __forceinline__ void issue_qk(uint32_t tb, const uint8_t* sQ, const uint8_t* sK, int i) {
+  constexpr uint32_t idesc = idesc_bf16_f32(128, KT, 0, 0);
+#pragma unroll
+  for (int ks = 0; ks < 8; ++ks) {
+    const uint32_t off = (ks >> 2) * HALF + (ks & 3) * 32;
+    mma_ss(tb + col_s(i), smem_desc_sw128(smem_u32(sQ + i * TILE) + off, 16, 1024),
+           smem_desc_sw128(smem_u32(sK) + off, 16, 1024), idesc, ks > 0);
+  }
+}
+
+template <bool PRECISE>
+__device__ __forceinline__ void issue_pv(uint32_t tb, const uint8_t* sV, int i, bool first) {
+  constexpr uint32_t idesc = idesc_bf16_f32(128, 128, 0, 1);
+#pragma unroll
+  for (int ks = 0; ks < 8; ++ks) {
+    const uint64_t bd = smem_desc_sw128(smem_u32(sV) + ks * 2048, HALF, 1024);
+    mma_ts(tb + col_o(i), tb + col_s(i) + ks * 8, bd, idesc, (first && ks == 0) ? 0u : 1u);
+    if constexpr (PRECISE) mma_ts(tb + col_o(i), tb + col_s(i) + 64 + ks * 8, bd, idesc, 1u);
+  }
+}
+
+template <bool PRECISE>
+__global__ void __launch_bounds__(NTHREADS, 1)
+    tree_attn_tc_kernel(const __grid_constant__ Tmaps tm, const TcArgs a) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  __shared__ uint64_t bar_q, k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[2], p_full[2], o_full;
+  __shared__ uint32_t tmem_base;
+  __shared__ int s_abort;
+
+  const int split = blockIdx.x, bh = blockIdx.y, rb = blockIdx.z;
+  const int b = bh / a.Hkv, h = bh % a.Hkv;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const TileInfo ti = tile_info(a, b, split);
+  const int n_mt = a.n_mt;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&bar_q, 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&k_full[s], 1);
+      mbar_init(&k_empty[s], 1);
+      mbar_init(&v_full[s], 1);
+      mbar_init(&v_empty[s], 1);
+      mbar_init(&s_full[s], 1);
+      mbar_init(&p_full[s], 128);
+    }
+    mbar_init(&o_full, 1);
+    s_abort = 0;
+    fence_barrier_init();
+  }
+  if (warp == 9) {
+    tmem_alloc(&tmem_base, 512);
+    tmem_relinquish();
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tb = tmem_base;
+  uint8_t* sQ = smem + SM_Q;
+
+  if (warp == 8) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0 && ti.n_tiles > 0) {
+      prefetch_tmap(&tm.q);
+      prefetch_tmap(&tm.kc);
+      prefetch_tmap(&tm.vc);
+      mbar_arrive_expect_tx(&bar_q, n_mt * TILE);
+      for (int i = 0; i < n_mt; ++i) {
+        const int node0 = (rb * a.rows_per_cta + i * 128) / a.G;
+        for (int hh = 0; hh < 2; ++hh)
+          tma_load_3d(sQ + i * TILE + hh * HALF, &tm.q, 64 * hh, h * a.G, b * a.R + node0, &bar_q);
+      }
+      const uint64_t policy = policy_evict_first();
+      for (int t = 0; t < ti.n_tiles; ++t) {
+        const int s = t & 1, use = t >> 1;
+        const bool tree = t >= ti.n_pt;
+        const CUtensorMap* mk = tree ? &tm.tk : &tm.kc;
+        const CUtensorMap* mv = tree ? &tm.tv : &tm.vc;
+        const int y = tree ? bh * a.R : bh * a.P + (ti.t_begin + t) * KT;
+        if (use > 0 && !wait_parity(&k_empty[s], (use - 1) & 1, a.err, ERR_KEMPTY)) break;
+        mbar_arrive_expect_tx(&k_full[s], TILE);
+        tma_load_2d_hint(smem + SM_K + s * TILE, mk, 0, y, &k_full[s], policy);
+        tma_load_2d_hint(smem + SM_K + s * TILE + HALF, mk, 64, y, &k_full[s], policy);
+        if (use > 0 && !wait_parity(&v_empty[s], (use - 1) & 1, a.err, ERR_VEMPTY)) break;
+        mbar_arrive_expect_tx(&v_full[s], TILE);
+        tma_load_2d_hint(smem + SM_V + s * TILE, mv, 0, y, &v_full[s], policy);
+        tma_load_2d_hint(smem + SM_V + s * TILE + HALF, mv, 64, y, &v_full[s], policy);
+      }
+    }
+  } else if (warp == 9) {
+    // ------------------------------------------------------------ MMA issuer
+    bool ok = ti.n_tiles > 0;
+    if (ok && lane == 0) ok = wait_parity(&bar_q, 0, a.err, ERR_Q);
+    ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+    auto qk = [&](int t) {  // both M-tiles of tile t; lane 0
+      const int s = t & 1;
+      if (!wait_parity(&k_full[s], (t >> 1) & 1, a.err, ERR_KFULL)) return false;
+      tc_fence_after();
+      for (int i = 0; i < n_mt; ++i) {
+        issue_qk<PRECISE>(tb, sQ, smem + SM_K + s * TILE, i);
+        mma_commit(&s_full[i]);
+      }
+      mma_commit(&k_empty[s]);
+      return true;
+    };
+    if (ok && lane == 0) ok = qk(0);
+    ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+    for (int t = 0; t < ti.n_tiles && ok; ++t) {
+      const int s = t & 1;
+      // V of tile t: wait, then zero the rows past the last valid key
+      ok = wait_parity(&v_full[s], (t >> 1) & 1, a.err, ERR_VFULL);
+      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+      if (!ok) break;
+      const int nv = tile_valid(a, ti, t);
+      if (nv < KT) {
+        uint8_t* sv = smem + SM_V + s * TILE;
+        for (int idx = lane; idx < (KT - nv) * 16; idx += 32) {
+          const int row = nv + (idx >> 4), part = idx & 15;
+          *reinterpret_cast<uint4*>(sv + (part >> 3) * HALF + row * 128 + (part & 7) * 16) = make_uint4(0, 0, 0, 0);
+        }
+        fence_proxy_async_smem();
+      }
+      __syncwarp();
+      if (lane == 0) {
+        uint8_t* sv = smem + SM_V + s * TILE;
+        for (int i = 0; i < n_mt && ok; ++i) {
+          ok = wait_parity(&p_full[i], t & 1, a.err, ERR_P);
+          if (!ok) break;
+          tc_fence_after();
+          issue_pv<PRECISE>(tb, sv, i, t == 0);
+          if (i == 0 && t + 1 < ti.n_tiles) {
+            // next tile's S0 as soon as PV0 is queued (tensor core stays busy while
+            // warpgroup 1 finishes its softmax)
+            const int s1 = (t + 1) & 1;
+            if (!wait_parity(&k_full[s1], ((t + 1) >> 1) & 1, a.err, ERR_KFULL)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            issue_qk<PRECISE>(tb, sQ, smem + SM_K + s1 * TILE, 0);
+            mma_commit(&s_full[0]);
+            if (n_mt == 1) mma_commit(&k_empty[s1]);
+          }
+        }
+        if (ok) {
+          mma_commit(&v_empty[s]);
+          if (n_mt == 2 && t + 1 < ti.n_tiles) {
+            const int s1 = (t + 1) & 1;
+            issue_qk<PRECISE>(tb, sQ, smem + SM_K + s1 * TILE, 1);
+            mma_commit(&s_full[1]);
+            mma_commit(&k_empty[s1]);
+          }
+        }
+      }
+      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+    }
+    if (lane == 0 && ti.n_tiles > 0) mma_commit(&o_full);
+  } else if (warp < 4 * n_mt) {
+    // ------------------------------------------------------------ softmax warpgroup i
+    const int i = warp >> 2;                 // M-tile
+    const int qd = warp & 3;                 // TMEM lane quarter
+    const int r_local = qd * 32 + lane;      // row within the M-tile = TMEM lane
+    const int row = rb * a.rows_per_cta + i * 128 + r_local;
+    const bool vrow = row < a.R * a.G;
+    const int node = vrow ? row / a.G : 0;
+    const int hq = h * a.G + (vrow ? row % a.G : 0);
+    uint64_t mw0 = 0, mw1 = 0;
+    if (vrow) {
+      mw0 = a.anc_mask[(static_cast<size_t>(b) * a.R + node) * a.W];
+      if (a.W > 1) mw1 = a.anc_mask[(static_cast<size_t>(b) * a.R + node) * a.W + 1];
+    }
+    const uint32_t lb = tb + (static_cast<uint32_t>(qd * 32) << 16);
+    const float sl2 = a.scale_log2;
+    float m_ref = -INFINITY, l = 0.f;
+    bool ok = true;
+    for (int t = 0; t < ti.n_tiles && ok; ++t) {
+      ok = __all_sync(0xffffffffu, wait_parity(&s_full[i], t & 1, a.err, ERR_S));
+      if (!ok) break;
+      tc_fence_after();
+      const bool tree = t >= ti.n_pt;
+      const int nv = tile_valid(a, ti, t);
+      // key k of this tile counts for this row
+      auto keep = [&](int k) {
+        return vrow && (tree ? (k < a.R && (((k < 64 ? mw0 >> k : mw1 >> (k - 64)) & 1ull) != 0)) : k < nv);
+      };
+      // pass 1: row max over the valid keys, 32 columns at a time
+      float mx = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t r[32];
+        tmem_ld32(lb + col_s(i) + 32 * c, r);
+        tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          if (keep(32 * c + j)) mx = fmaxf(mx, __uint_as_float(r[j]));
+      }
+      const float m_new = fmaxf(m_ref, mx);
+      // lazy rescale: move this row's reference max only when it grew by > 2^8; O
+      // holds earlier tiles only when m_ref is already finite.  tcgen05.ld/st are
+      // warp-collective, so the whole warp touches O when any of its rows must.
+      const bool move = m_new != -INFINITY && (m_ref == -INFINITY || (m_new - m_ref) * sl2 > kRescaleLog2);
+      const bool scale_o = move && m_ref != -INFINITY;
+      const float alpha = scale_o ? exp2f((m_ref - m_new) * sl2) : 1.f;
+      if (__any_sync(0xffffffffu, scale_o)) {
+        l *= alpha;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t o[32];
+          tmem_ld32(lb + col_o(i) + 32 * c, o);
+          tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha);
+          tmem_st32(lb + col_o(i) + 32 * c, o);
+        }
+        tmem_st_wait();
+      }
+      if (move) m_ref = m_new;
+      const float mu = (m_ref == -INFINITY) ? 0.f : m_ref * sl2;
+      // pass 2: P = 2^(s c - m c) as bf16 pairs into S_i's first 64 columns.  Chunk c
+      // (columns 32c..32c+31) is read before its P lands in columns 16c..16c+15, so no
+      // unread S is overwritten.  The precise path also writes the low parts into
+      // columns 64..127, so it holds chunks 2 and 3 in registers first.
+      uint32_t keep23[PRECISE ? 64 : 1];
+      if constexpr (PRECISE) {
+        tmem_ld32(lb + col_s(i) + 64, *reinterpret_cast<uint32_t(*)[32]>(&keep23[0]));
+        tmem_ld32(lb + col_s(i) + 96, *reinterpret_cast<uint32_t(*)[32]>(&keep23[32]));
+        tmem_ld_wait();
+      }
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t r[32];
+        if (PRECISE && c >= 2) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) r[j] = keep23[(c - 2) * 32 + j];
+        } else {
+          tmem_ld32(lb + col_s(i) + 32 * c, r);
+          tmem_ld_wait();
+        }
+        uint32_t hi[16], lo[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const int k0 = 32 * c + 2 * j;
+          const float p0 = keep(k0) ? exp2f(fmaf(__uint_as_float(r[2 * j]), sl2, -mu)) : 0.f;
+          const float p1 = keep(k0 + 1) ? exp2f(fmaf(__uint_as_float(r[2 * j + 1]), sl2, -mu)) : 0.f;
+          __nv_bfloat162 u = __floats2bfloat162_rn(p0, p1);
+          hi[j] = *reinterpret_cast<uint32_t*>(&u);
+          const float h0 = __uint_as_float(hi[j] << 16), h1 = __uint_as_float(hi[j] & 0xffff0000u);
+          if constexpr (PRECISE) {
+            __nv_bfloat162 w = __floats2bfloat162_rn(p0 - h0, p1 - h1);
+            lo[j] = *reinterpret_cast<uint32_t*>(&w);
+            l += (h0 + __uint_as_float(lo[j] << 16)) + (h1 + __uint_as_float(lo[j] & 0xffff0000u));
+          } else {
+            l += h0 + h1;
+          }
+        }
+        tmem_st16(lb + col_s(i) + 16 * c, hi);
+        if constexpr (PRECISE) tmem_st16(lb + col_s(i) + 64 + 16 * c, lo);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(&p_full[i]);
+    }
+    // ---- epilogue: O from TMEM to the output (one split) or the partials
+    const bool have = ok && ti.n_tiles > 0;
+    bool done = have ? __all_sync(0xffffffffu, wait_parity(&o_full, 0, a.err, ERR_O)) : false;
+    tc_fence_after();
+    const size_t prow = (static_cast<size_t>(bh) * a.splits + split) * a.rows_pad + row;
+    const float inv = (a.splits == 1 && l > 0.f) ? 1.f / l : 1.f;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      uint32_t o[32];
+      if (done) {
+        tmem_ld32(lb + col_o(i) + 32 * c, o);
+        tmem_ld_wait();
+      } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) o[j] = 0u;
+      }
+      if (!vrow) continue;
+      if (a.splits == 1) {
+        const size_t orow = (static_cast<size_t>(b * a.R + node) * a.Hq + hq) * 128 + 32 * c;
+        if (a.out_f32) {
+          float4* dst = reinterpret_cast<float4*>(static_cast<float*>(a.out) + orow);
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            dst[j] = make_float4(__uint_as_float(o[4 * j]) * inv, __uint_as_float(o[4 * j + 1]) * inv,
+                                 __uint_as_float(o[4 * j + 2]) * inv, __uint_as_float(o[4 * j + 3]) * inv);
+        } else {
+          uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.out) + orow);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            uint32_t w[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              __nv_bfloat162 u = __floats2bfloat162_rn(__uint_as_float(o[8 * j + 2 * e]) * inv,
+                                                       __uint_as_float(o[8 * j + 2 * e + 1]) * inv);
+              w[e] = *reinterpret_cast<uint32_t*>(&u);
+            }
+            dst[j] = make_uint4(w[0], w[1], w[2], w[3]);
+          }
+        }
+      } else {
+        float4* dst = reinterpret_cast<float4*>(a.part_o + prow * 128 + 32 * c);
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          dst[j] = make_float4(__uint_as_float(o[4 * j]), __uint_as_float(o[4 * j + 1]), __uint_as_float(o[4 * j + 2]),
+                               __uint_as_float(o[4 * j + 3]));
+      }
+    }
+    if (vrow) {
+      if (a.splits == 1) {
+        if (a.lse) a.lse[static_cast<size_t>(b * a.R + node) * a.Hq + hq] = a.scale * m_ref + logf(l);
+      } else {
+        *reinterpret_cast<float2*>(a.part_ml + prow * 2) = make_float2(done ? m_ref : -INFINITY, done ? l : 0.f);
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 9) {
+    tc_fence_after();
+    tmem_dealloc(tb, 512);
+  }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+// bf16 tensor map of `rank` dims (innermost first), 128-byte swizzle, zero fill.
+bool make_tmap(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims, const cuuint64_t* strides,
+               const cuuint32_t* box) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint32_t es[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <bool PRECISE>
+cudaError_t launch_tc(const Tmaps& tm, const TcArgs& a, dim3 grid, cudaStream_t s) {
+  auto kern = tree_attn_tc_kernel<PRECISE>;
+  static unsigned long long configured = 0;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev >= 64 || !(__atomic_load_n(&configured, __ATOMIC_ACQUIRE) & (1ull << dev))) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    if (dev < 64) __atomic_fetch_or(&configured, 1ull << dev, __ATOMIC_RELEASE);
+  }
+  kern<<<grid, NTHREADS, SMEM_BYTES, s>>>(tm, a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_tree_attn_tc(const AttnPlan& p, const void* q, const void* k_cache, const void* v_cache,
+                                const void* tree_k, const void* tree_v, const int32_t* seq_len,
+                                const uint64_t* anc_mask, void* out, float* lse, void* ws, cudaStream_t s) {
+  Tmaps tm;
+  const cuuint64_t D = 128;
+  {
+    const cuuint64_t dims[3] = {D, static_cast<cuuint64_t>(p.Hq), static_cast<cuuint64_t>(p.B) * p.R};
+    const cuuint64_t strides[2] = {D * 2, static_cast<cuuint64_t>(p.Hq) * D * 2};
+    const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(p.G), static_cast<cuuint32_t>(128 / p.G)};
+    if (!make_tmap(&tm.q, q, 3, dims, strides, box)) return cudaErrorInvalidValue;
+  }
+  {
+    const cuuint64_t dims[2] = {D, static_cast<cuuint64_t>(p.B) * p.Hkv * p.P};
+    const cuuint64_t strides[1] = {D * 2};
+    const cuuint32_t box[2] = {64, 128};
+    if (!make_tmap(&tm.kc, k_cache, 2, dims, strides, box)) return cudaErrorInvalidValue;
+    if (!make_tmap(&tm.vc, v_cache, 2, dims, strides, box)) return cudaErrorInvalidValue;
+  }
+  {
+    const cuuint64_t dims[2] = {D, static_cast<cuuint64_t>(p.B) * p.Hkv * p.R};
+    const cuuint64_t strides[1] = {D * 2};
+    const cuuint32_t box[2] = {64, 128};
+    if (!make_tmap(&tm.tk, tree_k, 2, dims, strides, box)) return cudaErrorInvalidValue;
+    if (!make_tmap(&tm.tv, tree_v, 2, dims, strides, box)) return cudaErrorInvalidValue;
+  }
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  TcArgs a;
+  a.seq_len = seq_len;
+  a.anc_mask = anc_mask;
+  a.out = out;
+  a.lse = lse;
+  a.part_o = p.splits > 1 ? reinterpret_cast<float*>(w + p.off_o) : nullptr;
+  a.part_ml = p.splits > 1 ? reinterpret_cast<float*>(w + p.off_ml) : nullptr;
+  a.err = reinterpret_cast<int*>(w + p.off_err);
+  a.B = p.B;
+  a.R = p.R;
+  a.Hq = p.Hq;
+  a.Hkv = p.Hkv;
+  a.G = p.G;
+  a.P = p.P;
+  a.W = p.W;
+  a.splits = p.splits;
+  a.rows_pad = p.rows_pad;
+  a.rows_per_cta = p.rows_per_cta;
+  a.n_mt = p.rows_per_cta / 128;
+  a.out_f32 = p.out_dtype == EAGLE_F32;
+  a.scale = p.scale;
+  a.scale_log2 = p.scale * kLog2e;
+  cudaError_t e = cudaMemsetAsync(a.err, 0, sizeof(int), s);
+  if (e != cudaSuccess) return e;
+  dim3 grid(p.splits, p.B * p.Hkv, p.row_blocks);
+  e = p.precise ? launch_tc<true>(tm, a, grid, s) : launch_tc<false>(tm, a, grid, s);
+  if (e != cudaSuccess || p.splits == 1) return e;
+  return launch_tree_attn_combine(p, out, lse, a.part_o, a.part_ml, s);
+}
+
+}  // namespace eagle

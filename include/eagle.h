@@ -101,6 +101,11 @@ enum {
                               step; for sharply peaked rows where bf16 rounding of P shows */
 };
 
+/* Attention kernel selection.  The tcgen05 kernel covers bf16 inputs with head_dim 128
+ * and 128 % (Hq / Hkv) == 0; everything else runs the mma.sync (bf16) or SIMT (fp32)
+ * kernels. */
+enum { EAGLE_ENGINE_AUTO = 0, EAGLE_ENGINE_MMA_SYNC = 1 };
+
 /* Workspace kinds for eagle_workspace_size() */
 enum { EAGLE_WS_TREE_BUILD = 1, EAGLE_WS_TREE_ATTN = 2, EAGLE_WS_ACCEPT = 3 };
 
@@ -169,6 +174,8 @@ typedef struct {
   int32_t num_splits;  /* prefix splits per (request, KV head); 0 = choose from the SM count */
   int32_t out_dtype;   /* element type of out: EAGLE_F32, or EAGLE_BF16 when dtype is EAGLE_BF16 */
   int32_t precision;   /* EAGLE_ATTN_STANDARD or EAGLE_ATTN_PRECISE (ignored for fp32 inputs) */
+  int32_t engine;      /* EAGLE_ENGINE_AUTO (tensor-core tcgen05 kernel where supported) or
+                          EAGLE_ENGINE_MMA_SYNC (the legacy warp-level MMA kernel) */
 } eagle_attn_desc;
 
 /* One layer of tree attention.  Row i of request b, query head hq attends to the
@@ -178,7 +185,10 @@ typedef struct {
  *   q [B][R][Hq][D]; k_cache, v_cache [B][Hkv][P][D]; tree_k, tree_v [B][Hkv][R][D];
  *   seq_len [B] int32 (0 <= seq_len <= P); anc_mask [B][R][W]; out [B][R][Hq][D];
  *   lse [B][R][Hq] fp32, may be NULL.
- * ws: eagle_workspace_size(EAGLE_WS_TREE_ATTN, d) bytes (split partials).
+ * ws: eagle_workspace_size(EAGLE_WS_TREE_ATTN, d) bytes (split partials).  The tcgen05
+ * kernel keeps an error word in the first 16 bytes of ws (cleared by the call): a
+ * non-zero value after the stream completes means a bounded wait inside the kernel
+ * gave up, and the outputs of that call are not valid.
  * Unsupported: head_dim not 64/128, R > 128, Hq % Hkv != 0, B * Hkv > 65535, bf16 out
  * with fp32 inputs. */
 int eagle_tree_attn(const eagle_attn_desc* d, const void* q, const void* k_cache, const void* v_cache,
@@ -262,6 +272,11 @@ const char* eagle_status_string(int status);
 
 /* Library version string. */
 const char* eagle_version(void);
+
+/* The CUDA error behind the calling thread's most recent EAGLE_ERR_CUDA (a
+ * cudaError_t value, 0 if none), and its name.  Thread-local, like cudaGetLastError. */
+int eagle_last_cuda_error(void);
+const char* eagle_last_cuda_error_string(void);
 
 #ifdef __cplusplus
 }

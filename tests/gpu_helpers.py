@@ -34,13 +34,13 @@ def random_tree(rows: int, seed: int, chain: bool = False):
 
 def run_attn(w: synth.Workload, batch: int, seq_len: np.ndarray, rows: int, parent: np.ndarray,
              mask: np.ndarray, layer: int = 0, q_scale: float = 1.0, num_splits: int = 0, out_f32: bool = False,
-             precision: int = B.EAGLE_ATTN_STANDARD):
+             precision: int = B.EAGLE_ATTN_STANDARD, engine: int = B.EAGLE_ENGINE_AUTO):
     """Generate one layer's inputs and run eagle_tree_attn; returns host inputs and outputs."""
     q, kc, vc, tk, tv = synth.attn_tensors(w, layer, batch, seq_len, rows, q_scale)
     dt = B.EAGLE_F32 if w.dtype == "f32" else B.EAGLE_BF16
     odt = B.EAGLE_F32 if (out_f32 or w.dtype == "f32") else B.EAGLE_BF16
     desc = B.AttnDesc(batch, rows, w.n_q_heads, w.n_kv_heads, w.head_dim, w.max_seq, 1.0 / math.sqrt(w.head_dim),
-                      dt, num_splits, odt, precision)
+                      dt, num_splits, odt, precision, engine)
     ws = torch.zeros(B.workspace_size(B.EAGLE_WS_TREE_ATTN, desc), dtype=torch.uint8, device="cuda")
     tq = dev(q, w.dtype)
     out = torch.empty(tq.shape, dtype=torch.float32 if odt == B.EAGLE_F32 else torch.bfloat16, device="cuda")
@@ -49,7 +49,15 @@ def run_attn(w: synth.Workload, batch: int, seq_len: np.ndarray, rows: int, pare
     B.eagle_tree_attn(desc, tq, dev(kc, w.dtype), dev(vc, w.dtype), dev(tk, w.dtype), dev(tv, w.dtype),
                       torch.from_numpy(np.asarray(seq_len, np.int32)).cuda(), am, out, lse, ws)
     torch.cuda.synchronize()
+    if ws.numel() >= 4:  # the tensor-core kernel's error word (bounded waits that gave up)
+        assert int(ws[:4].view(torch.int32).item()) == 0 or not is_tc(desc), "tcgen05 kernel wait timed out"
     return (q, kc, vc, tk, tv), out.float().cpu().numpy(), lse.cpu().numpy()
+
+
+def is_tc(desc) -> bool:
+    """Whether a descriptor runs the tcgen05 kernel (bf16, head_dim 128, G divides 128, auto engine)."""
+    G = desc.n_q_heads // desc.n_kv_heads
+    return desc.dtype == B.EAGLE_BF16 and desc.head_dim == 128 and 128 % G == 0 and desc.engine == B.EAGLE_ENGINE_AUTO
 
 
 def head_slice(inputs, h: int, G: int, b: int):

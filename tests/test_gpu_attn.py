@@ -19,9 +19,10 @@ pytestmark = pytest.mark.gpu
 W = synth.WORKLOADS
 
 
-def _run_one(w, batch, seq_len, rows, par, mask, heads, q_scale, num_splits, out_f32, precision, bound_fn):
+def _run_one(w, batch, seq_len, rows, par, mask, heads, q_scale, num_splits, out_f32, precision, bound_fn,
+             engine=B.EAGLE_ENGINE_AUTO):
     inputs, out, lse = run_attn(w, batch, seq_len, rows, par, mask, q_scale=q_scale, num_splits=num_splits,
-                                out_f32=out_f32, precision=precision)
+                                out_f32=out_f32, precision=precision, engine=engine)
     G = w.group
     tol = F32_TOL if w.dtype == "f32" else BF16_TOL
     worst = 0.0
@@ -30,7 +31,7 @@ def _run_one(w, batch, seq_len, rows, par, mask, heads, q_scale, num_splits, out
         ref, ref_lse = oracle.tree_attn(*sub, seq_len[b:b + 1], par[None], 1.0 / np.sqrt(w.head_dim))
         err = np.abs(out[b:b + 1, :, h * G:(h + 1) * G] - ref)
         bound = bound_fn(ref, sub)
-        assert (err <= bound).all(), (f"b={b} h={h} precision={precision} out_f32={out_f32}: max abs error "
+        assert (err <= bound).all(), (f"b={b} h={h} engine={engine} precision={precision} out_f32={out_f32}: max abs error "
                                       f"{err.max():.3e}, worst excess {(err - bound).max():.3e}")
         worst = max(worst, float(err.max()))
         lerr = float(np.abs(lse[b:b + 1, :, h * G:(h + 1) * G] - ref_lse).max())
@@ -42,7 +43,8 @@ def _check(w, batch, seq_len, rows, par, mask, heads, q_scale=1.0, num_splits=0,
     """Check one case against the oracle.
 
     fp32 inputs: max abs error < 1e-5.
-    bf16 inputs, two launches:
+    bf16 inputs, three launches (the tensor-core kernel where it applies, plus the
+    legacy warp-MMA kernel on the standard path):
       * precise PV path with fp32 output: max abs error < 2e-3 (the stated bound);
       * the benchmark's launch (standard PV path, bf16 output): P rounded to bf16
         (unit roundoff u = 2^-8) moves O by at most u/(1-u) * max_j |v_j - O| <=
@@ -63,6 +65,9 @@ def _check(w, batch, seq_len, rows, par, mask, heads, q_scale=1.0, num_splits=0,
             return BF16_TOL + u * np.abs(ref)
         return BF16_TOL + u / (1 - u) * 2 * vmax + u * np.abs(ref)
 
+    # the standard path on both kernels: tensor-core (auto) and the legacy warp-MMA one
+    _run_one(w, batch, seq_len, rows, par, mask, heads, q_scale, num_splits, False, B.EAGLE_ATTN_STANDARD, derived,
+             engine=B.EAGLE_ENGINE_MMA_SYNC)
     return _run_one(w, batch, seq_len, rows, par, mask, heads, q_scale, num_splits, False, B.EAGLE_ATTN_STANDARD,
                     derived)
 
