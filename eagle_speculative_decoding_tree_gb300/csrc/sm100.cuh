@@ -113,6 +113,43 @@ __device__ __forceinline__ void prefetch_tmap(const void* tmap) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");
 }
 
+// 2-D tiled store of one box from shared memory (bulk-group completion).  Writers of
+// the box must have issued fence_proxy_async_smem() and synchronised before this.
+__device__ __forceinline__ void tma_store_2d(const void* tmap, const void* src, int x, int y) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(tmap)),
+               "r"(smem_u32(src)), "r"(x), "r"(y)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Wait until every committed bulk store has finished reading shared memory.
+__device__ __forceinline__ void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+
+// ------------------------------------------------------------------ named barriers
+// Barrier `id` over `count` threads (a multiple of 32) that also returns whether
+// `pred` held in every participating thread.
+__device__ __forceinline__ bool bar_and(int id, int count, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n .reg .pred p, q;\n setp.ne.u32 p, %3, 0;\n barrier.cta.red.and.pred q, %1, %2, p;\n selp.u32 %0, 1, 0, q;\n}\n"
+      : "=r"(r)
+      : "r"(id), "r"(count), "r"(pred ? 1u : 0u)
+      : "memory");
+  return r != 0;
+}
+__device__ __forceinline__ void bar_sync(int id, int count) {
+  asm volatile("barrier.cta.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
+// ------------------------------------------------------------------ special functions
+// 2^x on the multi-function unit (PTX ex2.approx, subnormal results flushed to 0;
+// 2^-inf = 0).
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // ------------------------------------------------------------------ tensor memory
 // Allocation is done by one whole warp; the allocated base address is written to
 // shared memory.  ncols is a power of two in [32, 512].

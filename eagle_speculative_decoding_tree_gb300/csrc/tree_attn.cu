@@ -344,6 +344,9 @@ __global__ void __launch_bounds__(NW * 32, (NW == 4) ? 2 : 1) tree_attn_mma_kern
 }
 
 // Merge split partials: M = max m_s, L = sum l_s 2^((m_s - M) c), O = sum O_s 2^((m_s - M) c) / L.
+// One warp per row: lane s holds split s's (m, l) (splits <= 64, two per lane), the
+// weights travel by shuffle, and the partial rows are loaded eight splits at a time
+// so that the loads overlap.
 template <int D>
 __global__ void __launch_bounds__(128) tree_attn_combine_kernel(const AttnArgs a) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -354,29 +357,54 @@ __global__ void __launch_bounds__(128) tree_attn_combine_kernel(const AttnArgs a
   const int nd = r / a.G, hq = h * a.G + r % a.G;
   constexpr int PER = D / 32;
   const size_t base = static_cast<size_t>(bh) * a.splits * a.rows_pad + r;
-  float M = -INFINITY;
-  for (int s = 0; s < a.splits; ++s) M = fmaxf(M, a.part_ml[(base + static_cast<size_t>(s) * a.rows_pad) * 2]);
+  float m2[2], l2[2];
+#pragma unroll
+  for (int k = 0; k < 2; ++k) {
+    const int s = lane + 32 * k;
+    float2 ml = make_float2(-INFINITY, 0.f);
+    if (s < a.splits) ml = *reinterpret_cast<const float2*>(a.part_ml + (base + static_cast<size_t>(s) * a.rows_pad) * 2);
+    m2[k] = ml.x;
+    l2[k] = ml.y;
+  }
+  const float M = warp_max(fmaxf(m2[0], m2[1]));
+  float w2[2];
+#pragma unroll
+  for (int k = 0; k < 2; ++k) w2[k] = (m2[k] == -INFINITY) ? 0.f : exp2f((m2[k] - M) * a.scale_log2);
+  const float Ls = warp_sum(l2[0] * w2[0] + l2[1] * w2[1]);
   float acc[PER];
 #pragma unroll
   for (int e = 0; e < PER; ++e) acc[e] = 0.f;
-  float Ls = 0.f;
-  for (int s = 0; s < a.splits; ++s) {
-    const size_t prow = base + static_cast<size_t>(s) * a.rows_pad;
-    const float2 ml = *reinterpret_cast<const float2*>(a.part_ml + prow * 2);
-    const float w = (ml.x == -INFINITY) ? 0.f : exp2f((ml.x - M) * a.scale_log2);
-    Ls += ml.y * w;
-    const float* po = a.part_o + prow * D + lane * PER;
-    if constexpr (PER == 4) {
-      const float4 v = *reinterpret_cast<const float4*>(po);
-      acc[0] += w * v.x;
-      acc[1] += w * v.y;
-      acc[2] += w * v.z;
-      acc[3] += w * v.w;
-    } else {
-      const float2 v = *reinterpret_cast<const float2*>(po);
-      acc[0] += w * v.x;
-      acc[1] += w * v.y;
+  const float* po0 = a.part_o + base * D + lane * PER;
+  const size_t sstride = static_cast<size_t>(a.rows_pad) * D;
+  for (int s0 = 0; s0 < a.splits; s0 += 8) {
+    float v[8][PER], wv[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int s = s0 + u;
+      wv[u] = __shfl_sync(0xffffffffu, s < 32 ? w2[0] : w2[1], s & 31);
+      if (s < a.splits) {
+        const float* po = po0 + static_cast<size_t>(s) * sstride;
+        if constexpr (PER == 4) {
+          const float4 t = *reinterpret_cast<const float4*>(po);
+          v[u][0] = t.x;
+          v[u][1] = t.y;
+          v[u][2] = t.z;
+          v[u][3] = t.w;
+        } else {
+          const float2 t = *reinterpret_cast<const float2*>(po);
+          v[u][0] = t.x;
+          v[u][1] = t.y;
+        }
+      } else {
+        wv[u] = 0.f;
+#pragma unroll
+        for (int e = 0; e < PER; ++e) v[u][e] = 0.f;
+      }
     }
+#pragma unroll
+    for (int u = 0; u < 8; ++u)
+#pragma unroll
+      for (int e = 0; e < PER; ++e) acc[e] = fmaf(wv[u], v[u][e], acc[e]);
   }
   const float inv = 1.f / Ls;
   const size_t orow = (static_cast<size_t>(b * a.R + nd) * a.Hq + hq) * D + lane * PER;

@@ -12,19 +12,23 @@
 //                 S_i = Q_i K^T (Q, K K-major, 128-byte swizzle) and O_i += P_i V (P from
 //                 TMEM, V MN-major); the warp zeroes V rows past the last valid key so
 //                 that masked keys contribute exactly 0.
-//   warps 0-3     online softmax of M-tile 0 (thread = row = TMEM lane),
-//   warps 4-7     of M-tile 1: read S_i, mask, running max, P = 2^((s - m) c) written
-//                 back into S_i's columns as packed bf16 (the PV A operand).  O is
-//                 rescaled in TMEM only when the row max grows by more than 2^8.
-// MMA issue order QK0 QK1 | PV0 QK0' PV1 QK1' | ... lets one warpgroup's softmax
-// overlap the other's MMAs.  TMEM columns: S0 [0,128) S1 [128,256) O0 [256,384)
-// O1 [384,512).  Splits write unnormalised partials (O, m, l) merged by the shared
-// combine kernel; a single split writes the output directly.
+//   warps 0-7     online softmax, all eight on one M-tile at a time: warp w takes
+//                 TMEM lane quarter w & 3 (32 rows) and key half w >> 2; the halves of
+//                 a row agree on its max through shared memory.  P = 2^((s - m) c) goes
+//                 back into the half's own S columns as packed bf16 (the PV A operand).
+//                 O is rescaled in TMEM only when the row max grows by more than 2^8.
+// MMA issue order QK0 QK1 | PV0 QK0' PV1 QK1' | ...: the tensor cores run M-tile 0's
+// PV and next QK while the warps do M-tile 1's softmax, and the other way round.
+// TMEM columns: S0 [0,128) S1 [128,256) O0 [256,384) O1 [384,512).  Splits write
+// unnormalised partials (O, m, l), O by TMA store, merged by the shared combine
+// kernel; a single split writes the output directly.
 //
 // Every mbarrier wait is bounded; a timeout ORs a bit into an error word at the
 // start of the workspace and the roles stop, so the kernel ends instead of hanging.
 #include <cuda.h>
 #include <cudaTypedefs.h>
+
+#include <cstring>
 
 #include "common.cuh"
 #include "launch.h"
@@ -67,6 +71,7 @@ struct Tmaps {
   CUtensorMap vc;
   CUtensorMap tk;  // [B*Hkv*R][128], box {64, 128}
   CUtensorMap tv;
+  CUtensorMap po;  // fp32 partial O [B*Hkv*splits*rows_pad][128], box {32, 128}
 };
 
 struct TileInfo {
@@ -77,11 +82,15 @@ __device__ __forceinline__ TileInfo tile_info(const TcArgs& a, int b, int split)
   TileInfo ti;
   int L = a.seq_len[b];
   L = L < 0 ? 0 : (L > a.P ? a.P : L);
+  // units of work: the prefix tiles, then the tree tile; split s takes units
+  // [U s / S, U (s + 1) / S), so only the last split holds the tree tile
   const int n_pref = (L + KT - 1) / KT;
-  ti.t_begin = static_cast<int>(static_cast<long long>(n_pref) * split / a.splits);
-  const int t_end = static_cast<int>(static_cast<long long>(n_pref) * (split + 1) / a.splits);
-  ti.n_pt = t_end - ti.t_begin;
-  ti.n_tiles = ti.n_pt + (split == a.splits - 1 ? 1 : 0);
+  const int U = n_pref + 1;
+  const int u0 = static_cast<int>(static_cast<long long>(U) * split / a.splits);
+  const int u1 = static_cast<int>(static_cast<long long>(U) * (split + 1) / a.splits);
+  ti.t_begin = u0;
+  ti.n_pt = max(0, min(u1, n_pref) - u0);
+  ti.n_tiles = u1 - u0;
   ti.L = L;
   return ti;
 }
@@ -90,6 +99,29 @@ __device__ __forceinline__ TileInfo tile_info(const TcArgs& a, int b, int split)
 __device__ __forceinline__ int tile_valid(const TcArgs& a, const TileInfo& ti, int t) {
   if (t < ti.n_pt) return min(KT, ti.L - (ti.t_begin + t) * KT);
   return a.R;
+}
+
+// Bits 0..n-1 set (n clamped to [0, 32]).
+__device__ __forceinline__ uint32_t low_bits(int n) {
+  return n >= 32 ? 0xffffffffu : (n <= 0 ? 0u : (1u << n) - 1u);
+}
+
+// Scores of keys whose bit is clear become -inf.
+__device__ __forceinline__ void mask_keys(uint32_t (&r)[32], uint32_t bits) {
+#pragma unroll
+  for (int j = 0; j < 32; ++j) r[j] = ((bits >> j) & 1u) ? r[j] : 0xff800000u;
+}
+
+// Maximum of 32 floats as a balanced tree (short dependency chains).
+__device__ __forceinline__ float max32(const uint32_t (&r)[32]) {
+  float m[16];
+#pragma unroll
+  for (int j = 0; j < 16; ++j) m[j] = fmaxf(__uint_as_float(r[j]), __uint_as_float(r[j + 16]));
+#pragma unroll
+  for (int w = 8; w >= 1; w >>= 1)
+#pragma unroll
+    for (int j = 0; j < w; ++j) m[j] = fmaxf(m[j], m[j + w]);
+  return m[0];
 }
 
 template <bool PRECISE>
@@ -103,14 +135,17 @@ __device__ __forceinline__ void issue_qk(uint32_t tb, const uint8_t* sQ, const u
   }
 }
 
+// O_i += P_i V over the 8 K-steps of 16 keys; the P of keys 64 h + 16 k .. sits in
+// S_i's columns 64 h + 8 k .. (the precise low parts 32 columns further on).
 template <bool PRECISE>
 __device__ __forceinline__ void issue_pv(uint32_t tb, const uint8_t* sV, int i, bool first) {
   constexpr uint32_t idesc = idesc_bf16_f32(128, 128, 0, 1);
 #pragma unroll
   for (int ks = 0; ks < 8; ++ks) {
     const uint64_t bd = smem_desc_sw128(smem_u32(sV) + ks * 2048, HALF, 1024);
-    mma_ts(tb + col_o(i), tb + col_s(i) + ks * 8, bd, idesc, (first && ks == 0) ? 0u : 1u);
-    if constexpr (PRECISE) mma_ts(tb + col_o(i), tb + col_s(i) + 64 + ks * 8, bd, idesc, 1u);
+    const uint32_t acol = col_s(i) + (ks >> 2) * 64 + (ks & 3) * 8;
+    mma_ts(tb + col_o(i), tb + acol, bd, idesc, (first && ks == 0) ? 0u : 1u);
+    if constexpr (PRECISE) mma_ts(tb + col_o(i), tb + acol + 32, bd, idesc, 1u);
   }
 }
 
@@ -122,6 +157,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   __shared__ uint64_t bar_q, k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[2], p_full[2], o_full;
   __shared__ uint32_t tmem_base;
   __shared__ int s_abort;
+  __shared__ float s_red[2][2][2][128];  // [tile parity][M-tile][key half][row] half-row maxima
+  __shared__ float s_l[2][2][128];        // [M-tile][key half][row] half-row sums
 
   const int split = blockIdx.x, bh = blockIdx.y, rb = blockIdx.z;
   const int b = bh / a.Hkv, h = bh % a.Hkv;
@@ -137,7 +174,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       mbar_init(&v_full[s], 1);
       mbar_init(&v_empty[s], 1);
       mbar_init(&s_full[s], 1);
-      mbar_init(&p_full[s], 128);
+      mbar_init(&p_full[s], 256);
     }
     mbar_init(&o_full, 1);
     s_abort = 0;
@@ -249,163 +286,240 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
     }
     if (lane == 0 && ti.n_tiles > 0) mma_commit(&o_full);
-  } else if (warp < 4 * n_mt) {
-    // ------------------------------------------------------------ softmax warpgroup i
-    const int i = warp >> 2;                 // M-tile
-    const int qd = warp & 3;                 // TMEM lane quarter
-    const int r_local = qd * 32 + lane;      // row within the M-tile = TMEM lane
-    const int row = rb * a.rows_per_cta + i * 128 + r_local;
-    const bool vrow = row < a.R * a.G;
-    const int node = vrow ? row / a.G : 0;
-    const int hq = h * a.G + (vrow ? row % a.G : 0);
-    uint64_t mw0 = 0, mw1 = 0;
-    if (vrow) {
-      mw0 = a.anc_mask[(static_cast<size_t>(b) * a.R + node) * a.W];
-      if (a.W > 1) mw1 = a.anc_mask[(static_cast<size_t>(b) * a.R + node) * a.W + 1];
-    }
+  } else {
+    // ------------------------------------------------------------ softmax, warps 0-7
+    // All eight warps work on one M-tile at a time: warp w reads TMEM lane quarter
+    // w & 3 (32 rows) and key half w >> 2 (keys / S columns [64 hf, 64 hf + 64)).  The
+    // two halves of a row agree on its max through shared memory; each half writes
+    // its P into its own S columns, so S stays in registers between the passes.
+    const int qd = warp & 3;
+    const int hf = warp >> 2;
+    const int r_local = qd * 32 + lane;      // row within an M-tile = TMEM lane
     const uint32_t lb = tb + (static_cast<uint32_t>(qd * 32) << 16);
     const float sl2 = a.scale_log2;
-    float m_ref = -INFINITY, l = 0.f;
+    bool vrow[2];
+    int node[2], hq[2];
+    uint32_t tw[2][2];                       // this half's ancestor words (keys >= R cleared)
+    float m_ref[2], l[2];
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const int row = rb * a.rows_per_cta + i * 128 + r_local;
+      vrow[i] = i < n_mt && row < a.R * a.G;
+      node[i] = vrow[i] ? row / a.G : 0;
+      hq[i] = h * a.G + (vrow[i] ? row % a.G : 0);
+      tw[i][0] = tw[i][1] = 0u;
+      if (vrow[i]) {
+        const uint64_t* mrow = a.anc_mask + (static_cast<size_t>(b) * a.R + node[i]) * a.W;
+        const uint64_t mw = (hf == 0) ? mrow[0] : (a.W > 1 ? mrow[1] : 0ull);
+        tw[i][0] = static_cast<uint32_t>(mw) & low_bits(a.R - 64 * hf);
+        tw[i][1] = static_cast<uint32_t>(mw >> 32) & low_bits(a.R - 64 * hf - 32);
+      }
+      m_ref[i] = -INFINITY;
+      l[i] = 0.f;
+    }
     bool ok = true;
     for (int t = 0; t < ti.n_tiles && ok; ++t) {
-      ok = __all_sync(0xffffffffu, wait_parity(&s_full[i], t & 1, a.err, ERR_S));
-      if (!ok) break;
-      tc_fence_after();
       const bool tree = t >= ti.n_pt;
       const int nv = tile_valid(a, ti, t);
-      // key k of this tile counts for this row
-      auto keep = [&](int k) {
-        return vrow && (tree ? (k < a.R && (((k < 64 ? mw0 >> k : mw1 >> (k - 64)) & 1ull) != 0)) : k < nv);
-      };
-      // pass 1: row max over the valid keys, 32 columns at a time
-      float mx = -INFINITY;
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t r[32];
-        tmem_ld32(lb + col_s(i) + 32 * c, r);
-        tmem_ld_wait();
-#pragma unroll
-        for (int j = 0; j < 32; ++j)
-          if (keep(32 * c + j)) mx = fmaxf(mx, __uint_as_float(r[j]));
-      }
-      const float m_new = fmaxf(m_ref, mx);
-      // lazy rescale: move this row's reference max only when it grew by > 2^8; O
-      // holds earlier tiles only when m_ref is already finite.  tcgen05.ld/st are
-      // warp-collective, so the whole warp touches O when any of its rows must.
-      const bool move = m_new != -INFINITY && (m_ref == -INFINITY || (m_new - m_ref) * sl2 > kRescaleLog2);
-      const bool scale_o = move && m_ref != -INFINITY;
-      const float alpha = scale_o ? exp2f((m_ref - m_new) * sl2) : 1.f;
-      if (__any_sync(0xffffffffu, scale_o)) {
-        l *= alpha;
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t o[32];
-          tmem_ld32(lb + col_o(i) + 32 * c, o);
+      for (int i = 0; i < 2; ++i) {
+        if (i >= n_mt) break;
+        const bool got = __all_sync(0xffffffffu, wait_parity(&s_full[i], t & 1, a.err, ERR_S));
+        tc_fence_after();
+        // pass 1: max of this half's 64 scores over the kept keys
+        const uint32_t k0 = !vrow[i] ? 0u : (tree ? tw[i][0] : low_bits(nv - 64 * hf));
+        const uint32_t k1 = !vrow[i] ? 0u : (tree ? tw[i][1] : low_bits(nv - 64 * hf - 32));
+        const bool full = __all_sync(0xffffffffu, (k0 & k1) == 0xffffffffu);
+        float mx = -INFINITY;
+        if (got) {
+          uint32_t s0[32], s1[32];
+          tmem_ld32(lb + col_s(i) + 64 * hf, s0);
+          tmem_ld32(lb + col_s(i) + 64 * hf + 32, s1);
           tmem_ld_wait();
-#pragma unroll
-          for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha);
-          tmem_st32(lb + col_o(i) + 32 * c, o);
-        }
-        tmem_st_wait();
-      }
-      if (move) m_ref = m_new;
-      const float mu = (m_ref == -INFINITY) ? 0.f : m_ref * sl2;
-      // pass 2: P = 2^(s c - m c) as bf16 pairs into S_i's first 64 columns.  Chunk c
-      // (columns 32c..32c+31) is read before its P lands in columns 16c..16c+15, so no
-      // unread S is overwritten.  The precise path also writes the low parts into
-      // columns 64..127, so it holds chunks 2 and 3 in registers first.
-      uint32_t keep23[PRECISE ? 64 : 1];
-      if constexpr (PRECISE) {
-        tmem_ld32(lb + col_s(i) + 64, *reinterpret_cast<uint32_t(*)[32]>(&keep23[0]));
-        tmem_ld32(lb + col_s(i) + 96, *reinterpret_cast<uint32_t(*)[32]>(&keep23[32]));
-        tmem_ld_wait();
-      }
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t r[32];
-        if (PRECISE && c >= 2) {
-#pragma unroll
-          for (int j = 0; j < 32; ++j) r[j] = keep23[(c - 2) * 32 + j];
-        } else {
-          tmem_ld32(lb + col_s(i) + 32 * c, r);
-          tmem_ld_wait();
-        }
-        uint32_t hi[16], lo[16];
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const int k0 = 32 * c + 2 * j;
-          const float p0 = keep(k0) ? exp2f(fmaf(__uint_as_float(r[2 * j]), sl2, -mu)) : 0.f;
-          const float p1 = keep(k0 + 1) ? exp2f(fmaf(__uint_as_float(r[2 * j + 1]), sl2, -mu)) : 0.f;
-          __nv_bfloat162 u = __floats2bfloat162_rn(p0, p1);
-          hi[j] = *reinterpret_cast<uint32_t*>(&u);
-          const float h0 = __uint_as_float(hi[j] << 16), h1 = __uint_as_float(hi[j] & 0xffff0000u);
-          if constexpr (PRECISE) {
-            __nv_bfloat162 w = __floats2bfloat162_rn(p0 - h0, p1 - h1);
-            lo[j] = *reinterpret_cast<uint32_t*>(&w);
-            l += (h0 + __uint_as_float(lo[j] << 16)) + (h1 + __uint_as_float(lo[j] & 0xffff0000u));
-          } else {
-            l += h0 + h1;
+          if (!full) {
+            mask_keys(s0, k0);
+            mask_keys(s1, k1);
           }
+          mx = fmaxf(max32(s0), max32(s1));
         }
-        tmem_st16(lb + col_s(i) + 16 * c, hi);
-        if constexpr (PRECISE) tmem_st16(lb + col_s(i) + 64 + 16 * c, lo);
+        s_red[t & 1][i][hf][r_local] = mx;
+        if (!bar_and(1, 256, got)) {  // every softmax warp leaves together on a timeout
+          ok = false;
+          break;
+        }
+        const float m_new = fmaxf(m_ref[i], fmaxf(mx, s_red[t & 1][i][hf ^ 1][r_local]));
+        // lazy rescale: move the row's reference max only when it grew by > 2^8; O
+        // holds earlier tiles only when m_ref is already finite.  Both halves of a row
+        // decide alike; each rescales its own 64 O columns.  tcgen05.ld/st are
+        // warp-collective, so the whole warp touches O when any of its rows must.
+        const bool move = m_new != -INFINITY && (m_ref[i] == -INFINITY || (m_new - m_ref[i]) * sl2 > kRescaleLog2);
+        const bool scale_o = move && m_ref[i] != -INFINITY;
+        const float alpha = scale_o ? ex2((m_ref[i] - m_new) * sl2) : 1.f;
+        if (__any_sync(0xffffffffu, scale_o)) {
+          l[i] *= alpha;
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {
+            uint32_t o[32];
+            tmem_ld32(lb + col_o(i) + 64 * hf + 32 * c, o);
+            tmem_ld_wait();
+#pragma unroll
+            for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha);
+            tmem_st32(lb + col_o(i) + 64 * hf + 32 * c, o);
+          }
+          tmem_st_wait();
+        }
+        if (move) m_ref[i] = m_new;
+        const float mu = (m_ref[i] == -INFINITY) ? 0.f : m_ref[i] * sl2;
+        // pass 2: S again from TMEM, P = 2^(s c - m c) as bf16 pairs (masked keys hold
+        // -inf and give exactly 0): keys 64 hf + 32 c .. + 31 go to columns
+        // 64 hf + 16 c .. + 15; the precise path puts the low parts 32 columns further
+        // on.  Both chunks are read before either is written.
+        float ls[4] = {0.f, 0.f, 0.f, 0.f};
+        auto emit = [&](const uint32_t (&r)[32], int c) {
+          uint32_t hi[16], lo[PRECISE ? 16 : 1];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const float p0 = ex2(fmaf(__uint_as_float(r[2 * j]), sl2, -mu));
+            const float p1 = ex2(fmaf(__uint_as_float(r[2 * j + 1]), sl2, -mu));
+            __nv_bfloat162 u = __floats2bfloat162_rn(p0, p1);
+            hi[j] = *reinterpret_cast<uint32_t*>(&u);
+            const float h0 = __uint_as_float(hi[j] << 16), h1 = __uint_as_float(hi[j] & 0xffff0000u);
+            if constexpr (PRECISE) {
+              __nv_bfloat162 w = __floats2bfloat162_rn(p0 - h0, p1 - h1);
+              lo[j] = *reinterpret_cast<uint32_t*>(&w);
+              ls[j & 3] += (h0 + __uint_as_float(lo[j] << 16)) + (h1 + __uint_as_float(lo[j] & 0xffff0000u));
+            } else {
+              ls[j & 3] += h0 + h1;
+            }
+          }
+          tmem_st16(lb + col_s(i) + 64 * hf + 16 * c, hi);
+          if constexpr (PRECISE) tmem_st16(lb + col_s(i) + 64 * hf + 32 + 16 * c, lo);
+        };
+        {
+          uint32_t s0[32], s1[32];
+          tmem_ld32(lb + col_s(i) + 64 * hf, s0);
+          tmem_ld32(lb + col_s(i) + 64 * hf + 32, s1);
+          tmem_ld_wait();
+          if (!full) {
+            mask_keys(s0, k0);
+            mask_keys(s1, k1);
+          }
+          emit(s0, 0);
+          emit(s1, 1);
+        }
+        l[i] += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(&p_full[i]);
       }
-      tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive(&p_full[i]);
     }
     // ---- epilogue: O from TMEM to the output (one split) or the partials
     const bool have = ok && ti.n_tiles > 0;
-    bool done = have ? __all_sync(0xffffffffu, wait_parity(&o_full, 0, a.err, ERR_O)) : false;
+    const bool done = have ? __all_sync(0xffffffffu, wait_parity(&o_full, 0, a.err, ERR_O)) : false;
     tc_fence_after();
-    const size_t prow = (static_cast<size_t>(bh) * a.splits + split) * a.rows_pad + row;
-    const float inv = (a.splits == 1 && l > 0.f) ? 1.f / l : 1.f;
 #pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      uint32_t o[32];
-      if (done) {
-        tmem_ld32(lb + col_o(i) + 32 * c, o);
-        tmem_ld_wait();
-      } else {
+    for (int i = 0; i < 2; ++i) s_l[i][hf][r_local] = l[i];
+    const bool all_done = bar_and(2, 256, done);
+    float l_tot[2];
 #pragma unroll
-        for (int j = 0; j < 32; ++j) o[j] = 0u;
-      }
-      if (!vrow) continue;
-      if (a.splits == 1) {
-        const size_t orow = (static_cast<size_t>(b * a.R + node) * a.Hq + hq) * 128 + 32 * c;
-        if (a.out_f32) {
-          float4* dst = reinterpret_cast<float4*>(static_cast<float*>(a.out) + orow);
+    for (int i = 0; i < 2; ++i) l_tot[i] = l[i] + s_l[i][hf ^ 1][r_local];
+    if (a.splits > 1 && all_done) {
+      // partial O of each M-tile (128 rows x 512 B, contiguous in the workspace) is
+      // staged in the free K/V stages as four 128-byte-swizzled column slices, then
+      // stored with one TMA store per slice.  Row r's 16-byte chunk j sits at chunk
+      // j ^ (r & 7), so each quarter-warp store covers all 32 banks.
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        if (i >= n_mt) break;
+        uint8_t* so = smem + SM_K + i * 4 * HALF;
+#pragma unroll
+        for (int cc = 0; cc < 2; ++cc) {
+          const int c = 2 * hf + cc;
+          uint32_t o[32];
+          tmem_ld32(lb + col_o(i) + 32 * c, o);
+          tmem_ld_wait();
+          uint8_t* dst = so + c * HALF + r_local * 128;
 #pragma unroll
           for (int j = 0; j < 8; ++j)
-            dst[j] = make_float4(__uint_as_float(o[4 * j]) * inv, __uint_as_float(o[4 * j + 1]) * inv,
-                                 __uint_as_float(o[4 * j + 2]) * inv, __uint_as_float(o[4 * j + 3]) * inv);
-        } else {
-          uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.out) + orow);
+            *reinterpret_cast<uint4*>(dst + ((j ^ (r_local & 7)) << 4)) =
+                make_uint4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
+        }
+      }
+      fence_proxy_async_smem();
+      bar_sync(2, 256);
+      if (threadIdx.x == 0) {
+        for (int i = 0; i < n_mt; ++i) {
+          const int y = (bh * a.splits + split) * a.rows_pad + rb * a.rows_per_cta + i * 128;
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            uint32_t w[4];
+          for (int c = 0; c < 4; ++c) tma_store_2d(&tm.po, smem + SM_K + i * 4 * HALF + c * HALF, 32 * c, y);
+        }
+        bulk_commit();
+        bulk_wait_read0();
+      }
+      if (hf == 0) {
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              __nv_bfloat162 u = __floats2bfloat162_rn(__uint_as_float(o[8 * j + 2 * e]) * inv,
-                                                       __uint_as_float(o[8 * j + 2 * e + 1]) * inv);
-              w[e] = *reinterpret_cast<uint32_t*>(&u);
+        for (int i = 0; i < 2; ++i) {
+          if (!vrow[i]) continue;
+          const size_t prow = (static_cast<size_t>(bh) * a.splits + split) * a.rows_pad + rb * a.rows_per_cta + i * 128 + r_local;
+          *reinterpret_cast<float2*>(a.part_ml + prow * 2) = make_float2(m_ref[i], l_tot[i]);
+        }
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        if (i >= n_mt) break;
+        const float inv = (a.splits == 1 && l_tot[i] > 0.f) ? 1.f / l_tot[i] : 1.f;
+        const size_t prow = (static_cast<size_t>(bh) * a.splits + split) * a.rows_pad + rb * a.rows_per_cta + i * 128 + r_local;
+#pragma unroll
+        for (int cc = 0; cc < 2; ++cc) {
+          const int c = 2 * hf + cc;
+          uint32_t o[32];
+          if (all_done) {
+            tmem_ld32(lb + col_o(i) + 32 * c, o);
+            tmem_ld_wait();
+          } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) o[j] = 0u;
+          }
+          if (!vrow[i]) continue;
+          if (a.splits == 1) {
+            const size_t orow = (static_cast<size_t>(b * a.R + node[i]) * a.Hq + hq[i]) * 128 + 32 * c;
+            if (a.out_f32) {
+              float4* dst = reinterpret_cast<float4*>(static_cast<float*>(a.out) + orow);
+#pragma unroll
+              for (int j = 0; j < 8; ++j)
+                dst[j] = make_float4(__uint_as_float(o[4 * j]) * inv, __uint_as_float(o[4 * j + 1]) * inv,
+                                     __uint_as_float(o[4 * j + 2]) * inv, __uint_as_float(o[4 * j + 3]) * inv);
+            } else {
+              uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.out) + orow);
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                uint32_t w[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                  __nv_bfloat162 u = __floats2bfloat162_rn(__uint_as_float(o[8 * j + 2 * e]) * inv,
+                                                           __uint_as_float(o[8 * j + 2 * e + 1]) * inv);
+                  w[e] = *reinterpret_cast<uint32_t*>(&u);
+                }
+                dst[j] = make_uint4(w[0], w[1], w[2], w[3]);
+              }
             }
-            dst[j] = make_uint4(w[0], w[1], w[2], w[3]);
+          } else {
+            float4* dst = reinterpret_cast<float4*>(a.part_o + prow * 128 + 32 * c);
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+              dst[j] = make_float4(__uint_as_float(o[4 * j]), __uint_as_float(o[4 * j + 1]),
+                                   __uint_as_float(o[4 * j + 2]), __uint_as_float(o[4 * j + 3]));
           }
         }
-      } else {
-        float4* dst = reinterpret_cast<float4*>(a.part_o + prow * 128 + 32 * c);
-#pragma unroll
-        for (int j = 0; j < 8; ++j)
-          dst[j] = make_float4(__uint_as_float(o[4 * j]), __uint_as_float(o[4 * j + 1]), __uint_as_float(o[4 * j + 2]),
-                               __uint_as_float(o[4 * j + 3]));
-      }
-    }
-    if (vrow) {
-      if (a.splits == 1) {
-        if (a.lse) a.lse[static_cast<size_t>(b * a.R + node) * a.Hq + hq] = a.scale * m_ref + logf(l);
-      } else {
-        *reinterpret_cast<float2*>(a.part_ml + prow * 2) = make_float2(done ? m_ref : -INFINITY, done ? l : 0.f);
+        if (vrow[i] && hf == 0) {
+          if (a.splits == 1) {
+            if (a.lse) a.lse[static_cast<size_t>(b * a.R + node[i]) * a.Hq + hq[i]] = a.scale * m_ref[i] + logf(l_tot[i]);
+          } else {
+            *reinterpret_cast<float2*>(a.part_ml + prow * 2) =
+                make_float2(all_done ? m_ref[i] : -INFINITY, all_done ? l_tot[i] : 0.f);
+          }
+        }
       }
     }
   }
@@ -429,15 +543,15 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// bf16 tensor map of `rank` dims (innermost first), 128-byte swizzle, zero fill.
-bool make_tmap(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims, const cuuint64_t* strides,
-               const cuuint32_t* box) {
+// Tensor map of `rank` dims (innermost first), 128-byte swizzle, zero fill.
+bool make_tmap(CUtensorMap* m, CUtensorMapDataType dt, const void* base, int rank, const cuuint64_t* dims,
+               const cuuint64_t* strides, const cuuint32_t* box) {
   auto fn = encode_fn();
   if (!fn) return false;
   cuuint32_t es[3] = {1, 1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), dims, strides, box, es,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  return fn(m, dt, rank, const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+         CUDA_SUCCESS;
 }
 
 template <bool PRECISE>
@@ -467,23 +581,31 @@ cudaError_t launch_tree_attn_tc(const AttnPlan& p, const void* q, const void* k_
     const cuuint64_t dims[3] = {D, static_cast<cuuint64_t>(p.Hq), static_cast<cuuint64_t>(p.B) * p.R};
     const cuuint64_t strides[2] = {D * 2, static_cast<cuuint64_t>(p.Hq) * D * 2};
     const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(p.G), static_cast<cuuint32_t>(128 / p.G)};
-    if (!make_tmap(&tm.q, q, 3, dims, strides, box)) return cudaErrorInvalidValue;
+    if (!make_tmap(&tm.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, q, 3, dims, strides, box)) return cudaErrorInvalidValue;
   }
   {
     const cuuint64_t dims[2] = {D, static_cast<cuuint64_t>(p.B) * p.Hkv * p.P};
     const cuuint64_t strides[1] = {D * 2};
     const cuuint32_t box[2] = {64, 128};
-    if (!make_tmap(&tm.kc, k_cache, 2, dims, strides, box)) return cudaErrorInvalidValue;
-    if (!make_tmap(&tm.vc, v_cache, 2, dims, strides, box)) return cudaErrorInvalidValue;
+    if (!make_tmap(&tm.kc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, k_cache, 2, dims, strides, box)) return cudaErrorInvalidValue;
+    if (!make_tmap(&tm.vc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, v_cache, 2, dims, strides, box)) return cudaErrorInvalidValue;
   }
   {
     const cuuint64_t dims[2] = {D, static_cast<cuuint64_t>(p.B) * p.Hkv * p.R};
     const cuuint64_t strides[1] = {D * 2};
     const cuuint32_t box[2] = {64, 128};
-    if (!make_tmap(&tm.tk, tree_k, 2, dims, strides, box)) return cudaErrorInvalidValue;
-    if (!make_tmap(&tm.tv, tree_v, 2, dims, strides, box)) return cudaErrorInvalidValue;
+    if (!make_tmap(&tm.tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, tree_k, 2, dims, strides, box)) return cudaErrorInvalidValue;
+    if (!make_tmap(&tm.tv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, tree_v, 2, dims, strides, box)) return cudaErrorInvalidValue;
   }
   uint8_t* w = static_cast<uint8_t*>(ws);
+  memset(&tm.po, 0, sizeof(tm.po));
+  if (p.splits > 1) {
+    const cuuint64_t dims[2] = {D, static_cast<cuuint64_t>(p.B) * p.Hkv * p.splits * p.rows_pad};
+    const cuuint64_t strides[1] = {D * 4};
+    const cuuint32_t box[2] = {32, 128};
+    if (!make_tmap(&tm.po, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, w + p.off_o, 2, dims, strides, box))
+      return cudaErrorInvalidValue;
+  }
   TcArgs a;
   a.seq_len = seq_len;
   a.anc_mask = anc_mask;
