@@ -44,7 +44,9 @@ struct AttnPlan {
   int row_blocks;
   int splits;
   int rows_pad;      // row_blocks * rows_per_cta
-  size_t off_err, off_o, off_ml, total;
+  bool coop;         // tcgen05, splits > 1, grid fits on the SMs at once: the splits of a
+                     // (request, KV head, row block) merge their partials in the kernel
+  size_t off_err, off_cnt, off_o, off_ml, total;
 };
 void plan_tree_attn(const eagle_attn_desc* d, int num_sms, AttnPlan* p);
 // Merge split partials into out / lse (shared by the mma.sync and tcgen05 kernels).

@@ -141,6 +141,20 @@ __device__ __forceinline__ void bar_sync(int id, int count) {
   asm volatile("barrier.cta.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
+// ------------------------------------------------------------------ global memory ordering
+// Orders this thread's completed bulk (async proxy) writes to global memory before
+// its later generic-proxy operations.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+// Completion of every committed bulk store, writes included.
+__device__ __forceinline__ void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+__device__ __forceinline__ int ld_acquire_gpu(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
 // ------------------------------------------------------------------ special functions
 // 2^x on the multi-function unit (PTX ex2.approx, subnormal results flushed to 0;
 // 2^-inf = 0).

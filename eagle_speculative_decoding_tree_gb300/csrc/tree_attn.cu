@@ -15,6 +15,8 @@
 // tree_attn_combine merges with the log-sum-exp rule.
 //
 // fp32 path: a plain SIMT kernel, one warp per (request, node, query head).
+#include <algorithm>
+
 #include "common.cuh"
 #include "launch.h"
 
@@ -344,67 +346,80 @@ __global__ void __launch_bounds__(NW * 32, (NW == 4) ? 2 : 1) tree_attn_mma_kern
 }
 
 // Merge split partials: M = max m_s, L = sum l_s 2^((m_s - M) c), O = sum O_s 2^((m_s - M) c) / L.
-// One warp per row: lane s holds split s's (m, l) (splits <= 64, two per lane), the
-// weights travel by shuffle, and the partial rows are loaded eight splits at a time
-// so that the loads overlap.
+// One warp per row: lane s holds split s's (m, l) (splits <= 64, two per lane) and
+// the weights travel by shuffle.  The partial rows of up to 32 splits are requested
+// before any of them is used, so a row costs about one memory latency.
 template <int D>
 __global__ void __launch_bounds__(128) tree_attn_combine_kernel(const AttnArgs a) {
+  constexpr int PER = D / 32;
+  constexpr int BATCH = 32;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int r = blockIdx.x * 4 + warp;
   const int bh = blockIdx.y;
   if (r >= a.R * a.G) return;
   const int b = bh / a.Hkv, h = bh % a.Hkv;
   const int nd = r / a.G, hq = h * a.G + r % a.G;
-  constexpr int PER = D / 32;
   const size_t base = static_cast<size_t>(bh) * a.splits * a.rows_pad + r;
-  float m2[2], l2[2];
+  const size_t sstride = static_cast<size_t>(a.rows_pad) * D;
+  const float* po0 = a.part_o + base * D + lane * PER;
+  float2 ml[2];
 #pragma unroll
   for (int k = 0; k < 2; ++k) {
     const int s = lane + 32 * k;
-    float2 ml = make_float2(-INFINITY, 0.f);
-    if (s < a.splits) ml = *reinterpret_cast<const float2*>(a.part_ml + (base + static_cast<size_t>(s) * a.rows_pad) * 2);
-    m2[k] = ml.x;
-    l2[k] = ml.y;
+    ml[k] = s < a.splits ? *reinterpret_cast<const float2*>(a.part_ml + (base + static_cast<size_t>(s) * a.rows_pad) * 2)
+                         : make_float2(-INFINITY, 0.f);
   }
-  const float M = warp_max(fmaxf(m2[0], m2[1]));
+  float v[BATCH][PER];
+#pragma unroll
+  for (int u = 0; u < BATCH; ++u) {
+    if (u < a.splits) {
+      const float* po = po0 + static_cast<size_t>(u) * sstride;
+      if constexpr (PER == 4) {
+        const float4 t = *reinterpret_cast<const float4*>(po);
+        v[u][0] = t.x;
+        v[u][1] = t.y;
+        v[u][2] = t.z;
+        v[u][3] = t.w;
+      } else {
+        const float2 t = *reinterpret_cast<const float2*>(po);
+        v[u][0] = t.x;
+        v[u][1] = t.y;
+      }
+    } else {
+#pragma unroll
+      for (int e = 0; e < PER; ++e) v[u][e] = 0.f;
+    }
+  }
+  const float M = warp_max(fmaxf(ml[0].x, ml[1].x));
   float w2[2];
 #pragma unroll
-  for (int k = 0; k < 2; ++k) w2[k] = (m2[k] == -INFINITY) ? 0.f : exp2f((m2[k] - M) * a.scale_log2);
-  const float Ls = warp_sum(l2[0] * w2[0] + l2[1] * w2[1]);
+  for (int k = 0; k < 2; ++k) w2[k] = (ml[k].x == -INFINITY) ? 0.f : exp2f((ml[k].x - M) * a.scale_log2);
+  const float Ls = warp_sum(ml[0].y * w2[0] + ml[1].y * w2[1]);
   float acc[PER];
 #pragma unroll
   for (int e = 0; e < PER; ++e) acc[e] = 0.f;
-  const float* po0 = a.part_o + base * D + lane * PER;
-  const size_t sstride = static_cast<size_t>(a.rows_pad) * D;
-  for (int s0 = 0; s0 < a.splits; s0 += 8) {
-    float v[8][PER], wv[8];
+#pragma unroll
+  for (int u = 0; u < BATCH; ++u) {
+    const float w = __shfl_sync(0xffffffffu, w2[0], u);
+#pragma unroll
+    for (int e = 0; e < PER; ++e) acc[e] = fmaf(w, v[u][e], acc[e]);
+  }
+  for (int s0 = BATCH; s0 < a.splits; s0 += 8) {  // splits beyond 32: eight at a time
+    float x[8][PER], wv[8];
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
       const int s = s0 + u;
-      wv[u] = __shfl_sync(0xffffffffu, s < 32 ? w2[0] : w2[1], s & 31);
-      if (s < a.splits) {
-        const float* po = po0 + static_cast<size_t>(s) * sstride;
-        if constexpr (PER == 4) {
-          const float4 t = *reinterpret_cast<const float4*>(po);
-          v[u][0] = t.x;
-          v[u][1] = t.y;
-          v[u][2] = t.z;
-          v[u][3] = t.w;
-        } else {
-          const float2 t = *reinterpret_cast<const float2*>(po);
-          v[u][0] = t.x;
-          v[u][1] = t.y;
-        }
-      } else {
-        wv[u] = 0.f;
+      wv[u] = __shfl_sync(0xffffffffu, w2[1], s & 31);
+      const bool in = s < a.splits;
+      const float* po = po0 + static_cast<size_t>(in ? s : 0) * sstride;
 #pragma unroll
-        for (int e = 0; e < PER; ++e) v[u][e] = 0.f;
-      }
+      for (int e = 0; e < PER; ++e) x[u][e] = in ? po[e] : 0.f;
+      if (!in) wv[u] = 0.f;
     }
 #pragma unroll
     for (int u = 0; u < 8; ++u)
 #pragma unroll
-      for (int e = 0; e < PER; ++e) acc[e] = fmaf(wv[u], v[u][e], acc[e]);
+      for (int e = 0; e < PER; ++e) acc[e] = fmaf(wv[u], x[u][e], acc[e]);
   }
   const float inv = 1.f / Ls;
   const size_t orow = (static_cast<size_t>(b * a.R + nd) * a.Hq + hq) * D + lane * PER;
@@ -504,8 +519,9 @@ void plan_tree_attn(const eagle_attn_desc* d, int num_sms, AttnPlan* p) {
   p->scale = d->scale;
   p->out_dtype = d->out_dtype;
   p->precise = d->precision == EAGLE_ATTN_PRECISE;
-  p->off_err = p->off_o = p->off_ml = p->total = 0;
+  p->off_err = p->off_cnt = p->off_o = p->off_ml = p->total = 0;
   p->tc = false;
+  p->coop = false;
   const int RG = p->R * p->G;
   if (p->dtype == EAGLE_F32) {
     p->rows_per_cta = 4;
@@ -530,16 +546,22 @@ void plan_tree_attn(const eagle_attn_desc* d, int num_sms, AttnPlan* p) {
   p->row_blocks = (RG + p->rows_per_cta - 1) / p->rows_per_cta;
   p->rows_pad = p->row_blocks * p->rows_per_cta;
   const int max_tiles = (p->P + key_tile - 1) / key_tile;
+  const int base = std::max(1, p->B * p->Hkv * p->row_blocks);
   int splits = d->num_splits;
-  if (splits <= 0) {
-    const int base = p->B * p->Hkv * p->row_blocks;
-    splits = num_sms * slots_per_sm / (base > 0 ? base : 1);
-  }
+  if (splits <= 0) splits = num_sms * slots_per_sm / base;
   if (splits > max_tiles) splits = max_tiles;
   if (splits > 64) splits = 64;
   if (splits < 1) splits = 1;
   p->splits = splits;
+  // tcgen05 with splits: when the whole grid fits on the SMs at once (one CTA per SM)
+  // the kernel merges the partials itself (cooperative launch); else the combine
+  // kernel does.
+  p->coop = p->tc && splits > 1 && static_cast<long long>(base) * splits <= num_sms;
   size_t off = p->tc ? 256 : 0;  // tcgen05: error word first
+  if (p->coop) {
+    p->off_cnt = off;
+    off += (static_cast<size_t>(base) * 4 + 255) / 256 * 256;
+  }
   if (splits > 1) {
     const size_t rows = static_cast<size_t>(p->B) * p->Hkv * splits * p->rows_pad;
     p->off_o = off;

@@ -50,8 +50,10 @@ constexpr int SMEM_BYTES = 6 * TILE + 1024;
 __device__ __forceinline__ uint32_t col_s(int i) { return static_cast<uint32_t>(i) * 128u; }          // S_i / P_i
 __device__ __forceinline__ uint32_t col_o(int i) { return 256u + static_cast<uint32_t>(i) * 128u; }  // O_i
 constexpr float kRescaleLog2 = 8.f;       // lazy rescale threshold (log2 units)
+constexpr int kMergeBatch = 20;           // group merge: splits whose rows are loaded at once
 
-enum : int { ERR_Q = 1, ERR_KFULL = 2, ERR_KEMPTY = 4, ERR_VFULL = 8, ERR_VEMPTY = 16, ERR_S = 32, ERR_P = 64, ERR_O = 128 };
+enum : int { ERR_Q = 1, ERR_KFULL = 2, ERR_KEMPTY = 4, ERR_VFULL = 8, ERR_VEMPTY = 16, ERR_S = 32, ERR_P = 64, ERR_O = 128,
+             ERR_GROUP = 256 };
 
 struct TcArgs {
   const int32_t* seq_len;
@@ -62,6 +64,8 @@ struct TcArgs {
   float* part_ml;  // [B*Hkv][splits][rows_pad][2]
   int* err;
   int B, R, Hq, Hkv, G, P, W, splits, rows_pad, rows_per_cta, n_mt, out_f32;
+  int coop;        // 1: the splits of a group merge their partials in this kernel
+  int* cnt;        // coop: per (request, KV head, row block) count of published splits
   float scale, scale_log2;
 };
 
@@ -99,6 +103,24 @@ __device__ __forceinline__ TileInfo tile_info(const TcArgs& a, int b, int split)
 __device__ __forceinline__ int tile_valid(const TcArgs& a, const TileInfo& ti, int t) {
   if (t < ti.n_pt) return min(KT, ti.L - (ti.t_begin + t) * KT);
   return a.R;
+}
+
+// Counts this split into its group and waits (at most 2 s, then ERR_GROUP) until all
+// `n` splits of the group have counted.  Only valid when the whole grid is resident
+// (cooperative launch).
+__device__ __forceinline__ bool group_arrive_wait(int* cnt, int n, int* err) {
+  __threadfence();
+  atomicAdd(cnt, 1);
+  if (ld_acquire_gpu(cnt) >= n) return true;
+  const uint64_t t0 = global_ns();
+  while (ld_acquire_gpu(cnt) < n) {
+    if (global_ns() - t0 > 2000000000ull) {
+      atomicOr(err, ERR_GROUP);
+      return false;
+    }
+    __nanosleep(100);
+  }
+  return true;
 }
 
 // Bits 0..n-1 set (n clamped to [0, 32]).
@@ -159,6 +181,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   __shared__ int s_abort;
   __shared__ float s_red[2][2][2][128];  // [tile parity][M-tile][key half][row] half-row maxima
   __shared__ float s_l[2][2][128];        // [M-tile][key half][row] half-row sums
+  __shared__ int s_go;                    // group merge: every split published in time
 
   const int split = blockIdx.x, bh = blockIdx.y, rb = blockIdx.z;
   const int b = bh / a.Hkv, h = bh % a.Hkv;
@@ -454,7 +477,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           for (int c = 0; c < 4; ++c) tma_store_2d(&tm.po, smem + SM_K + i * 4 * HALF + c * HALF, 32 * c, y);
         }
         bulk_commit();
-        bulk_wait_read0();
+        if (a.coop)
+          bulk_wait0();  // other CTAs read these rows
+        else
+          bulk_wait_read0();
       }
       if (hf == 0) {
 #pragma unroll
@@ -522,6 +548,77 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
       }
     }
+    if (a.coop) {
+      // the group's merge: publish this split's partials (all writes fenced, then one
+      // release-ordered count), wait until every split of this (request, KV head, row
+      // block) has counted, then merge rows [split n / S, (split + 1) n / S) of the
+      // block from the partials in L2, a warp per row: M = max m_s,
+      // w_s = 2^((m_s - M) c), O = sum w_s O_s / sum w_s l_s
+      fence_proxy_async_global();
+      __threadfence();
+      bar_sync(2, 256);
+      if (threadIdx.x == 0) s_go = group_arrive_wait(a.cnt + bh * gridDim.z + rb, a.splits, a.err) ? 1 : 0;
+      bar_sync(2, 256);
+      if (s_go) {
+        // a warp per row; every load of a row (the splits' (m, l) one per lane, their
+        // partial rows 16 bytes per lane) is issued before any is used, so a row costs
+        // one L2 round trip for up to kMergeBatch splits
+        const int n = min(a.rows_per_cta, a.R * a.G - rb * a.rows_per_cta);
+        const int hi = (split + 1) * n / a.splits;
+        for (int lr = split * n / a.splits + warp; lr < hi; lr += 8) {
+          const int grow = rb * a.rows_per_cta + lr;
+          const size_t base = static_cast<size_t>(bh) * a.splits * a.rows_pad + grow;
+          const size_t sstride = a.rows_pad;
+          float4 v[kMergeBatch];
+#pragma unroll
+          for (int u = 0; u < kMergeBatch; ++u)
+            v[u] = u < a.splits ? __ldcg(reinterpret_cast<const float4*>(a.part_o + (base + u * sstride) * 128) + lane)
+                                : make_float4(0.f, 0.f, 0.f, 0.f);
+          float2 ml[2];
+#pragma unroll
+          for (int k = 0; k < 2; ++k) {
+            const int sp = lane + 32 * k;
+            ml[k] = sp < a.splits ? __ldcg(reinterpret_cast<const float2*>(a.part_ml + (base + sp * sstride) * 2))
+                                  : make_float2(-INFINITY, 0.f);
+          }
+          const float M = warp_max(fmaxf(ml[0].x, ml[1].x));
+          float w2[2];
+#pragma unroll
+          for (int k = 0; k < 2; ++k) w2[k] = (ml[k].x == -INFINITY) ? 0.f : ex2((ml[k].x - M) * sl2);
+          const float L = warp_sum(ml[0].y * w2[0] + ml[1].y * w2[1]);
+          float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+          for (int u = 0; u < kMergeBatch; ++u) {
+            const float ws = __shfl_sync(0xffffffffu, w2[0], u);
+            acc.x = fmaf(ws, v[u].x, acc.x);
+            acc.y = fmaf(ws, v[u].y, acc.y);
+            acc.z = fmaf(ws, v[u].z, acc.z);
+            acc.w = fmaf(ws, v[u].w, acc.w);
+          }
+          for (int sp = kMergeBatch; sp < a.splits; ++sp) {  // more splits than one batch
+            const float ws = __shfl_sync(0xffffffffu, sp < 32 ? w2[0] : w2[1], sp & 31);
+            const float4 x = __ldcg(reinterpret_cast<const float4*>(a.part_o + (base + sp * sstride) * 128) + lane);
+            acc.x = fmaf(ws, x.x, acc.x);
+            acc.y = fmaf(ws, x.y, acc.y);
+            acc.z = fmaf(ws, x.z, acc.z);
+            acc.w = fmaf(ws, x.w, acc.w);
+          }
+          const float inv = 1.f / L;
+          const int node = grow / a.G, hq = h * a.G + grow % a.G;
+          const size_t orow = (static_cast<size_t>(b * a.R + node) * a.Hq + hq) * 128 + 4 * lane;
+          if (a.out_f32) {
+            *reinterpret_cast<float4*>(static_cast<float*>(a.out) + orow) =
+                make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+          } else {
+            __nv_bfloat162 u0 = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
+            __nv_bfloat162 u1 = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
+            *reinterpret_cast<uint2*>(static_cast<uint16_t*>(a.out) + orow) =
+                make_uint2(*reinterpret_cast<uint32_t*>(&u0), *reinterpret_cast<uint32_t*>(&u1));
+          }
+          if (a.lse && lane == 0) a.lse[static_cast<size_t>(b * a.R + node) * a.Hq + hq] = a.scale * M + logf(L);
+        }
+      }
+    }
   }
   tc_fence_before();
   __syncthreads();
@@ -554,19 +651,41 @@ bool make_tmap(CUtensorMap* m, CUtensorMapDataType dt, const void* base, int ran
          CUDA_SUCCESS;
 }
 
+// One-time per-device kernel attribute: the dynamic shared memory.
 template <bool PRECISE>
-cudaError_t launch_tc(const Tmaps& tm, const TcArgs& a, dim3 grid, cudaStream_t s) {
-  auto kern = tree_attn_tc_kernel<PRECISE>;
+cudaError_t configure_tc() {
   static unsigned long long configured = 0;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (dev >= 64 || !(__atomic_load_n(&configured, __ATOMIC_ACQUIRE) & (1ull << dev))) {
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
-    if (e != cudaSuccess) return e;
-    if (dev < 64) __atomic_fetch_or(&configured, 1ull << dev, __ATOMIC_RELEASE);
+  if (dev < 64 && (__atomic_load_n(&configured, __ATOMIC_ACQUIRE) & (1ull << dev))) return cudaSuccess;
+  e = cudaFuncSetAttribute(tree_attn_tc_kernel<PRECISE>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  if (dev < 64) __atomic_fetch_or(&configured, 1ull << dev, __ATOMIC_RELEASE);
+  return cudaSuccess;
+}
+
+// Cooperative launch when the CTAs of a split group wait on one another (a.coop):
+// the driver then guarantees that the whole grid is resident at once, or fails the
+// launch.
+template <bool PRECISE>
+cudaError_t launch_tc(const Tmaps& tm, const TcArgs& a, dim3 grid, cudaStream_t s) {
+  cudaError_t e = configure_tc<PRECISE>();
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(NTHREADS, 1, 1);
+  cfg.dynamicSmemBytes = SMEM_BYTES;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  if (a.coop) {
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
   }
-  kern<<<grid, NTHREADS, SMEM_BYTES, s>>>(tm, a);
+  e = cudaLaunchKernelEx(&cfg, tree_attn_tc_kernel<PRECISE>, tm, a);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
@@ -611,8 +730,9 @@ cudaError_t launch_tree_attn_tc(const AttnPlan& p, const void* q, const void* k_
   a.anc_mask = anc_mask;
   a.out = out;
   a.lse = lse;
-  a.part_o = p.splits > 1 ? reinterpret_cast<float*>(w + p.off_o) : nullptr;
-  a.part_ml = p.splits > 1 ? reinterpret_cast<float*>(w + p.off_ml) : nullptr;
+  const bool partials = p.splits > 1;
+  a.part_o = partials ? reinterpret_cast<float*>(w + p.off_o) : nullptr;
+  a.part_ml = partials ? reinterpret_cast<float*>(w + p.off_ml) : nullptr;
   a.err = reinterpret_cast<int*>(w + p.off_err);
   a.B = p.B;
   a.R = p.R;
@@ -625,14 +745,17 @@ cudaError_t launch_tree_attn_tc(const AttnPlan& p, const void* q, const void* k_
   a.rows_pad = p.rows_pad;
   a.rows_per_cta = p.rows_per_cta;
   a.n_mt = p.rows_per_cta / 128;
+  a.coop = p.coop ? 1 : 0;
+  a.cnt = p.coop ? reinterpret_cast<int*>(w + p.off_cnt) : nullptr;
   a.out_f32 = p.out_dtype == EAGLE_F32;
   a.scale = p.scale;
   a.scale_log2 = p.scale * kLog2e;
-  cudaError_t e = cudaMemsetAsync(a.err, 0, sizeof(int), s);
+  // error word (and the split-group counters of a cooperative launch) start at zero
+  cudaError_t e = cudaMemsetAsync(w, 0, p.coop ? p.off_o : sizeof(int), s);
   if (e != cudaSuccess) return e;
   dim3 grid(p.splits, p.B * p.Hkv, p.row_blocks);
   e = p.precise ? launch_tc<true>(tm, a, grid, s) : launch_tc<false>(tm, a, grid, s);
-  if (e != cudaSuccess || p.splits == 1) return e;
+  if (e != cudaSuccess || !partials || p.coop) return e;
   return launch_tree_attn_combine(p, out, lse, a.part_o, a.part_ml, s);
 }
 

@@ -78,6 +78,7 @@ def _check(w, batch, seq_len, rows, par, mask, heads, q_scale=1.0, num_splits=0,
     ("mha-bf16-ragged", dict(prefix=1000, prefix_min=1000), 1000, 61, 1.0, 0),
     ("gqa-bf16", dict(prefix=777, prefix_min=777), 777, 61, 1.0, 0),
     ("gqa-bf16-forced-splits", dict(prefix=1500, prefix_min=1500), 1500, 61, 1.0, 7),
+    ("gqa-bf16-20-splits", dict(prefix=3000, prefix_min=3000), 3000, 61, 1.0, 20),
     ("gqa-bf16-one-split", dict(prefix=300, prefix_min=300), 300, 61, 1.0, 1),
     ("gqa-bf16-128rows", dict(prefix=200, prefix_min=200), 200, 128, 1.0, 0),
     ("gqa-bf16-65rows", dict(prefix=129, prefix_min=129), 129, 65, 1.0, 0),
