@@ -225,8 +225,7 @@ def run_ours(args):
             with torch.cuda.graph(g, stream=stream):
                 st.run(stream)
     step = (lambda: g.replay()) if g is not None else (lambda: st.run(stream))
-    splits = B.workspace_size(B.EAGLE_WS_TREE_ATTN, st.attn_desc)  # noqa: F841 (plan is fixed per desc)
-    per_layer_launches = 1 if st.attn_ws.numel() <= 16 else 2
+    attn_splits, per_layer_launches = B.tree_attn_plan(st.attn_desc)
     launches_per_step = st.L * per_layer_launches + 2 + 2
 
     with torch.cuda.stream(stream):
@@ -314,7 +313,7 @@ def run_ours(args):
             "unit": "steps/s", "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(ms_per_step, 5), "us_per_step": round(ms_per_step * 1e3, 2),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
-            "config": {**_workload_desc(w, batch), "l2": l2_note, "graph": g is not None,
+            "config": {**_workload_desc(w, batch), "l2": l2_note, "graph": g is not None, "attn_splits": attn_splits,
                        "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU"},
             "step_roofline_frac": round(step_frac, 4), "step_algorithmic_bytes": int(step_bytes),
             "mean_accept_length": float(np.mean(n_acc + 1)), "roofline": roofline, "e2e": e2e,

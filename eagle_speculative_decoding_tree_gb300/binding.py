@@ -31,7 +31,7 @@ EAGLE_STATUS_BAD_TREE, EAGLE_STATUS_PATH_OVERFLOW, EAGLE_STATUS_CACHE_FULL, EAGL
 EXPORTED_SYMBOLS = ("eagle_tree_build", "eagle_tree_attn", "eagle_accept", "eagle_kv_commit",
                     "eagle_workspace_size", "eagle_status_string", "eagle_version",
                     "eagle_tree_frontier_rows", "eagle_tree_max_frontier", "eagle_last_cuda_error",
-                    "eagle_last_cuda_error_string")
+                    "eagle_last_cuda_error_string", "eagle_tree_attn_plan")
 
 
 class TreeDesc(ctypes.Structure):
@@ -99,8 +99,10 @@ def load() -> ctypes.CDLL:
         L.eagle_last_cuda_error_string.restype = ctypes.c_char_p
         L.eagle_tree_frontier_rows.argtypes = [ctypes.POINTER(TreeDesc), i32]
         L.eagle_tree_max_frontier.argtypes = [ctypes.POINTER(TreeDesc)]
+        L.eagle_tree_attn_plan.argtypes = [ctypes.POINTER(AttnDesc), ctypes.POINTER(ctypes.c_int32),
+                                           ctypes.POINTER(ctypes.c_int32)]
         for f in (L.eagle_tree_build, L.eagle_tree_attn, L.eagle_accept, L.eagle_kv_commit,
-                  L.eagle_tree_frontier_rows, L.eagle_tree_max_frontier):
+                  L.eagle_tree_frontier_rows, L.eagle_tree_max_frontier, L.eagle_tree_attn_plan):
             f.restype = ctypes.c_int
         _lib = L
     return _lib
@@ -163,6 +165,15 @@ def tree_desc(batch, vocab, mode, depth, top_k=0, total_tokens=0, static_parent:
 
 def workspace_size(which: int, desc) -> int:
     return int(load().eagle_workspace_size(which, ctypes.cast(ctypes.pointer(desc), ctypes.c_void_p)))
+
+
+def tree_attn_plan(desc: AttnDesc) -> tuple:
+    """(splits, kernel launches per call) eagle_tree_attn uses for desc on this device."""
+    sp, kn = ctypes.c_int32(0), ctypes.c_int32(0)
+    st = load().eagle_tree_attn_plan(ctypes.byref(desc), ctypes.byref(sp), ctypes.byref(kn))
+    if st != EAGLE_OK:
+        raise EagleError("eagle_tree_attn_plan", st)
+    return sp.value, kn.value
 
 
 def tree_frontier_rows(desc: TreeDesc, level: int) -> int:

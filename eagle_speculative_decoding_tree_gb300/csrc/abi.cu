@@ -157,6 +157,17 @@ int eagle_tree_max_frontier(const eagle_tree_desc* d) {
   return p.f_max;
 }
 
+int eagle_tree_attn_plan(const eagle_attn_desc* d, int32_t* splits, int32_t* kernels) {
+  if (!d) return EAGLE_ERR_INVALID_ARG;
+  const int st = check_attn_desc(d);
+  if (st != EAGLE_OK) return st;
+  AttnPlan p;
+  plan_tree_attn(d, num_sms(), &p);
+  if (splits) *splits = p.splits;
+  if (kernels) *kernels = (p.splits > 1 && !p.coop) ? 2 : 1;
+  return EAGLE_OK;
+}
+
 int eagle_tree_build(const eagle_tree_desc* d, int level, const void* frontier_logits, const float* u_draft,
                      const int32_t* root_tok, const int32_t* seq_len, void* ws, size_t ws_bytes,
                      const eagle_tree* out, void* stream) {

@@ -560,7 +560,7 @@ void plan_tree_attn(const eagle_attn_desc* d, int num_sms, AttnPlan* p) {
   size_t off = p->tc ? 256 : 0;  // tcgen05: error word first
   if (p->coop) {
     p->off_cnt = off;
-    off += (static_cast<size_t>(base) * 4 + 255) / 256 * 256;
+    off += (static_cast<size_t>(base) * 8 + 255) / 256 * 256;  // published / finished counts
   }
   if (splits > 1) {
     const size_t rows = static_cast<size_t>(p->B) * p->Hkv * splits * p->rows_pad;

@@ -19,12 +19,19 @@
 //                 O is rescaled in TMEM only when the row max grows by more than 2^8.
 // MMA issue order QK0 QK1 | PV0 QK0' PV1 QK1' | ...: the tensor cores run M-tile 0's
 // PV and next QK while the warps do M-tile 1's softmax, and the other way round.
-// TMEM columns: S0 [0,128) S1 [128,256) O0 [256,384) O1 [384,512).  Splits write
-// unnormalised partials (O, m, l), O by TMA store, merged by the shared combine
-// kernel; a single split writes the output directly.
+// TMEM columns: S0 [0,128) S1 [128,256) O0 [256,384) O1 [384,512).
 //
-// Every mbarrier wait is bounded; a timeout ORs a bit into an error word at the
-// start of the workspace and the roles stop, so the kernel ends instead of hanging.
+// Splits: each CTA covers a contiguous range of key tiles (the tree tile counts as
+// one) and keeps unnormalised partials (O, m, l).  One split writes the output
+// directly.  When the whole grid fits on the SMs at once the launch is cooperative:
+// every split stores its partial rows (TMA) and counts itself into its group
+// (request, KV head, row block); once the group is complete each CTA merges a slice
+// of the group's rows from L2.  Otherwise the shared combine kernel merges them.
+//
+// Every wait is bounded; a timeout ORs a bit into the error word at the start of the
+// workspace (it stays set until the caller clears it) and the roles stop, so the
+// kernel ends instead of hanging.  The group counters return to zero by the end of
+// every launch, so a zero-filled workspace stays valid across calls.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -65,7 +72,8 @@ struct TcArgs {
   int* err;
   int B, R, Hq, Hkv, G, P, W, splits, rows_pad, rows_per_cta, n_mt, out_f32;
   int coop;        // 1: the splits of a group merge their partials in this kernel
-  int* cnt;        // coop: per (request, KV head, row block) count of published splits
+  int* cnt;        // coop: [2][n_groups] published / finished splits per (request, KV head, row block)
+  int n_groups;
   float scale, scale_log2;
 };
 
@@ -557,7 +565,17 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       fence_proxy_async_global();
       __threadfence();
       bar_sync(2, 256);
-      if (threadIdx.x == 0) s_go = group_arrive_wait(a.cnt + bh * gridDim.z + rb, a.splits, a.err) ? 1 : 0;
+      const int grp = bh * gridDim.z + rb;
+      if (threadIdx.x == 0) {
+        s_go = group_arrive_wait(a.cnt + grp, a.splits, a.err) ? 1 : 0;
+        // past the wait: the last split of the group to get here returns both counters
+        // to zero for the next call
+        int* done = a.cnt + a.n_groups + grp;
+        if (atomicAdd(done, 1) == a.splits - 1) {
+          atomicExch(a.cnt + grp, 0);
+          atomicExch(done, 0);
+        }
+      }
       bar_sync(2, 256);
       if (s_go) {
         // a warp per row; every load of a row (the splits' (m, l) one per lane, their
@@ -747,12 +765,11 @@ cudaError_t launch_tree_attn_tc(const AttnPlan& p, const void* q, const void* k_
   a.n_mt = p.rows_per_cta / 128;
   a.coop = p.coop ? 1 : 0;
   a.cnt = p.coop ? reinterpret_cast<int*>(w + p.off_cnt) : nullptr;
+  a.n_groups = p.B * p.Hkv * p.row_blocks;
   a.out_f32 = p.out_dtype == EAGLE_F32;
   a.scale = p.scale;
   a.scale_log2 = p.scale * kLog2e;
-  // error word (and the split-group counters of a cooperative launch) start at zero
-  cudaError_t e = cudaMemsetAsync(w, 0, p.coop ? p.off_o : sizeof(int), s);
-  if (e != cudaSuccess) return e;
+  cudaError_t e;
   dim3 grid(p.splits, p.B * p.Hkv, p.row_blocks);
   e = p.precise ? launch_tc<true>(tm, a, grid, s) : launch_tc<false>(tm, a, grid, s);
   if (e != cudaSuccess || !partials || p.coop) return e;

@@ -185,16 +185,27 @@ typedef struct {
  *   q [B][R][Hq][D]; k_cache, v_cache [B][Hkv][P][D]; tree_k, tree_v [B][Hkv][R][D];
  *   seq_len [B] int32 (0 <= seq_len <= P); anc_mask [B][R][W]; out [B][R][Hq][D];
  *   lse [B][R][Hq] fp32, may be NULL.
- * ws: eagle_workspace_size(EAGLE_WS_TREE_ATTN, d) bytes (split partials).  The tcgen05
- * kernel keeps an error word in the first 16 bytes of ws (cleared by the call): a
- * non-zero value after the stream completes means a bounded wait inside the kernel
- * gave up, and the outputs of that call are not valid.
+ * ws: eagle_workspace_size(EAGLE_WS_TREE_ATTN, d) bytes (split partials and, for the
+ * tcgen05 kernel, an error word and split-group counters), zero-filled by the caller
+ * before its first use; every call leaves the counters at zero again.  The tcgen05
+ * kernel ORs a bit into the error word (the first 4 bytes of ws) when a bounded wait
+ * inside it gives up; the word stays set until the caller clears it, and the outputs
+ * of the calls made since it was last zero are not valid (re-zero the whole workspace
+ * before further use).  When the splits merge inside the kernel its launch is
+ * cooperative (all CTAs resident at once, one per SM).
  * Unsupported: head_dim not 64/128, R > 128, Hq % Hkv != 0, B * Hkv > 65535, bf16 out
  * with fp32 inputs. */
 int eagle_tree_attn(const eagle_attn_desc* d, const void* q, const void* k_cache, const void* v_cache,
                     const void* tree_k, const void* tree_v, const int32_t* seq_len,
                     const uint64_t* anc_mask, void* out, float* lse, void* ws, size_t ws_bytes,
                     void* stream);
+
+/* How eagle_tree_attn runs a descriptor on the current device (no counterpart in the
+ * method's description; it reports the launch plan): *splits = prefix splits per
+ * (request, KV head, row block), *kernels = kernel launches one call makes (1, or 2
+ * when a separate kernel merges the splits).  Either pointer may be NULL.  Returns
+ * EAGLE_OK, or the status eagle_tree_attn would return for a bad descriptor. */
+int eagle_tree_attn_plan(const eagle_attn_desc* d, int32_t* splits, int32_t* kernels);
 
 /* ---------------------------------------------------------------- acceptance */
 typedef struct {

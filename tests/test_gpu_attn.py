@@ -6,13 +6,16 @@ GQA-4, ragged batches) in the launch configuration the benchmark uses, and check
 whole KV heads against the oracle.  Tolerance: max abs error 2e-3 for bf16 inputs
 (fp32 accumulation), 1e-5 for fp32.
 """
+import math
+
 import numpy as np
 import pytest
+import torch
 
 import oracle
 from eagle_speculative_decoding_tree_gb300 import binding as B
 from eagle_speculative_decoding_tree_gb300 import synth
-from gpu_helpers import BF16_TOL, F32_TOL, head_slice, random_tree, run_attn
+from gpu_helpers import BF16_TOL, F32_TOL, dev, head_slice, random_tree, run_attn
 
 pytestmark = pytest.mark.gpu
 
@@ -133,3 +136,32 @@ def test_tree_attention_full_size_concurrency_batch8():
     seq_len = synth.prefix_lengths(w, 8)
     par, mask = random_tree(w.rows, seed=12)
     _check(w, 8, seq_len, w.rows, par, mask, [(0, 0), (7, 7), (3, 2)], strict_standard=True)
+
+
+@pytest.mark.gpu
+def test_tree_attention_workspace_reuse():
+    """Calls on one workspace: identical outputs, group counters back at zero, no timeouts."""
+    w = W["llama8b"]
+    rows = w.rows
+    par, mask = random_tree(rows, seed=21)
+    seq_len = synth.prefix_lengths(w, 1)
+    q, kc, vc, tk, tv = synth.attn_tensors(w, 0, 1, seq_len, rows, 1.0)
+    desc = B.AttnDesc(1, rows, w.n_q_heads, w.n_kv_heads, w.head_dim, w.max_seq, 1.0 / math.sqrt(w.head_dim),
+                      B.EAGLE_BF16, 0, B.EAGLE_BF16, B.EAGLE_ATTN_STANDARD, B.EAGLE_ENGINE_AUTO)
+    splits, kernels = B.tree_attn_plan(desc)
+    ws = torch.zeros(B.workspace_size(B.EAGLE_WS_TREE_ATTN, desc), dtype=torch.uint8, device="cuda")
+    args = [dev(x, w.dtype) for x in (q, kc, vc, tk, tv)]
+    sl = torch.from_numpy(np.asarray(seq_len, np.int32)).cuda()
+    am = torch.from_numpy(np.ascontiguousarray(mask).view(np.int64)).cuda().reshape(1, rows, -1)
+    outs = []
+    for _ in range(3):
+        out = torch.empty_like(args[0])
+        lse = torch.empty(1, rows, w.n_q_heads, dtype=torch.float32, device="cuda")
+        B.eagle_tree_attn(desc, *args, sl, am, out, lse, ws)
+        torch.cuda.synchronize()
+        outs.append((out.clone(), lse.clone()))
+    for o, l in outs[1:]:
+        assert torch.equal(o, outs[0][0]) and torch.equal(l, outs[0][1])
+    assert int(ws[:4].view(torch.int32).item()) == 0
+    if kernels == 1 and splits > 1:  # merged in the kernel: counters live after the error word
+        assert int(ws[256:512].count_nonzero().item()) == 0
