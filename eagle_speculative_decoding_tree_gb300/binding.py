@@ -31,7 +31,7 @@ EAGLE_STATUS_BAD_TREE, EAGLE_STATUS_PATH_OVERFLOW, EAGLE_STATUS_CACHE_FULL, EAGL
 EXPORTED_SYMBOLS = ("eagle_tree_build", "eagle_tree_attn", "eagle_accept", "eagle_kv_commit",
                     "eagle_workspace_size", "eagle_status_string", "eagle_version",
                     "eagle_tree_frontier_rows", "eagle_tree_max_frontier", "eagle_last_cuda_error",
-                    "eagle_last_cuda_error_string", "eagle_tree_attn_plan")
+                    "eagle_last_cuda_error_string", "eagle_tree_attn_plan", "eagle_accept_noalloc")
 
 
 class TreeDesc(ctypes.Structure):
@@ -89,6 +89,8 @@ def load() -> ctypes.CDLL:
         L.eagle_tree_attn.argtypes = [ctypes.POINTER(AttnDesc), vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
         L.eagle_accept.argtypes = [ctypes.POINTER(AcceptDesc), vp, vp, vp, vp, vp, vp, ctypes.POINTER(AcceptOut), vp,
                                    sz, vp]
+        L.eagle_accept_noalloc.argtypes = [ctypes.POINTER(AcceptDesc), vp, vp, vp, vp, vp, vp,
+                                           ctypes.POINTER(AcceptOut), vp]
         L.eagle_kv_commit.argtypes = [ctypes.POINTER(CommitDesc), vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
         L.eagle_workspace_size.argtypes = [i32, vp]
         L.eagle_workspace_size.restype = sz
@@ -102,7 +104,8 @@ def load() -> ctypes.CDLL:
         L.eagle_tree_attn_plan.argtypes = [ctypes.POINTER(AttnDesc), ctypes.POINTER(ctypes.c_int32),
                                            ctypes.POINTER(ctypes.c_int32)]
         for f in (L.eagle_tree_build, L.eagle_tree_attn, L.eagle_accept, L.eagle_kv_commit,
-                  L.eagle_tree_frontier_rows, L.eagle_tree_max_frontier, L.eagle_tree_attn_plan):
+                  L.eagle_tree_frontier_rows, L.eagle_tree_max_frontier, L.eagle_tree_attn_plan,
+                  L.eagle_accept_noalloc):
             f.restype = ctypes.c_int
         _lib = L
     return _lib
@@ -266,6 +269,18 @@ def eagle_accept(desc: AcceptDesc, target_logits, draft_logits, tree_tokens, tre
         _ptr(tree_tokens, torch.int32, "tree_tokens"), _ptr(tree_parent, torch.int32, "tree_parent"),
         _ptr(u_accept, torch.float32, "u_accept"), _ptr(u_final, torch.float32, "u_final"), ctypes.byref(o),
         _ptr(ws, name="ws"), ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def eagle_accept_noalloc(desc: AcceptDesc, target_logits, draft_logits, tree_tokens, tree_parent, u_accept,
+                         u_final, out: AcceptBuffers, stream=None) -> None:
+    """eagle_accept with the library's fixed device scratch instead of a workspace (see
+    eagle.h: eagle_accept_noalloc)."""
+    o = out.c_struct()
+    _check("eagle_accept_noalloc", load().eagle_accept_noalloc(
+        ctypes.byref(desc), _ptr(target_logits, FLOATS, "target_logits"), _ptr(draft_logits, FLOATS, "draft_logits"),
+        _ptr(tree_tokens, torch.int32, "tree_tokens"), _ptr(tree_parent, torch.int32, "tree_parent"),
+        _ptr(u_accept, torch.float32, "u_accept"), _ptr(u_final, torch.float32, "u_final"), ctypes.byref(o),
+        _stream(stream)))
 
 
 class LayerPointers:

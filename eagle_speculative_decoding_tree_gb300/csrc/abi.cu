@@ -95,6 +95,10 @@ int check_accept_desc(const eagle_accept_desc* d) {
 
 }  // namespace
 
+// Records a CUDA error for eagle_last_cuda_error() and returns EAGLE_ERR_CUDA (EAGLE_OK
+// for cudaSuccess); for entry points defined in other translation units.
+int eagle::report_cuda_error(cudaError_t e) { return cuda_status(e); }
+
 extern "C" {
 
 const char* eagle_version(void) { return "eagle-tree-gb300 0.1 (sm_103a)"; }

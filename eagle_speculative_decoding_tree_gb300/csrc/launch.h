@@ -48,6 +48,9 @@ struct AttnPlan {
                      // (request, KV head, row block) merge their partials in the kernel
   size_t off_err, off_cnt, off_o, off_ml, total;
 };
+// Records a CUDA error for eagle_last_cuda_error(); EAGLE_ERR_CUDA (EAGLE_OK on success).
+int report_cuda_error(cudaError_t e);
+
 void plan_tree_attn(const eagle_attn_desc* d, int num_sms, AttnPlan* p);
 // Merge split partials into out / lse (shared by the mma.sync and tcgen05 kernels).
 cudaError_t launch_tree_attn_combine(const AttnPlan& p, void* out, float* lse, const float* part_o,

@@ -243,6 +243,30 @@ int eagle_accept(const eagle_accept_desc* d, const void* target_logits, const vo
                  const float* u_final, const eagle_accept_out* out, void* ws, size_t ws_bytes,
                  void* stream);
 
+/* eagle_accept without a caller workspace.  The method's description has no
+ * counterpart: this is a deployment convenience for callers that cannot allocate
+ * device memory when they verify a draft (memory reserved up front, an allocator
+ * that is not reachable from the calling thread, plain C code with no device
+ * allocator).  Same arguments, semantics and kernels as eagle_accept, minus ws and
+ * ws_bytes: the scratch eagle_accept would take from ws lives in a device array of
+ * EAGLE_ACCEPT_NOALLOC_SCRATCH_BYTES inside the library (one per device).  The call
+ * allocates nothing.
+ *   - A descriptor whose scratch (eagle_workspace_size(EAGLE_WS_ACCEPT, d)) exceeds
+ *     EAGLE_ACCEPT_NOALLOC_SCRATCH_BYTES is rejected with EAGLE_ERR_WORKSPACE before
+ *     anything is launched.  4 MiB is 768 bytes per tree row and proposal source at
+ *     vocab 128256: up to 89 requests of 61 rows with one source, 44 with the draft
+ *     logits as a second source.
+ *   - The first call on each device looks the buffer's address up (a CUDA runtime
+ *     query, done once per device with that device current); make that first call
+ *     outside any stream capture.
+ *   - The buffer needs no clearing: every entry is written before it is read.
+ *   - One buffer per device: calls on the same device must not overlap in time
+ *     (concurrent streams or host threads would race on it). */
+#define EAGLE_ACCEPT_NOALLOC_SCRATCH_BYTES (4u << 20)
+int eagle_accept_noalloc(const eagle_accept_desc* d, const void* target_logits, const void* draft_logits,
+                         const int32_t* tree_tokens, const int32_t* tree_parent, const float* u_accept,
+                         const float* u_final, const eagle_accept_out* out, void* stream);
+
 /* ---------------------------------------------------------------- KV commit */
 typedef struct {
   int32_t layers;      /* L, 1..128 */
