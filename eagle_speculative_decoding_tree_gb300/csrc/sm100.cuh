@@ -156,6 +156,13 @@ __device__ __forceinline__ int ld_acquire_gpu(const int* p) {
 }
 
 // ------------------------------------------------------------------ special functions
+// max(a, b, c) in one instruction (three-input max.f32).
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
 // 2^x on the multi-function unit (PTX ex2.approx, subnormal results flushed to 0;
 // 2^-inf = 0).
 __device__ __forceinline__ float ex2(float x) {

@@ -142,16 +142,21 @@ __device__ __forceinline__ void mask_keys(uint32_t (&r)[32], uint32_t bits) {
   for (int j = 0; j < 32; ++j) r[j] = ((bits >> j) & 1u) ? r[j] : 0xff800000u;
 }
 
-// Maximum of 32 floats as a balanced tree (short dependency chains).
-__device__ __forceinline__ float max32(const uint32_t (&r)[32]) {
-  float m[16];
+// Maximum of 64 floats with three-input max instructions, as a shallow tree.
+__device__ __forceinline__ float max64(const uint32_t (&a)[32], const uint32_t (&b)[32]) {
+  float m[22];
 #pragma unroll
-  for (int j = 0; j < 16; ++j) m[j] = fmaxf(__uint_as_float(r[j]), __uint_as_float(r[j + 16]));
+  for (int i = 0; i < 10; ++i)
+    m[i] = max3(__uint_as_float(a[3 * i]), __uint_as_float(a[3 * i + 1]), __uint_as_float(a[3 * i + 2]));
+  m[10] = max3(__uint_as_float(a[30]), __uint_as_float(a[31]), __uint_as_float(b[0]));
 #pragma unroll
-  for (int w = 8; w >= 1; w >>= 1)
+  for (int i = 0; i < 10; ++i)
+    m[11 + i] = max3(__uint_as_float(b[3 * i + 1]), __uint_as_float(b[3 * i + 2]), __uint_as_float(b[3 * i + 3]));
+  m[21] = fmaxf(__uint_as_float(b[31]), m[0]);
+  float n[7];
 #pragma unroll
-    for (int j = 0; j < w; ++j) m[j] = fmaxf(m[j], m[j + w]);
-  return m[0];
+  for (int i = 0; i < 7; ++i) n[i] = max3(m[3 * i + 1], m[3 * i + 2], m[3 * i + 3]);
+  return max3(max3(n[0], n[1], n[2]), max3(n[3], n[4], n[5]), n[6]);
 }
 
 template <bool PRECISE>
@@ -371,7 +376,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             mask_keys(s0, k0);
             mask_keys(s1, k1);
           }
-          mx = fmaxf(max32(s0), max32(s1));
+          mx = max64(s0, s1);
         }
         s_red[t & 1][i][hf][r_local] = mx;
         if (!bar_and(1, 256, got)) {  // every softmax warp leaves together on a timeout
@@ -404,7 +409,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         // pass 2: S again from TMEM, P = 2^(s c - m c) as bf16 pairs (masked keys hold
         // -inf and give exactly 0): keys 64 hf + 32 c .. + 31 go to columns
         // 64 hf + 16 c .. + 15; the precise path puts the low parts 32 columns further
-        // on.  Both chunks are read before either is written.
+        // on.  Both chunks are read before either is written.  l sums the fp32 p (the
+        // precise path: hi + lo).
         float ls[4] = {0.f, 0.f, 0.f, 0.f};
         auto emit = [&](const uint32_t (&r)[32], int c) {
           uint32_t hi[16], lo[PRECISE ? 16 : 1];
@@ -414,13 +420,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             const float p1 = ex2(fmaf(__uint_as_float(r[2 * j + 1]), sl2, -mu));
             __nv_bfloat162 u = __floats2bfloat162_rn(p0, p1);
             hi[j] = *reinterpret_cast<uint32_t*>(&u);
-            const float h0 = __uint_as_float(hi[j] << 16), h1 = __uint_as_float(hi[j] & 0xffff0000u);
             if constexpr (PRECISE) {
+              const float h0 = __uint_as_float(hi[j] << 16), h1 = __uint_as_float(hi[j] & 0xffff0000u);
               __nv_bfloat162 w = __floats2bfloat162_rn(p0 - h0, p1 - h1);
               lo[j] = *reinterpret_cast<uint32_t*>(&w);
               ls[j & 3] += (h0 + __uint_as_float(lo[j] << 16)) + (h1 + __uint_as_float(lo[j] & 0xffff0000u));
             } else {
-              ls[j & 3] += h0 + h1;
+              ls[j & 3] += p0 + p1;
             }
           }
           tmem_st16(lb + col_s(i) + 64 * hf + 16 * c, hi);
