@@ -46,6 +46,7 @@ struct AttnPlan {
   int rows_pad;      // row_blocks * rows_per_cta
   bool coop;         // tcgen05, splits > 1, grid fits on the SMs at once: the splits of a
                      // (request, KV head, row block) merge their partials in the kernel
+  bool part_bf16;    // coop with standard precision: partial O kept as bf16
   size_t off_err, off_cnt, off_o, off_ml, total;
 };
 // Records a CUDA error for eagle_last_cuda_error(); EAGLE_ERR_CUDA (EAGLE_OK on success).

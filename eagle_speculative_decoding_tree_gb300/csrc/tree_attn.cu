@@ -522,6 +522,7 @@ void plan_tree_attn(const eagle_attn_desc* d, int num_sms, AttnPlan* p) {
   p->off_err = p->off_cnt = p->off_o = p->off_ml = p->total = 0;
   p->tc = false;
   p->coop = false;
+  p->part_bf16 = false;
   const int RG = p->R * p->G;
   if (p->dtype == EAGLE_F32) {
     p->rows_per_cta = 4;
@@ -557,6 +558,8 @@ void plan_tree_attn(const eagle_attn_desc* d, int num_sms, AttnPlan* p) {
   // the kernel merges the partials itself (cooperative launch); else the combine
   // kernel does.
   p->coop = p->tc && splits > 1 && static_cast<long long>(base) * splits <= num_sms;
+  // the kernel's own merge keeps partial O in bf16 unless the precise mode was asked for
+  p->part_bf16 = p->coop && !p->precise;
   size_t off = p->tc ? 256 : 0;  // tcgen05: error word first
   if (p->coop) {
     p->off_cnt = off;
@@ -565,7 +568,7 @@ void plan_tree_attn(const eagle_attn_desc* d, int num_sms, AttnPlan* p) {
   if (splits > 1) {
     const size_t rows = static_cast<size_t>(p->B) * p->Hkv * splits * p->rows_pad;
     p->off_o = off;
-    off += ((rows * p->D * 4) + 255) / 256 * 256;
+    off += ((rows * p->D * (p->part_bf16 ? 2 : 4)) + 255) / 256 * 256;
     p->off_ml = off;
     off += rows * 2 * 4;
   }

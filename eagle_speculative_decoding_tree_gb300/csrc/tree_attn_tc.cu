@@ -36,6 +36,7 @@
 #include <cudaTypedefs.h>
 
 #include <cstring>
+#include <type_traits>
 
 #include "common.cuh"
 #include "launch.h"
@@ -67,7 +68,8 @@ struct TcArgs {
   const uint64_t* anc_mask;
   void* out;
   float* lse;
-  float* part_o;   // [B*Hkv][splits][rows_pad][128]
+  void* part_o;    // [B*Hkv][splits][rows_pad][128], bf16 when part_bf16 else fp32
+  int part_bf16;
   float* part_ml;  // [B*Hkv][splits][rows_pad][2]
   int* err;
   int B, R, Hq, Hkv, G, P, W, splits, rows_pad, rows_per_cta, n_mt, out_f32;
@@ -83,7 +85,7 @@ struct Tmaps {
   CUtensorMap vc;
   CUtensorMap tk;  // [B*Hkv*R][128], box {64, 128}
   CUtensorMap tv;
-  CUtensorMap po;  // fp32 partial O [B*Hkv*splits*rows_pad][128], box {32, 128}
+  CUtensorMap po;  // partial O [B*Hkv*splits*rows_pad][128]: fp32 box {32, 128} or bf16 box {64, 128}
 };
 
 struct TileInfo {
@@ -111,6 +113,84 @@ __device__ __forceinline__ TileInfo tile_info(const TcArgs& a, int b, int split)
 __device__ __forceinline__ int tile_valid(const TcArgs& a, const TileInfo& ti, int t) {
   if (t < ti.n_pt) return min(KT, ti.L - (ti.t_begin + t) * KT);
   return a.R;
+}
+
+// Partial-O row `prow`, columns 4 lane .. 4 lane + 3, through L2: raw bf16 (uint2) or
+// fp32 (float4) words, converted only where they are used.
+template <bool BF16>
+struct PartWords {
+  using T = typename std::conditional<BF16, uint2, float4>::type;
+  static __device__ __forceinline__ T load(const TcArgs& a, size_t prow, int lane) {
+    if constexpr (BF16)
+      return __ldcg(reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(a.part_o) + prow * 128) + lane);
+    else
+      return __ldcg(reinterpret_cast<const float4*>(static_cast<const float*>(a.part_o) + prow * 128) + lane);
+  }
+  static __device__ __forceinline__ float4 f32(const T& w) {
+    if constexpr (BF16)
+      return make_float4(__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xffff0000u), __uint_as_float(w.y << 16),
+                         __uint_as_float(w.y & 0xffff0000u));
+    else
+      return w;
+  }
+};
+
+// Merge of one output row from the group's split partials, by one warp: lane s holds
+// split s's (m, l) (two per lane), M = max m_s, w_s = 2^((m_s - M) c), L = sum w_s l_s,
+// O = sum w_s O_s / L.  The first kMergeBatch partial rows are requested before any
+// is used (split indices past the last are clamped; their weight is 0), so the row
+// costs about one L2 round trip.
+template <bool BF16>
+__device__ __forceinline__ void merge_row(const TcArgs& a, int bh, int h, int b, int grow, int lane, float sl2) {
+  using PW = PartWords<BF16>;
+  const size_t base = static_cast<size_t>(bh) * a.splits * a.rows_pad + grow;
+  const size_t sstride = a.rows_pad;
+  typename PW::T v[kMergeBatch];
+#pragma unroll
+  for (int u = 0; u < kMergeBatch; ++u) v[u] = PW::load(a, base + min(u, a.splits - 1) * sstride, lane);
+  float2 ml[2];
+#pragma unroll
+  for (int k = 0; k < 2; ++k) {
+    const int sp = lane + 32 * k;
+    ml[k] = sp < a.splits ? __ldcg(reinterpret_cast<const float2*>(a.part_ml + (base + sp * sstride) * 2))
+                          : make_float2(-INFINITY, 0.f);
+  }
+  const float M = warp_max(fmaxf(ml[0].x, ml[1].x));
+  float w2[2];
+#pragma unroll
+  for (int k = 0; k < 2; ++k) w2[k] = (ml[k].x == -INFINITY) ? 0.f : ex2((ml[k].x - M) * sl2);
+  const float L = warp_sum(ml[0].y * w2[0] + ml[1].y * w2[1]);
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+  for (int u = 0; u < kMergeBatch; ++u) {
+    const float ws = __shfl_sync(0xffffffffu, w2[0], u);  // 0 for u >= splits
+    const float4 x = PW::f32(v[u]);
+    acc.x = fmaf(ws, x.x, acc.x);
+    acc.y = fmaf(ws, x.y, acc.y);
+    acc.z = fmaf(ws, x.z, acc.z);
+    acc.w = fmaf(ws, x.w, acc.w);
+  }
+  for (int sp = kMergeBatch; sp < a.splits; ++sp) {  // more splits than one batch
+    const float ws = __shfl_sync(0xffffffffu, sp < 32 ? w2[0] : w2[1], sp & 31);
+    const float4 x = PW::f32(PW::load(a, base + sp * sstride, lane));
+    acc.x = fmaf(ws, x.x, acc.x);
+    acc.y = fmaf(ws, x.y, acc.y);
+    acc.z = fmaf(ws, x.z, acc.z);
+    acc.w = fmaf(ws, x.w, acc.w);
+  }
+  const float inv = 1.f / L;
+  const int node = grow / a.G, hq = h * a.G + grow % a.G;
+  const size_t orow = (static_cast<size_t>(b * a.R + node) * a.Hq + hq) * 128 + 4 * lane;
+  if (a.out_f32) {
+    *reinterpret_cast<float4*>(static_cast<float*>(a.out) + orow) =
+        make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+  } else {
+    __nv_bfloat162 u0 = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
+    __nv_bfloat162 u1 = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
+    *reinterpret_cast<uint2*>(static_cast<uint16_t*>(a.out) + orow) =
+        make_uint2(*reinterpret_cast<uint32_t*>(&u0), *reinterpret_cast<uint32_t*>(&u1));
+  }
+  if (a.lse && lane == 0) a.lse[static_cast<size_t>(b * a.R + node) * a.Hq + hq] = a.scale * M + logf(L);
 }
 
 // Counts this split into its group and waits (at most 2 s, then ERR_GROUP) until all
@@ -461,25 +541,46 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 #pragma unroll
     for (int i = 0; i < 2; ++i) l_tot[i] = l[i] + s_l[i][hf ^ 1][r_local];
     if (a.splits > 1 && all_done) {
-      // partial O of each M-tile (128 rows x 512 B, contiguous in the workspace) is
-      // staged in the free K/V stages as four 128-byte-swizzled column slices, then
-      // stored with one TMA store per slice.  Row r's 16-byte chunk j sits at chunk
-      // j ^ (r & 7), so each quarter-warp store covers all 32 banks.
+      // partial O of each M-tile (128 rows, contiguous in the workspace) is staged in
+      // the free K/V stages as 128-byte-swizzled column slices (fp32: four slices of
+      // 32 columns; bf16: two of 64), then stored with one TMA store per slice.  Row
+      // r's 16-byte chunk j sits at chunk j ^ (r & 7), so each quarter-warp store
+      // covers all 32 banks.
 #pragma unroll
       for (int i = 0; i < 2; ++i) {
         if (i >= n_mt) break;
         uint8_t* so = smem + SM_K + i * 4 * HALF;
-#pragma unroll
-        for (int cc = 0; cc < 2; ++cc) {
-          const int c = 2 * hf + cc;
-          uint32_t o[32];
-          tmem_ld32(lb + col_o(i) + 32 * c, o);
+        if (a.part_bf16) {
+          uint32_t o0[32], o1[32];
+          tmem_ld32(lb + col_o(i) + 64 * hf, o0);
+          tmem_ld32(lb + col_o(i) + 64 * hf + 32, o1);
           tmem_ld_wait();
-          uint8_t* dst = so + c * HALF + r_local * 128;
+          uint8_t* dst = so + hf * HALF + r_local * 128;
 #pragma unroll
-          for (int j = 0; j < 8; ++j)
-            *reinterpret_cast<uint4*>(dst + ((j ^ (r_local & 7)) << 4)) =
-                make_uint4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
+          for (int j = 0; j < 8; ++j) {
+            uint32_t w[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const uint32_t* src = (j < 4) ? o0 : o1;
+              const int k = 8 * (j & 3) + 2 * e;
+              __nv_bfloat162 u = __floats2bfloat162_rn(__uint_as_float(src[k]), __uint_as_float(src[k + 1]));
+              w[e] = *reinterpret_cast<uint32_t*>(&u);
+            }
+            *reinterpret_cast<uint4*>(dst + ((j ^ (r_local & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+          }
+        } else {
+#pragma unroll
+          for (int cc = 0; cc < 2; ++cc) {
+            const int c = 2 * hf + cc;
+            uint32_t o[32];
+            tmem_ld32(lb + col_o(i) + 32 * c, o);
+            tmem_ld_wait();
+            uint8_t* dst = so + c * HALF + r_local * 128;
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+              *reinterpret_cast<uint4*>(dst + ((j ^ (r_local & 7)) << 4)) =
+                  make_uint4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
+          }
         }
       }
       fence_proxy_async_smem();
@@ -487,8 +588,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       if (threadIdx.x == 0) {
         for (int i = 0; i < n_mt; ++i) {
           const int y = (bh * a.splits + split) * a.rows_pad + rb * a.rows_per_cta + i * 128;
-#pragma unroll
-          for (int c = 0; c < 4; ++c) tma_store_2d(&tm.po, smem + SM_K + i * 4 * HALF + c * HALF, 32 * c, y);
+          const int slices = a.part_bf16 ? 2 : 4;
+          for (int c = 0; c < slices; ++c)
+            tma_store_2d(&tm.po, smem + SM_K + i * 4 * HALF + c * HALF, (a.part_bf16 ? 64 : 32) * c, y);
         }
         bulk_commit();
         if (a.coop)
@@ -544,8 +646,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 dst[j] = make_uint4(w[0], w[1], w[2], w[3]);
               }
             }
+          } else if (a.part_bf16) {  // a timed-out split: zeros (its weight is 0 too)
+            uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.part_o) + prow * 128 + 32 * c);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) dst[j] = make_uint4(0u, 0u, 0u, 0u);
           } else {
-            float4* dst = reinterpret_cast<float4*>(a.part_o + prow * 128 + 32 * c);
+            float4* dst = reinterpret_cast<float4*>(static_cast<float*>(a.part_o) + prow * 128 + 32 * c);
 #pragma unroll
             for (int j = 0; j < 8; ++j)
               dst[j] = make_float4(__uint_as_float(o[4 * j]), __uint_as_float(o[4 * j + 1]),
@@ -584,62 +690,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       }
       bar_sync(2, 256);
       if (s_go) {
-        // a warp per row; every load of a row (the splits' (m, l) one per lane, their
-        // partial rows 16 bytes per lane) is issued before any is used, so a row costs
-        // one L2 round trip for up to kMergeBatch splits
         const int n = min(a.rows_per_cta, a.R * a.G - rb * a.rows_per_cta);
         const int hi = (split + 1) * n / a.splits;
         for (int lr = split * n / a.splits + warp; lr < hi; lr += 8) {
-          const int grow = rb * a.rows_per_cta + lr;
-          const size_t base = static_cast<size_t>(bh) * a.splits * a.rows_pad + grow;
-          const size_t sstride = a.rows_pad;
-          float4 v[kMergeBatch];
-#pragma unroll
-          for (int u = 0; u < kMergeBatch; ++u)
-            v[u] = u < a.splits ? __ldcg(reinterpret_cast<const float4*>(a.part_o + (base + u * sstride) * 128) + lane)
-                                : make_float4(0.f, 0.f, 0.f, 0.f);
-          float2 ml[2];
-#pragma unroll
-          for (int k = 0; k < 2; ++k) {
-            const int sp = lane + 32 * k;
-            ml[k] = sp < a.splits ? __ldcg(reinterpret_cast<const float2*>(a.part_ml + (base + sp * sstride) * 2))
-                                  : make_float2(-INFINITY, 0.f);
-          }
-          const float M = warp_max(fmaxf(ml[0].x, ml[1].x));
-          float w2[2];
-#pragma unroll
-          for (int k = 0; k < 2; ++k) w2[k] = (ml[k].x == -INFINITY) ? 0.f : ex2((ml[k].x - M) * sl2);
-          const float L = warp_sum(ml[0].y * w2[0] + ml[1].y * w2[1]);
-          float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-          for (int u = 0; u < kMergeBatch; ++u) {
-            const float ws = __shfl_sync(0xffffffffu, w2[0], u);
-            acc.x = fmaf(ws, v[u].x, acc.x);
-            acc.y = fmaf(ws, v[u].y, acc.y);
-            acc.z = fmaf(ws, v[u].z, acc.z);
-            acc.w = fmaf(ws, v[u].w, acc.w);
-          }
-          for (int sp = kMergeBatch; sp < a.splits; ++sp) {  // more splits than one batch
-            const float ws = __shfl_sync(0xffffffffu, sp < 32 ? w2[0] : w2[1], sp & 31);
-            const float4 x = __ldcg(reinterpret_cast<const float4*>(a.part_o + (base + sp * sstride) * 128) + lane);
-            acc.x = fmaf(ws, x.x, acc.x);
-            acc.y = fmaf(ws, x.y, acc.y);
-            acc.z = fmaf(ws, x.z, acc.z);
-            acc.w = fmaf(ws, x.w, acc.w);
-          }
-          const float inv = 1.f / L;
-          const int node = grow / a.G, hq = h * a.G + grow % a.G;
-          const size_t orow = (static_cast<size_t>(b * a.R + node) * a.Hq + hq) * 128 + 4 * lane;
-          if (a.out_f32) {
-            *reinterpret_cast<float4*>(static_cast<float*>(a.out) + orow) =
-                make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
-          } else {
-            __nv_bfloat162 u0 = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
-            __nv_bfloat162 u1 = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
-            *reinterpret_cast<uint2*>(static_cast<uint16_t*>(a.out) + orow) =
-                make_uint2(*reinterpret_cast<uint32_t*>(&u0), *reinterpret_cast<uint32_t*>(&u1));
-          }
-          if (a.lse && lane == 0) a.lse[static_cast<size_t>(b * a.R + node) * a.Hq + hq] = a.scale * M + logf(L);
+          if (a.part_bf16)
+            merge_row<true>(a, bh, h, b, rb * a.rows_per_cta + lr, lane, sl2);
+          else
+            merge_row<false>(a, bh, h, b, rb * a.rows_per_cta + lr, lane, sl2);
         }
       }
     }
@@ -744,9 +801,10 @@ cudaError_t launch_tree_attn_tc(const AttnPlan& p, const void* q, const void* k_
   memset(&tm.po, 0, sizeof(tm.po));
   if (p.splits > 1) {
     const cuuint64_t dims[2] = {D, static_cast<cuuint64_t>(p.B) * p.Hkv * p.splits * p.rows_pad};
-    const cuuint64_t strides[1] = {D * 4};
-    const cuuint32_t box[2] = {32, 128};
-    if (!make_tmap(&tm.po, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, w + p.off_o, 2, dims, strides, box))
+    const cuuint64_t strides[1] = {D * (p.part_bf16 ? 2 : 4)};
+    const cuuint32_t box[2] = {p.part_bf16 ? 64u : 32u, 128};
+    if (!make_tmap(&tm.po, p.part_bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, w + p.off_o,
+                   2, dims, strides, box))
       return cudaErrorInvalidValue;
   }
   TcArgs a;
@@ -755,7 +813,8 @@ cudaError_t launch_tree_attn_tc(const AttnPlan& p, const void* q, const void* k_
   a.out = out;
   a.lse = lse;
   const bool partials = p.splits > 1;
-  a.part_o = partials ? reinterpret_cast<float*>(w + p.off_o) : nullptr;
+  a.part_o = partials ? static_cast<void*>(w + p.off_o) : nullptr;
+  a.part_bf16 = p.part_bf16 ? 1 : 0;
   a.part_ml = partials ? reinterpret_cast<float*>(w + p.off_ml) : nullptr;
   a.err = reinterpret_cast<int*>(w + p.off_err);
   a.B = p.B;
@@ -779,7 +838,7 @@ cudaError_t launch_tree_attn_tc(const AttnPlan& p, const void* q, const void* k_
   dim3 grid(p.splits, p.B * p.Hkv, p.row_blocks);
   e = p.precise ? launch_tc<true>(tm, a, grid, s) : launch_tc<false>(tm, a, grid, s);
   if (e != cudaSuccess || !partials || p.coop) return e;
-  return launch_tree_attn_combine(p, out, lse, a.part_o, a.part_ml, s);
+  return launch_tree_attn_combine(p, out, lse, static_cast<const float*>(a.part_o), a.part_ml, s);
 }
 
 }  // namespace eagle
