@@ -23,6 +23,7 @@ import json
 import math
 import os
 import subprocess
+import tempfile
 import sys
 import time
 
@@ -32,6 +33,8 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "traffic.json")
+ATTN_SRCS = [os.path.join(ROOT, "eagle_speculative_decoding_tree_gb300", "csrc", f)
+             for f in ("tree_attn_tc.cu", "sm100.cuh")]
 L2_BYTES = 129 * 1024 * 1024
 
 
@@ -83,8 +86,7 @@ class ClockSampler:
     def __init__(self, index: int):
         self.index = index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out" if os.path.isdir(os.path.join(ROOT, "gpurun_out")) else ".",
-                                 f".clocks_{os.getpid()}.csv")
+        self.path = os.path.join(tempfile.gettempdir(), f"eagle_bench_clocks_{os.getpid()}.csv")
 
     def __enter__(self):
         q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -137,14 +139,20 @@ class ClockSampler:
                 "reasons": sorted(reasons)}
 
 
-def _traffic_for(kernel_src: str, workload: str):
+def _kernel_sha(srcs) -> str:
+    h = hashlib.sha256()
+    for p in srcs:
+        h.update(open(p, "rb").read())
+    return h.hexdigest()
+
+
+def _traffic_for(kernel_srcs, workload: str):
     """dram bytes per launch from the committed ncu summary, if the kernel is unchanged."""
     try:
         with open(PROFILE_TRAFFIC) as f:
             t = json.load(f)
-        sha = hashlib.sha256(open(kernel_src, "rb").read()).hexdigest()
         e = t.get(workload)
-        if e and e.get("source_sha256") == sha:
+        if e and e.get("source_sha256") == _kernel_sha(kernel_srcs):
             return float(e["dram_bytes_per_launch"])
     except Exception:
         pass
@@ -304,9 +312,9 @@ def run_ours(args):
     peak, peak_kind = _peaks()
     bytes_layer = st.kv_bytes_per_layer()
     achieved = bytes_layer / (attn_ms / 1e3) / 1e9
-    traffic = _traffic_for(os.path.join(ROOT, "eagle_speculative_decoding_tree_gb300", "csrc", "tree_attn.cu"),
-                           args.config)
-    roofline = {"kernel": "tree_attn (split + combine launches, one layer)", "bound": "hbm",
+    traffic = _traffic_for(ATTN_SRCS, args.config)
+    roofline = {"kernel": f"tree_attn_tc_kernel ({per_layer_launches} launch(es) per layer, {attn_splits} splits)",
+                "bound": "hbm",
                 "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
                 "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
                 else "fallback 6.8 TB/s", "traffic": traffic, "algorithmic_bytes_per_launch": bytes_layer,
