@@ -492,25 +492,40 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         // on.  Both chunks are read before either is written.  l sums the fp32 p (the
         // precise path: hi + lo).
         float ls[4] = {0.f, 0.f, 0.f, 0.f};
+        uint64_t ls2[2] = {0ull, 0ull};  // standard path: packed row-sum accumulators
+        const uint64_t sl2x2 = f32x2(__float_as_uint(sl2), __float_as_uint(sl2));
+        const uint64_t nmux2 = f32x2(__float_as_uint(-mu), __float_as_uint(-mu));
         auto emit = [&](const uint32_t (&r)[32], int c) {
-          uint32_t hi[16], lo[PRECISE ? 16 : 1];
+          uint32_t hi[16];
+          if constexpr (!PRECISE) {
+            // two keys per packed instruction: x = s c - m c, then 2^x on the MUFU
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const float p0 = ex2(fmaf(__uint_as_float(r[2 * j]), sl2, -mu));
-            const float p1 = ex2(fmaf(__uint_as_float(r[2 * j + 1]), sl2, -mu));
-            __nv_bfloat162 u = __floats2bfloat162_rn(p0, p1);
-            hi[j] = *reinterpret_cast<uint32_t*>(&u);
-            if constexpr (PRECISE) {
+            for (int j = 0; j < 16; ++j) {
+              float x0, x1;
+              f32x2_split(fma_f32x2(f32x2(r[2 * j], r[2 * j + 1]), sl2x2, nmux2), x0, x1);
+              const float p0 = ex2(x0), p1 = ex2(x1);
+              __nv_bfloat162 u = __floats2bfloat162_rn(p0, p1);
+              hi[j] = *reinterpret_cast<uint32_t*>(&u);
+              ls2[j & 1] = add_f32x2(ls2[j & 1], f32x2(__float_as_uint(p0), __float_as_uint(p1)));
+            }
+            tmem_st16(lb + col_s(i) + 64 * hf + 16 * c, hi);
+          } else {
+            // P = hi + lo, both bf16; the low parts go 32 columns after the high ones
+            uint32_t lo[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const float p0 = ex2(fmaf(__uint_as_float(r[2 * j]), sl2, -mu));
+              const float p1 = ex2(fmaf(__uint_as_float(r[2 * j + 1]), sl2, -mu));
+              __nv_bfloat162 u = __floats2bfloat162_rn(p0, p1);
+              hi[j] = *reinterpret_cast<uint32_t*>(&u);
               const float h0 = __uint_as_float(hi[j] << 16), h1 = __uint_as_float(hi[j] & 0xffff0000u);
               __nv_bfloat162 w = __floats2bfloat162_rn(p0 - h0, p1 - h1);
               lo[j] = *reinterpret_cast<uint32_t*>(&w);
               ls[j & 3] += (h0 + __uint_as_float(lo[j] << 16)) + (h1 + __uint_as_float(lo[j] & 0xffff0000u));
-            } else {
-              ls[j & 3] += p0 + p1;
             }
+            tmem_st16(lb + col_s(i) + 64 * hf + 16 * c, hi);
+            tmem_st16(lb + col_s(i) + 64 * hf + 32 + 16 * c, lo);
           }
-          tmem_st16(lb + col_s(i) + 64 * hf + 16 * c, hi);
-          if constexpr (PRECISE) tmem_st16(lb + col_s(i) + 64 * hf + 32 + 16 * c, lo);
         };
         {
           uint32_t s0[32], s1[32];
@@ -524,7 +539,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           emit(s0, 0);
           emit(s1, 1);
         }
-        l[i] += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+        if constexpr (!PRECISE) {
+          float a0, a1, b0, b1;
+          f32x2_split(ls2[0], a0, a1);
+          f32x2_split(ls2[1], b0, b1);
+          l[i] += (a0 + a1) + (b0 + b1);
+        } else {
+          l[i] += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+        }
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(&p_full[i]);
