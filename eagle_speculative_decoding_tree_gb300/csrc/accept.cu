@@ -21,9 +21,11 @@
 //                           the crossing; drawn-proposal residuals take full passes.
 //
 // Precision: weights are expf((x - m) / T) in fp32; per-thread sums are compensated
-// (Neumaier) and every sum across threads, chunks or tiles is taken in double, so a
-// running sum is within about 2e-7 of the total mass of its exact value.  Draws are
-// reported as near-ties when they land within 1e-7 of the mass of a bin edge.
+// (Neumaier) and every sum across threads, chunks or tiles is float-float (about 48
+// significant bits, on the fp32 pipe: this GPU's fp64 pipe is too narrow for it), so a
+// running sum stays orders of magnitude within 1e-7 of the total mass of its exact
+// value.  Draws are reported as near-ties when they land within 1e-7 of the mass of a
+// bin edge; acceptance ratios (fp32) when within 1e-5 of u.
 #include <limits.h>
 
 #include "common.cuh"
@@ -34,14 +36,14 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kPer = kVocabChunk / kThreads;  // 16 elements per thread per tile
-constexpr double kIcdfNearEps = 1e-7;
+constexpr float kIcdfNearEps = 1e-7f;
 
 struct RowPart {
   float m;    // chunk max
   float av;   // chunk argmax value
   int ai;     // chunk argmax index (lowest on ties)
   int pad;
-  double s;   // sum exp((x - m) / T)
+  ff s;       // sum exp((x - m) / T), float-float
 };
 
 struct WalkArgs {
@@ -55,6 +57,61 @@ struct WalkArgs {
   const RowPart* part;  // [source][B*R][n_chunks]
 };
 
+// The 16 elements thread t takes of a 4096-token chunk starting at lo (each index of
+// the chunk exactly once): bf16 rows whose length is a multiple of 8 read two 16-byte
+// groups 2048 tokens apart, fp32 rows (length a multiple of 4) four groups 1024
+// apart, anything else one token per 256.  Out-of-range tokens read as -inf.  All the
+// loads are issued before any value is used.
+__device__ __forceinline__ void load_chunk(const void* base, size_t off, int lo, int hi, int dtype, int V, float (&x)[kPer],
+                                           int (&xi)[kPer]) {
+  const int t = threadIdx.x;
+  if (dtype == EAGLE_BF16 && (V & 7) == 0) {
+    uint4 u[2];
+#pragma unroll
+    for (int g = 0; g < 2; ++g) {
+      const int i0 = lo + g * 2048 + 8 * t;
+      u[g] = (i0 + 8 <= hi) ? __ldg(reinterpret_cast<const uint4*>(static_cast<const unsigned short*>(base) + off + i0))
+                            : make_uint4(0xff80ff80u, 0xff80ff80u, 0xff80ff80u, 0xff80ff80u);  // bf16 -inf pairs
+    }
+#pragma unroll
+    for (int g = 0; g < 2; ++g) {
+      x[8 * g + 0] = __uint_as_float(u[g].x << 16);
+      x[8 * g + 1] = __uint_as_float(u[g].x & 0xffff0000u);
+      x[8 * g + 2] = __uint_as_float(u[g].y << 16);
+      x[8 * g + 3] = __uint_as_float(u[g].y & 0xffff0000u);
+      x[8 * g + 4] = __uint_as_float(u[g].z << 16);
+      x[8 * g + 5] = __uint_as_float(u[g].z & 0xffff0000u);
+      x[8 * g + 6] = __uint_as_float(u[g].w << 16);
+      x[8 * g + 7] = __uint_as_float(u[g].w & 0xffff0000u);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) xi[8 * g + j] = lo + g * 2048 + 8 * t + j;
+    }
+  } else if (dtype == EAGLE_F32 && (V & 3) == 0) {
+    float4 f[4];
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+      const int i0 = lo + g * 1024 + 4 * t;
+      f[g] = (i0 + 4 <= hi) ? __ldg(reinterpret_cast<const float4*>(static_cast<const float*>(base) + off + i0))
+                            : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+    }
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+      x[4 * g + 0] = f[g].x;
+      x[4 * g + 1] = f[g].y;
+      x[4 * g + 2] = f[g].z;
+      x[4 * g + 3] = f[g].w;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) xi[4 * g + j] = lo + g * 1024 + 4 * t + j;
+    }
+  } else {
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) {
+      xi[k] = lo + k * kThreads + t;
+      x[k] = xi[k] < hi ? load_elem(base, off + xi[k], dtype) : -INFINITY;
+    }
+  }
+}
+
 __global__ void __launch_bounds__(kThreads) accept_rowstats_kernel(const AcceptPlan p, const void* target,
                                                                    const void* draft, RowPart* part) {
   const int row = blockIdx.x, c = blockIdx.y, src = blockIdx.z;
@@ -63,23 +120,30 @@ __global__ void __launch_bounds__(kThreads) accept_rowstats_kernel(const AcceptP
   const size_t off = static_cast<size_t>(row) * p.V;
   const int lo = c * kVocabChunk, hi = min(p.V, lo + kVocabChunk);
   const float invT = 1.f / (p.temperature > 0.f ? p.temperature : 1.f);
+  float x[kPer];
+  int xi[kPer];
+  load_chunk(base, off, lo, hi, p.dtype, p.V, x, xi);
+  // this thread's max and argmax (lowest index on ties), then its sum of
+  // exp((x - m) / T), compensated
   float m = -INFINITY, av = -INFINITY;
   int ai = INT_MAX;
-  CSum acc;
-  for (int v = lo + threadIdx.x; v < hi; v += kThreads) {
-    const float x = load_elem(base, off + v, p.dtype);
-    if (x > m) {
-      if (m != -INFINITY) acc.scale(expf((m - x) * invT));
-      m = x;
-    }
-    acc.add(expf((x - m) * invT));
-    if (before(x, v, av, ai)) {
-      av = x;
-      ai = v;
+#pragma unroll
+  for (int k = 0; k < kPer; ++k) {
+    if (xi[k] >= hi) continue;
+    m = fmaxf(m, x[k]);
+    if (before(x[k], xi[k], av, ai)) {
+      av = x[k];
+      ai = xi[k];
     }
   }
-  // warp max / argmax, then the sums rescaled to the warp max, in double
-  double s = acc.total();
+  CSum acc;
+  if (m != -INFINITY) {
+#pragma unroll
+    for (int k = 0; k < kPer; ++k)
+      if (xi[k] < hi) acc.add(expf((x[k] - m) * invT));
+  }
+  // warp max / argmax, then the sums rescaled to the warp max, float-float
+  ff s = csum_ff(acc);
   float M = m;
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
@@ -91,8 +155,8 @@ __global__ void __launch_bounds__(kThreads) accept_rowstats_kernel(const AcceptP
       ai = i2;
     }
   }
-  s = (m == -INFINITY) ? 0.0 : s * static_cast<double>(expf((m - M) * invT));
-  s = warp_sum_d(s);
+  s = (m == -INFINITY) ? ff_make(0.f) : ff_mul(s, expf((m - M) * invT));
+  s = warp_sum_ff(s);
   __shared__ RowPart wp[kThreads / 32];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (lane == 0) wp[warp] = RowPart{M, av, ai, 0, s};
@@ -100,9 +164,9 @@ __global__ void __launch_bounds__(kThreads) accept_rowstats_kernel(const AcceptP
   if (threadIdx.x == 0) {
     RowPart r = wp[0];
     for (int w = 1; w < kThreads / 32; ++w) r.m = fmaxf(r.m, wp[w].m);
-    double t = 0.0;
+    ff t = ff_make(0.f);
     for (int w = 0; w < kThreads / 32; ++w) {
-      if (wp[w].m != -INFINITY) t += wp[w].s * static_cast<double>(expf((wp[w].m - r.m) * invT));
+      if (wp[w].m != -INFINITY) t = ff_add(t, ff_mul(wp[w].s, expf((wp[w].m - r.m) * invT)));
       if (w > 0 && before(wp[w].av, wp[w].ai, r.av, r.ai)) {
         r.av = wp[w].av;
         r.ai = wp[w].ai;
@@ -115,36 +179,40 @@ __global__ void __launch_bounds__(kThreads) accept_rowstats_kernel(const AcceptP
 
 // ------------------------------------------------------------------ block helpers
 struct DrawScratch {
-  double wsum[kThreads / 32];
+  ff wsum[kThreads / 32];
   int found;
   int last;
-  double prev_edge, next_edge, total;
+  ff prev_edge, next_edge, total;
 };
+
+__device__ __forceinline__ ff ff_shfl_up(ff v, int o) {
+  return ff{__shfl_up_sync(0xffffffffu, v.hi, o), __shfl_up_sync(0xffffffffu, v.lo, o)};
+}
 
 // One tile of an inverse-CDF draw: elements [lo, hi) (hi - lo <= 4096), running mass
 // `base` before lo.  Each thread takes 16 consecutive elements; its running sum and
-// the thread offsets are taken in double.  Sets ds.found to the first index whose running mass
-// exceeds `target` (INT_MAX if none), ds.last to the last index with positive
+// the thread offsets are float-float.  Sets ds.found to the first index whose running
+// mass exceeds `target` (INT_MAX if none), ds.last to the last index with positive
 // weight (-1 if none) and ds.total to the tile's mass.
 template <class WF>
-__device__ void block_draw_tile(int lo, int hi, double base, double target, WF wf, DrawScratch& ds) {
+__device__ void block_draw_tile(int lo, int hi, ff base, ff target, WF wf, DrawScratch& ds) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int a0 = lo + threadIdx.x * kPer;
   float w[kPer];
-  double my = 0.0;
+  ff my = ff_make(0.f);
   int last = -1;
 #pragma unroll
   for (int e = 0; e < kPer; ++e) {
     const int v = a0 + e;
     w[e] = (v < hi) ? wf(v) : 0.f;
-    my += static_cast<double>(w[e]);
+    my = ff_add(my, w[e]);
     if (w[e] > 0.f) last = v;
   }
-  double incl = my;
+  ff incl = my;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    const double t = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += t;
+    const ff t = ff_shfl_up(incl, o);
+    if (lane >= o) incl = ff_add(incl, t);
   }
   __syncthreads();  // earlier readers of ds are done
   if (threadIdx.x == 0) {
@@ -153,24 +221,24 @@ __device__ void block_draw_tile(int lo, int hi, double base, double target, WF w
   }
   if (lane == 31) ds.wsum[warp] = incl;
   __syncthreads();
-  double wbase = 0.0, tot = 0.0;
+  ff wbase = ff_make(0.f), tot = ff_make(0.f);
   for (int i = 0; i < kThreads / 32; ++i) {
-    if (i < warp) wbase += ds.wsum[i];
-    tot += ds.wsum[i];
+    if (i < warp) wbase = ff_add(wbase, ds.wsum[i]);
+    tot = ff_add(tot, ds.wsum[i]);
   }
-  const double tbase = base + wbase + incl - my;  // mass before this thread's first element
-  const double rel = target - tbase;
+  const ff tbase = ff_sub(ff_add(ff_add(base, wbase), incl), my);  // mass before this thread's first element
+  const ff rel = ff_sub(target, tbase);
   int found = INT_MAX;
-  double pe = 0.0, ne = 0.0;
+  ff pe = ff_make(0.f), ne = ff_make(0.f);
   {
-    double cum = 0.0;
+    ff cum = ff_make(0.f);
 #pragma unroll
     for (int e = 0; e < kPer; ++e) {
-      const double nc = cum + static_cast<double>(w[e]);
-      if (found == INT_MAX && a0 + e < hi && w[e] > 0.f && nc > rel) {
+      const ff nc = ff_add(cum, w[e]);
+      if (found == INT_MAX && a0 + e < hi && w[e] > 0.f && ff_gt(nc, rel)) {
         found = a0 + e;
-        pe = tbase + cum;
-        ne = tbase + nc;
+        pe = ff_add(tbase, cum);
+        ne = ff_add(tbase, nc);
       }
       cum = nc;
     }
@@ -186,20 +254,87 @@ __device__ void block_draw_tile(int lo, int hi, double base, double target, WF w
   __syncthreads();
 }
 
-// Block sum of wf(v) over [lo, hi): compensated per thread, double across threads.
+// Block sum of wf(v) over [lo, hi): compensated per thread, float-float across threads.
 template <class WF>
-__device__ double block_sum(int lo, int hi, WF wf, double* red) {
+__device__ ff block_sum(int lo, int hi, WF wf, ff* red) {
   CSum acc;
   for (int v = lo + threadIdx.x; v < hi; v += kThreads) acc.add(wf(v));
-  double s = warp_sum_d(acc.total());
+  const ff s = warp_sum_ff(csum_ff(acc));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   __syncthreads();
   if (lane == 0) red[warp] = s;
   __syncthreads();
-  double t = 0.0;
-  for (int i = 0; i < kThreads / 32; ++i) t += red[i];
+  ff t = ff_make(0.f);
+  for (int i = 0; i < kThreads / 32; ++i) t = ff_add(t, red[i]);
   __syncthreads();
   return t;
+}
+
+// Block-wide merge of one row's chunk statistics: M = max chunk max, the argmax (lowest
+// index on ties), and the mass of each chunk relative to M, wc = s_c exp((m_c - M) / T)
+// (into tile_mass when non-null), summed as float-float.  Every thread returns the
+// totals.
+struct RowStats {
+  float M;
+  int amax;
+  ff Z;
+};
+
+__device__ RowStats merge_row_stats(const RowPart* rp, int C, float invT, ff* tile_mass, float* rf, int* ri,
+                                    ff* rd) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  float m = -INFINITY, av = -INFINITY;
+  int ai = INT_MAX;
+  for (int c = threadIdx.x; c < C; c += kThreads) {
+    const RowPart r = rp[c];
+    m = fmaxf(m, r.m);
+    if (before(r.av, r.ai, av, ai)) {
+      av = r.av;
+      ai = r.ai;
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    const float v2 = __shfl_xor_sync(0xffffffffu, av, o);
+    const int i2 = __shfl_xor_sync(0xffffffffu, ai, o);
+    if (before(v2, i2, av, ai)) {
+      av = v2;
+      ai = i2;
+    }
+  }
+  __syncthreads();  // earlier readers of the scratch are done
+  if (lane == 0) {
+    rf[warp] = m;
+    rf[kThreads / 32 + warp] = av;
+    ri[warp] = ai;
+  }
+  __syncthreads();
+  RowStats st;
+  st.M = rf[0];
+  av = rf[kThreads / 32];
+  ai = ri[0];
+  for (int w = 1; w < kThreads / 32; ++w) {
+    st.M = fmaxf(st.M, rf[w]);
+    if (before(rf[kThreads / 32 + w], ri[w], av, ai)) {
+      av = rf[kThreads / 32 + w];
+      ai = ri[w];
+    }
+  }
+  st.amax = ai;
+  ff z = ff_make(0.f);
+  for (int c = threadIdx.x; c < C; c += kThreads) {
+    const RowPart r = rp[c];
+    const ff wc = (r.m == -INFINITY) ? ff_make(0.f) : ff_mul(r.s, expf((r.m - st.M) * invT));
+    if (tile_mass) tile_mass[c] = wc;
+    z = ff_add(z, wc);
+  }
+  z = warp_sum_ff(z);
+  if (lane == 0) rd[warp] = z;
+  __syncthreads();
+  st.Z = ff_make(0.f);
+  for (int w = 0; w < kThreads / 32; ++w) st.Z = ff_add(st.Z, rd[w]);
+  return st;
 }
 
 __global__ void __launch_bounds__(kThreads) accept_walk_kernel(const AcceptPlan p, const WalkArgs a) {
@@ -208,27 +343,38 @@ __global__ void __launch_bounds__(kThreads) accept_walk_kernel(const AcceptPlan 
   const bool greedy = !(p.temperature > 0.f);
   const bool sampled = !greedy && p.proposal == EAGLE_PROPOSAL_SAMPLED;
   const float invT = 1.f / (greedy ? 1.f : p.temperature);
-  const int32_t* tok = a.tokens + static_cast<size_t>(b) * R;
-  const int32_t* par = a.parent + static_cast<size_t>(b) * R;
   const int maxp = p.max_depth + 1;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   __shared__ int s_path[kMaxRows + 1];
+  __shared__ int s_par[kMaxRows], s_tokr[kMaxRows];
+  __shared__ uint32_t s_kidmask[kMaxRows / 32];
   __shared__ int s_kids[kMaxRows];
+  __shared__ float s_wk[kMaxRows];  // point-mass proposals: exp((x_d - M) / T) of each child's token
+  __shared__ float s_uk[kMaxRows];  // the children's acceptance uniforms
   __shared__ int s_nk, s_len, s_cur, s_next, s_emit, s_done, s_near, s_flag;
   __shared__ unsigned s_status;
   __shared__ int s_rej[kMaxRows];
+  __shared__ float s_rejw[kMaxRows];
   __shared__ int s_nrej;
-  __shared__ double s_Z[kMaxRows];
+  __shared__ float s_Z[kMaxRows];  // drawn proposals: normalisers of the residual chain
   __shared__ int s_nz;
   __shared__ float s_M, s_Mq;
-  __shared__ double s_Zt, s_Zq, s_rejmass;
+  __shared__ ff s_Zt, s_Zq;
   __shared__ int s_amax;
-  __shared__ double red[kThreads / 32];
+  __shared__ ff red[kThreads / 32];
+  __shared__ float s_rf[kThreads / 16];
+  __shared__ int s_ri[kThreads / 32];
   __shared__ DrawScratch ds;
   __shared__ int s_chunk, s_fallback;
-  __shared__ double s_base, s_W;
-  __shared__ double s_tile[kMaxVocabTiles];
+  __shared__ ff s_base, s_W;
+  __shared__ ff s_tile[kMaxVocabTiles];
 
+  // the request's tree arrays, once; a parent that does not precede its row is a bad tree
+  for (int c = threadIdx.x; c < R; c += kThreads) {
+    s_par[c] = a.parent[static_cast<size_t>(b) * R + c];
+    s_tokr[c] = a.tokens[static_cast<size_t>(b) * R + c];
+  }
   if (threadIdx.x == 0) {
     s_len = 1;
     s_path[0] = 0;
@@ -239,55 +385,52 @@ __global__ void __launch_bounds__(kThreads) accept_walk_kernel(const AcceptPlan 
     s_emit = -1;
   }
   __syncthreads();
+  {
+    bool bad = false;
+    for (int c = 1 + threadIdx.x; c < R; c += kThreads) bad |= (s_par[c] >= c || s_par[c] < 0);
+    if (__syncthreads_or(bad) && threadIdx.x == 0) s_status |= EAGLE_STATUS_BAD_TREE;
+  }
 
   const size_t row_base = static_cast<size_t>(b) * R;
+  const int32_t* tok = s_tokr;
   for (int iter = 0; iter <= R && !s_done; ++iter) {
     const int cur = s_cur;
     const size_t xrow = (row_base + cur) * V;
+    // children of cur in row order: a ballot per 32 rows
+    if (warp < kMaxRows / 32) {
+      const int c = warp * 32 + lane;
+      const uint32_t mk = __ballot_sync(0xffffffffu, c > cur && c < R && s_par[c] == cur);
+      if (lane == 0) s_kidmask[warp] = mk;
+    }
+    // the target row's statistics (and the draft row's for drawn proposals)
+    const RowStats ts = merge_row_stats(a.part + (row_base + cur) * C, C, invT, s_tile, s_rf, s_ri, red);
+    RowStats qs{};
+    if (sampled)
+      qs = merge_row_stats(a.part + (static_cast<size_t>(p.B) * R + row_base + cur) * C, C, invT, nullptr, s_rf,
+                           s_ri, red);
     if (threadIdx.x == 0) {
       int nk = 0;
-      for (int c = cur + 1; c < R; ++c) {
-        const int pc = par[c];
-        if (pc >= c || pc < 0) s_status |= EAGLE_STATUS_BAD_TREE;
-        if (pc == cur) s_kids[nk++] = c;
-      }
-      s_nk = nk;
-      // merge the target row's chunk statistics
-      const RowPart* rp = a.part + (row_base + cur) * C;
-      float M = -INFINITY, av = -INFINITY;
-      int ai = INT_MAX;
-      for (int c = 0; c < C; ++c) {
-        M = fmaxf(M, rp[c].m);
-        if (before(rp[c].av, rp[c].ai, av, ai)) {
-          av = rp[c].av;
-          ai = rp[c].ai;
+      for (int w = 0; w < kMaxRows / 32; ++w) {
+        uint32_t mk = s_kidmask[w];
+        while (mk) {
+          s_kids[nk++] = w * 32 + __ffs(mk) - 1;
+          mk &= mk - 1;
         }
       }
-      double Z = 0.0;
-      for (int c = 0; c < C; ++c)
-        if (rp[c].m != -INFINITY) Z += rp[c].s * static_cast<double>(expf((rp[c].m - M) * invT));
-      s_M = M;
-      s_Zt = Z;
-      s_amax = ai;
-      if (sampled) {
-        const RowPart* dp = a.part + (static_cast<size_t>(p.B) * R + row_base + cur) * C;
-        float Mq = -INFINITY;
-        for (int c = 0; c < C; ++c) Mq = fmaxf(Mq, dp[c].m);
-        double Zq = 0.0;
-        for (int c = 0; c < C; ++c)
-          if (dp[c].m != -INFINITY) Zq += dp[c].s * static_cast<double>(expf((dp[c].m - Mq) * invT));
-        s_Mq = Mq;
-        s_Zq = Zq;
-      }
+      s_nk = nk;
+      s_M = ts.M;
+      s_Zt = ts.Z;
+      s_amax = ts.amax;
+      s_Mq = qs.M;
+      s_Zq = qs.Z;
       s_next = -1;
       s_nrej = 0;
       s_nz = 0;
-      s_rejmass = 0.0;
     }
     __syncthreads();
     const float M = s_M, Mq = s_Mq;
-    const float invZt = static_cast<float>(1.0 / s_Zt);
-    const float invZq = sampled ? static_cast<float>(1.0 / s_Zq) : 0.f;
+    const float invZt = 1.f / ff_float(s_Zt);
+    const float invZq = sampled ? 1.f / ff_float(s_Zq) : 0.f;
     auto w_target = [&](int v) { return expf((load_elem(a.target, xrow + v, p.dtype) - M) * invT); };
     auto p_of = [&](int v) { return w_target(v) * invZt; };
     auto q_of = [&](int v) { return expf((load_elem(a.draft, xrow + v, p.dtype) - Mq) * invT) * invZq; };
@@ -296,9 +439,17 @@ __global__ void __launch_bounds__(kThreads) accept_walk_kernel(const AcceptPlan 
       float pv = p_of(v);
       if (nz == 0) return pv;
       const float qv = q_of(v);
-      for (int i = 0; i < nz; ++i) pv = static_cast<float>(fmaxf(pv - qv, 0.f) / s_Z[i]);
+      for (int i = 0; i < nz; ++i) pv = fmaxf(pv - qv, 0.f) / s_Z[i];
       return pv;
     };
+    // the children's uniforms (and, for point-mass proposals, their target weights)
+    for (int i = threadIdx.x; i < s_nk; i += kThreads) {
+      const int c = s_kids[i];
+      const int d = tok[c];
+      s_uk[i] = a.u_accept[row_base + c];
+      s_wk[i] = (!greedy && !sampled && d >= 0 && d < V) ? w_target(d) : 0.f;
+    }
+    __syncthreads();
 
     if (greedy) {
       if (threadIdx.x == 0) {
@@ -317,6 +468,8 @@ __global__ void __launch_bounds__(kThreads) accept_walk_kernel(const AcceptPlan 
     } else if (!sampled) {
       // point-mass proposals: p_res(d) = p(d) / (1 - mass of the rejected tokens)
       if (threadIdx.x == 0) {
+        const float Zt = ff_float(s_Zt);
+        ff rejmass = ff_make(0.f);
         for (int i = 0; i < s_nk; ++i) {
           const int c = s_kids[i];
           const int d = tok[c];
@@ -326,18 +479,19 @@ __global__ void __launch_bounds__(kThreads) accept_walk_kernel(const AcceptPlan 
           }
           bool dup = false;
           for (int r = 0; r < s_nrej; ++r) dup |= (s_rej[r] == d);
-          const double pd = dup ? 0.0 : static_cast<double>(w_target(d)) / s_Zt;
-          const double denom = 1.0 - s_rejmass;
-          const double ratio = denom > 0.0 ? pd / denom : 0.0;
-          const double u = a.u_accept[row_base + c];
-          if (fabs(u - ratio) < static_cast<double>(kNearTieEps)) s_near = 1;
+          const float pd = dup ? 0.f : s_wk[i] / Zt;
+          const float denom = ff_float(ff_sub(ff_make(1.f), rejmass));
+          const float ratio = denom > 0.f ? pd / denom : 0.f;
+          const float u = s_uk[i];
+          if (fabsf(u - ratio) < kNearTieEps) s_near = 1;
           if (u < ratio) {
             s_next = c;
             break;
           }
           if (!dup) {
+            s_rejw[s_nrej] = s_wk[i];
             s_rej[s_nrej++] = d;
-            s_rejmass += pd;
+            rejmass = ff_add(rejmass, pd);
           }
         }
       }
@@ -353,12 +507,12 @@ __global__ void __launch_bounds__(kThreads) accept_walk_kernel(const AcceptPlan 
           if (d < 0 || d >= V) {
             s_status |= EAGLE_STATUS_BAD_TOKEN;
           } else {
-            const double qd = q_of(d);
-            const double pd = pres_of(d, nz);
-            const double ratio = qd > 0.0 ? pd / qd : INFINITY;
-            const double u = a.u_accept[row_base + c];
-            if (qd > 0.0 && fabs(u - ratio) < static_cast<double>(kNearTieEps)) s_near = 1;
-            if (!(qd > 0.0) || u < ratio)
+            const float qd = q_of(d);
+            const float pd = pres_of(d, nz);
+            const float ratio = qd > 0.f ? pd / qd : INFINITY;
+            const float u = s_uk[i];
+            if (qd > 0.f && fabsf(u - ratio) < kNearTieEps) s_near = 1;
+            if (!(qd > 0.f) || u < ratio)
               s_next = c;
             else
               s_flag = 1;
@@ -367,8 +521,8 @@ __global__ void __launch_bounds__(kThreads) accept_walk_kernel(const AcceptPlan 
         __syncthreads();
         if (s_next >= 0) break;
         if (s_flag) {
-          const double z = block_sum(0, V, [&](int v) { return fmaxf(pres_of(v, nz) - q_of(v), 0.f); }, red);
-          if (threadIdx.x == 0 && z > 0.0) s_Z[s_nz++] = z;
+          const ff z = block_sum(0, V, [&](int v) { return fmaxf(pres_of(v, nz) - q_of(v), 0.f); }, red);
+          if (threadIdx.x == 0 && z.hi > 0.f) s_Z[s_nz++] = ff_float(z);
         }
         __syncthreads();
       }
@@ -390,100 +544,73 @@ __global__ void __launch_bounds__(kThreads) accept_walk_kernel(const AcceptPlan 
     }
     if (s_done) break;
 
-    // ---- draw the emitted token from the (residual) target distribution
-    const double u = a.u_final[b];
-    if (sampled && s_nz > 0) {
-      // residual of drawn proposals: a mass per 4096-token tile, then the crossing
-      // tile is scanned element by element
-      const int nz = s_nz;
-      auto wres = [&](int v) { return pres_of(v, nz); };
+    // ---- draw the emitted token from the (residual) target distribution: a mass per
+    // 4096-token tile, the tile holding the crossing, then that tile element by element
+    const float u = a.u_final[b];
+    const bool residual = sampled && s_nz > 0;
+    const int nz = s_nz, nrej = s_nrej;
+    auto wres = [&](int v) { return pres_of(v, nz); };
+    auto w_of = [&](int v) {  // p with the rejected point-mass tokens zeroed
+      for (int r = 0; r < nrej; ++r)
+        if (s_rej[r] == v) return 0.f;
+      return w_target(v);
+    };
+    if (residual) {
       const int n_tiles = (V + kVocabChunk - 1) / kVocabChunk;
       for (int t = 0; t < n_tiles; ++t) {
-        const double m = block_sum(t * kVocabChunk, min(V, (t + 1) * kVocabChunk), wres, red);
+        const ff m = block_sum(t * kVocabChunk, min(V, (t + 1) * kVocabChunk), wres, red);
         if (threadIdx.x == 0) s_tile[t] = m;
       }
-      if (threadIdx.x == 0) {
-        double W = 0.0;
-        for (int t = 0; t < n_tiles; ++t) W += s_tile[t];
-        const double target = u * W;
-        double cum = 0.0, bs = 0.0;
-        int ts = -1, lastt = -1;
-        for (int t = 0; t < n_tiles; ++t) {
-          if (s_tile[t] > 0.0) lastt = t;
-          if (ts < 0 && cum + s_tile[t] > target) {
-            ts = t;
-            bs = cum;
-          }
-          cum += s_tile[t];
-        }
-        s_fallback = ts < 0;
-        if (ts < 0) ts = lastt < 0 ? 0 : lastt;
-        s_chunk = ts;
-        s_base = bs;
-        s_W = W;
+    }
+    if (threadIdx.x == 0) {
+      // tile masses: the residual's, or the row's chunk masses less the rejected tokens
+      ff W = ff_make(0.f);
+      if (residual) {
+        for (int t = 0; t < C; ++t) W = ff_add(W, s_tile[t]);
+      } else {
+        W = s_Zt;
+        for (int r = 0; r < nrej; ++r) W = ff_sub(W, ff_make(s_rejw[r]));
       }
-      __syncthreads();
-      const int lo = s_chunk * kVocabChunk;
-      const double W = s_W, target = s_fallback ? INFINITY : u * W;
-      block_draw_tile(lo, min(V, lo + kVocabChunk), s_base, target, wres, ds);
-      if (threadIdx.x == 0) {
-        int emit = ds.found;
-        if (emit == INT_MAX) {
-          emit = ds.last < 0 ? lo : ds.last;
-          s_near = 1;
-        } else if (target - ds.prev_edge < kIcdfNearEps * W || ds.next_edge - target < kIcdfNearEps * W) {
-          s_near = 1;
-        }
-        s_emit = emit;
-      }
-    } else {
-      // untouched p, or p with the rejected point-mass tokens zeroed: skip to the chunk
-      const int nrej = s_nrej;
-      auto w_of = [&](int v) {
-        for (int r = 0; r < nrej; ++r)
-          if (s_rej[r] == v) return 0.f;
-        return w_target(v);
-      };
-      if (threadIdx.x == 0) {
-        const RowPart* rp = a.part + (row_base + cur) * C;
-        double W = 0.0;
-        for (int c = 0; c < C; ++c)
-          if (rp[c].m != -INFINITY) W += rp[c].s * static_cast<double>(expf((rp[c].m - M) * invT));
-        for (int r = 0; r < nrej; ++r) W -= static_cast<double>(w_target(s_rej[r]));
-        const double target = u * W;
-        double cum = 0.0, bs = 0.0;
-        int cs = -1, lastc = -1;
-        for (int c = 0; c < C; ++c) {
-          double wc = (rp[c].m == -INFINITY) ? 0.0 : rp[c].s * static_cast<double>(expf((rp[c].m - M) * invT));
+      const ff target = ff_mul(W, u);
+      ff cum = ff_make(0.f), bs = ff_make(0.f);
+      int cs = -1, lastc = -1;
+      for (int c = 0; c < C; ++c) {
+        ff wc = s_tile[c];
+        if (!residual)
           for (int r = 0; r < nrej; ++r)
-            if (s_rej[r] / kVocabChunk == c) wc -= static_cast<double>(w_target(s_rej[r]));
-          if (wc > 0.0) lastc = c;
-          if (cs < 0 && cum + wc > target) {
-            cs = c;
-            bs = cum;
-          }
-          cum += wc;
+            if (s_rej[r] / kVocabChunk == c) wc = ff_sub(wc, ff_make(s_rejw[r]));
+        if (wc.hi > 0.f) lastc = c;
+        const ff nc = ff_add(cum, wc);
+        if (cs < 0 && ff_gt(nc, target)) {
+          cs = c;
+          bs = cum;
         }
-        s_fallback = cs < 0;  // nothing crosses (rounding): take the last positive weight
-        if (cs < 0) cs = lastc < 0 ? 0 : lastc;
-        s_chunk = cs;
-        s_base = bs;
-        s_W = W;
+        cum = nc;
       }
-      __syncthreads();
-      const int lo = s_chunk * kVocabChunk;
-      const double W = s_W, target = s_fallback ? INFINITY : u * W;
+      s_fallback = cs < 0;  // nothing crosses (rounding): take the last positive weight
+      if (cs < 0) cs = lastc < 0 ? 0 : lastc;
+      s_chunk = cs;
+      s_base = bs;
+      s_W = W;
+    }
+    __syncthreads();
+    const int lo = s_chunk * kVocabChunk;
+    const ff W = s_W;
+    const ff target = s_fallback ? ff{INFINITY, 0.f} : ff_mul(W, u);
+    if (residual)
+      block_draw_tile(lo, min(V, lo + kVocabChunk), s_base, target, wres, ds);
+    else
       block_draw_tile(lo, min(V, lo + kVocabChunk), s_base, target, w_of, ds);
-      if (threadIdx.x == 0) {
-        int emit = ds.found;
-        if (emit == INT_MAX) {
-          emit = ds.last < 0 ? lo : ds.last;
-          s_near = 1;
-        } else if (target - ds.prev_edge < kIcdfNearEps * W || ds.next_edge - target < kIcdfNearEps * W) {
-          s_near = 1;
-        }
-        s_emit = emit;
+    if (threadIdx.x == 0) {
+      int emit = ds.found;
+      const float win = kIcdfNearEps * ff_float(W);
+      if (emit == INT_MAX) {
+        emit = ds.last < 0 ? lo : ds.last;
+        s_near = 1;
+      } else if (ff_float(ff_sub(target, ds.prev_edge)) < win || ff_float(ff_sub(ds.next_edge, target)) < win) {
+        s_near = 1;
       }
+      s_emit = emit;
     }
     __syncthreads();
     break;
@@ -497,7 +624,7 @@ __global__ void __launch_bounds__(kThreads) accept_walk_kernel(const AcceptPlan 
     int32_t* ob = a.out.out_tok + static_cast<size_t>(b) * maxp;
     for (int j = 0; j < maxp; ++j) {
       pb[j] = j < len ? s_path[j] : -1;
-      ob[j] = j < na ? tok[s_path[j + 1]] : (j == na ? s_emit : -1);
+      ob[j] = j < na ? s_tokr[s_path[j + 1]] : (j == na ? s_emit : -1);
     }
     a.out.n_acc[b] = na;
     a.out.near_tie[b] = s_near;

@@ -61,6 +61,68 @@ struct CSum {
   __device__ __forceinline__ double total() const { return static_cast<double>(s) + static_cast<double>(c); }
 };
 
+// ------------------------------------------------------------------ float-float
+// A value held as an unevaluated sum hi + lo of two floats (|lo| <= ulp(hi) / 2), about
+// 48 significant bits, computed with error-free transformations (Knuth's TwoSum, and
+// a product whose rounding error an fma recovers) on the fp32 pipe.  Used instead of
+// double where sums must stay far below 1e-7 of the total: this GPU's fp64 pipe is
+// narrow, while these operations are a handful of fp32 instructions.
+struct ff {
+  float hi, lo;
+};
+
+__device__ __forceinline__ ff ff_make(float a) { return ff{a, 0.f}; }
+
+// a + b exactly as s + e (any magnitudes).
+__device__ __forceinline__ ff two_sum(float a, float b) {
+  const float s = a + b;
+  const float bb = s - a;
+  const float e = (a - (s - bb)) + (b - bb);
+  return ff{s, e};
+}
+
+// a + b exactly as s + e, given |a| >= |b| (or a == 0).
+__device__ __forceinline__ ff fast_two_sum(float a, float b) {
+  const float s = a + b;
+  return ff{s, b - (s - a)};
+}
+
+__device__ __forceinline__ ff ff_add(ff a, ff b) {
+  const ff s = two_sum(a.hi, b.hi);
+  return fast_two_sum(s.hi, s.lo + (a.lo + b.lo));
+}
+
+__device__ __forceinline__ ff ff_add(ff a, float b) {
+  const ff s = two_sum(a.hi, b);
+  return fast_two_sum(s.hi, s.lo + a.lo);
+}
+
+__device__ __forceinline__ ff ff_neg(ff a) { return ff{-a.hi, -a.lo}; }
+__device__ __forceinline__ ff ff_sub(ff a, ff b) { return ff_add(a, ff_neg(b)); }
+
+// a * b for a float b.
+__device__ __forceinline__ ff ff_mul(ff a, float b) {
+  const float p = a.hi * b;
+  float e = fmaf(a.hi, b, -p);
+  e = fmaf(a.lo, b, e);
+  return fast_two_sum(p, e);
+}
+
+__device__ __forceinline__ bool ff_gt(ff a, ff b) { return a.hi > b.hi || (a.hi == b.hi && a.lo > b.lo); }
+__device__ __forceinline__ float ff_float(ff a) { return a.hi + a.lo; }
+
+__device__ __forceinline__ ff ff_shfl_xor(ff v, int o) {
+  return ff{__shfl_xor_sync(0xffffffffu, v.hi, o), __shfl_xor_sync(0xffffffffu, v.lo, o)};
+}
+__device__ __forceinline__ ff warp_sum_ff(ff v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = ff_add(v, ff_shfl_xor(v, o));
+  return v;
+}
+
+// A compensated fp32 sum as a float-float value.
+__device__ __forceinline__ ff csum_ff(const CSum& a) { return two_sum(a.s, a.c); }
+
 // (value desc, index asc) order: true if (va, ia) comes before (vb, ib).
 __device__ __forceinline__ bool before(float va, int ia, float vb, int ib) {
   return va > vb || (va == vb && ia < ib);
