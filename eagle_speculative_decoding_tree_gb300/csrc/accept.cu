@@ -112,7 +112,7 @@ __device__ __forceinline__ void load_chunk(const void* base, size_t off, int lo,
   }
 }
 
-__global__ void __launch_bounds__(kThreads) accept_rowstats_kernel(const AcceptPlan p, const void* target,
+__global__ void __launch_bounds__(kThreads, 4) accept_rowstats_kernel(const AcceptPlan p, const void* target,
                                                                    const void* draft, RowPart* part) {
   const int row = blockIdx.x, c = blockIdx.y, src = blockIdx.z;
   const int rows = gridDim.x, n_chunks = gridDim.y;
@@ -189,22 +189,33 @@ __device__ __forceinline__ ff ff_shfl_up(ff v, int o) {
   return ff{__shfl_up_sync(0xffffffffu, v.hi, o), __shfl_up_sync(0xffffffffu, v.lo, o)};
 }
 
-// One tile of an inverse-CDF draw: elements [lo, hi) (hi - lo <= 4096), running mass
-// `base` before lo.  Each thread takes 16 consecutive elements; its running sum and
-// the thread offsets are float-float.  Sets ds.found to the first index whose running
-// mass exceeds `target` (INT_MAX if none), ds.last to the last index with positive
-// weight (-1 if none) and ds.total to the tile's mass.
-template <class WF>
-__device__ void block_draw_tile(int lo, int hi, ff base, ff target, WF wf, DrawScratch& ds) {
+// One tile of an inverse-CDF draw: elements [lo, hi) (lo < hi <= lo + 4096), running
+// mass `base` before lo.  Each thread takes 16 consecutive elements: ld(v) fetches an
+// element's raw values (all 16 requested before any is used), wt(v, raw) gives its
+// weight.  Its running sum and the thread offsets are float-float.  Sets ds.found to
+// the first index whose running mass exceeds `target` (INT_MAX if none), ds.last to the
+// last index with positive weight (-1 if none) and ds.total to the tile's mass.
+// The n_ex indices in ex[] (shared memory) get weight 0.
+template <class LD, class WT>
+__device__ void block_draw_tile(int lo, int hi, ff base, ff target, LD ld, WT wt, const int* ex, int n_ex,
+                                DrawScratch& ds) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int a0 = lo + threadIdx.x * kPer;
+  float2 raw[kPer];
+#pragma unroll
+  for (int e = 0; e < kPer; ++e) raw[e] = ld(min(a0 + e, hi - 1));
+  uint32_t exm = 0;  // excluded elements of this thread, one bit each
+  for (int r = 0; r < n_ex; ++r) {
+    const int d = ex[r] - a0;
+    if (d >= 0 && d < kPer) exm |= 1u << d;
+  }
   float w[kPer];
   ff my = ff_make(0.f);
   int last = -1;
 #pragma unroll
   for (int e = 0; e < kPer; ++e) {
     const int v = a0 + e;
-    w[e] = (v < hi) ? wf(v) : 0.f;
+    w[e] = (v < hi && !((exm >> e) & 1u)) ? wt(v, raw[e]) : 0.f;
     my = ff_add(my, w[e]);
     if (w[e] > 0.f) last = v;
   }
@@ -337,7 +348,7 @@ __device__ RowStats merge_row_stats(const RowPart* rp, int C, float invT, ff* ti
   return st;
 }
 
-__global__ void __launch_bounds__(kThreads) accept_walk_kernel(const AcceptPlan p, const WalkArgs a) {
+__global__ void __launch_bounds__(kThreads, 1) accept_walk_kernel(const AcceptPlan p, const WalkArgs a) {
   const int b = blockIdx.x;
   const int R = p.R, V = p.V, C = p.n_chunks;
   const bool greedy = !(p.temperature > 0.f);
@@ -468,7 +479,7 @@ __global__ void __launch_bounds__(kThreads) accept_walk_kernel(const AcceptPlan 
     } else if (!sampled) {
       // point-mass proposals: p_res(d) = p(d) / (1 - mass of the rejected tokens)
       if (threadIdx.x == 0) {
-        const float Zt = ff_float(s_Zt);
+        const float invZ = 1.f / ff_float(s_Zt);
         ff rejmass = ff_make(0.f);
         for (int i = 0; i < s_nk; ++i) {
           const int c = s_kids[i];
@@ -479,9 +490,9 @@ __global__ void __launch_bounds__(kThreads) accept_walk_kernel(const AcceptPlan 
           }
           bool dup = false;
           for (int r = 0; r < s_nrej; ++r) dup |= (s_rej[r] == d);
-          const float pd = dup ? 0.f : s_wk[i] / Zt;
+          const float pd = dup ? 0.f : s_wk[i] * invZ;
           const float denom = ff_float(ff_sub(ff_make(1.f), rejmass));
-          const float ratio = denom > 0.f ? pd / denom : 0.f;
+          const float ratio = denom > 0.f ? __fdividef(pd, denom) : 0.f;
           const float u = s_uk[i];
           if (fabsf(u - ratio) < kNearTieEps) s_near = 1;
           if (u < ratio) {
@@ -550,57 +561,87 @@ __global__ void __launch_bounds__(kThreads) accept_walk_kernel(const AcceptPlan 
     const bool residual = sampled && s_nz > 0;
     const int nz = s_nz, nrej = s_nrej;
     auto wres = [&](int v) { return pres_of(v, nz); };
-    auto w_of = [&](int v) {  // p with the rejected point-mass tokens zeroed
-      for (int r = 0; r < nrej; ++r)
-        if (s_rej[r] == v) return 0.f;
-      return w_target(v);
-    };
     if (residual) {
       const int n_tiles = (V + kVocabChunk - 1) / kVocabChunk;
       for (int t = 0; t < n_tiles; ++t) {
         const ff m = block_sum(t * kVocabChunk, min(V, (t + 1) * kVocabChunk), wres, red);
         if (threadIdx.x == 0) s_tile[t] = m;
       }
+    } else {
+      // the row's chunk masses less the rejected point-mass tokens
+      for (int c = threadIdx.x; c < C; c += kThreads) {
+        ff wc = s_tile[c];
+        for (int r = 0; r < nrej; ++r)
+          if (s_rej[r] / kVocabChunk == c) wc = ff_sub(wc, ff_make(s_rejw[r]));
+        s_tile[c] = wc;
+      }
     }
-    if (threadIdx.x == 0) {
-      // tile masses: the residual's, or the row's chunk masses less the rejected tokens
+    __syncthreads();
+    if (warp == 0) {
+      // total mass W, then the first tile whose running mass exceeds u W: an inclusive
+      // float-float scan over 32 tiles at a time, the crossing found by ballot
       ff W = ff_make(0.f);
       if (residual) {
-        for (int t = 0; t < C; ++t) W = ff_add(W, s_tile[t]);
+        for (int c = lane; c < C; c += 32) W = ff_add(W, s_tile[c]);
+        W = warp_sum_ff(W);
       } else {
         W = s_Zt;
         for (int r = 0; r < nrej; ++r) W = ff_sub(W, ff_make(s_rejw[r]));
       }
       const ff target = ff_mul(W, u);
-      ff cum = ff_make(0.f), bs = ff_make(0.f);
+      ff carry = ff_make(0.f), bs = ff_make(0.f);
       int cs = -1, lastc = -1;
-      for (int c = 0; c < C; ++c) {
-        ff wc = s_tile[c];
-        if (!residual)
-          for (int r = 0; r < nrej; ++r)
-            if (s_rej[r] / kVocabChunk == c) wc = ff_sub(wc, ff_make(s_rejw[r]));
-        if (wc.hi > 0.f) lastc = c;
-        const ff nc = ff_add(cum, wc);
-        if (cs < 0 && ff_gt(nc, target)) {
-          cs = c;
-          bs = cum;
+      for (int c0 = 0; c0 < C; c0 += 32) {
+        const int c = c0 + lane;
+        const ff wc = c < C ? s_tile[c] : ff_make(0.f);
+        ff incl = wc;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const ff t = ff_shfl_up(incl, o);
+          if (lane >= o) incl = ff_add(incl, t);
         }
-        cum = nc;
+        const ff cum = ff_add(carry, incl);
+        const unsigned pos = __ballot_sync(0xffffffffu, c < C && wc.hi > 0.f);
+        if (pos) lastc = c0 + 31 - __clz(pos);
+        const unsigned cross = __ballot_sync(0xffffffffu, c < C && ff_gt(cum, target));
+        const ff excl = ff_sub(cum, wc);
+        if (cs < 0 && cross) {
+          const int l = __ffs(cross) - 1;
+          cs = c0 + l;
+          bs = ff{__shfl_sync(0xffffffffu, excl.hi, l), __shfl_sync(0xffffffffu, excl.lo, l)};
+        }
+        carry = ff_add(carry, ff{__shfl_sync(0xffffffffu, incl.hi, 31), __shfl_sync(0xffffffffu, incl.lo, 31)});
       }
-      s_fallback = cs < 0;  // nothing crosses (rounding): take the last positive weight
-      if (cs < 0) cs = lastc < 0 ? 0 : lastc;
-      s_chunk = cs;
-      s_base = bs;
-      s_W = W;
+      if (lane == 0) {
+        s_fallback = cs < 0;  // nothing crosses (rounding): take the last positive weight
+        s_chunk = cs < 0 ? (lastc < 0 ? 0 : lastc) : cs;
+        s_base = bs;
+        s_W = W;
+      }
     }
     __syncthreads();
     const int lo = s_chunk * kVocabChunk;
     const ff W = s_W;
     const ff target = s_fallback ? ff{INFINITY, 0.f} : ff_mul(W, u);
-    if (residual)
-      block_draw_tile(lo, min(V, lo + kVocabChunk), s_base, target, wres, ds);
-    else
-      block_draw_tile(lo, min(V, lo + kVocabChunk), s_base, target, w_of, ds);
+    if (residual) {
+      block_draw_tile(
+          lo, min(V, lo + kVocabChunk), s_base, target,
+          [&](int v) {
+            return make_float2(load_elem(a.target, xrow + v, p.dtype), load_elem(a.draft, xrow + v, p.dtype));
+          },
+          [&](int v, float2 x) {
+            float pv = expf((x.x - M) * invT) * invZt;
+            const float qv = expf((x.y - Mq) * invT) * invZq;
+            for (int i = 0; i < nz; ++i) pv = fmaxf(pv - qv, 0.f) / s_Z[i];
+            return pv;
+          },
+          s_rej, 0, ds);
+    } else {
+      block_draw_tile(
+          lo, min(V, lo + kVocabChunk), s_base, target,
+          [&](int v) { return make_float2(load_elem(a.target, xrow + v, p.dtype), 0.f); },
+          [&](int, float2 x) { return expf((x.x - M) * invT); }, s_rej, nrej, ds);
+    }
     if (threadIdx.x == 0) {
       int emit = ds.found;
       const float win = kIcdfNearEps * ff_float(W);
