@@ -535,7 +535,7 @@ void plan_tree_attn(const eagle_attn_desc* d, int num_sms, AttnPlan* p) {
   p->tc = d->engine == EAGLE_ENGINE_AUTO && p->D == 128 && (128 % p->G) == 0;
   int key_tile, slots_per_sm;
   if (p->tc) {
-    p->rows_per_cta = (RG <= 128) ? 128 : 256;
+    p->rows_per_cta = 128;  // one M-tile: TMEM holds two S buffers and O
     key_tile = 128;
     slots_per_sm = 1;  // one CTA per SM: it holds all 512 TMEM columns
   } else {

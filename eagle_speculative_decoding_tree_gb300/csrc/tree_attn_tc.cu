@@ -5,21 +5,21 @@
 // of a request attends to the prefix keys j < seq_len and to the tree keys whose bit
 // is set in its ancestor words.
 //
-// One CTA per (request, KV head, split, row block), 320 threads, warp-specialised:
-//   warp 8        TMA producer: Q once (one box per 128-row M-tile and 64-dim half),
-//                 then K and V tiles of 128 keys through two-stage rings.
-//   warp 9        allocates all 512 TMEM columns; lane 0 issues tcgen05.mma:
-//                 S_i = Q_i K^T (Q, K K-major, 128-byte swizzle) and O_i += P_i V (P from
-//                 TMEM, V MN-major); the warp zeroes V rows past the last valid key so
-//                 that masked keys contribute exactly 0.
-//   warps 0-7     online softmax, all eight on one M-tile at a time: warp w takes
-//                 TMEM lane quarter w & 3 (32 rows) and key half w >> 2; the halves of
-//                 a row agree on its max through shared memory.  P = 2^((s - m) c) goes
-//                 back into the half's own S columns as packed bf16 (the PV A operand).
-//                 O is rescaled in TMEM only when the row max grows by more than 2^8.
-// MMA issue order QK0 QK1 | PV0 QK0' PV1 QK1' | ...: the tensor cores run M-tile 0's
-// PV and next QK while the warps do M-tile 1's softmax, and the other way round.
-// TMEM columns: S0 [0,128) S1 [128,256) O0 [256,384) O1 [384,512).
+// One CTA per (request, KV head, split, 128-row block), 320 threads, warp-specialised:
+//   warp 8        TMA producer: Q once (one box per 64-dim half: the G query heads of
+//                 128 / G nodes), then K and V tiles of 128 keys through two-stage rings.
+//   warp 9        allocates the TMEM columns and issues tcgen05.mma from lane 0:
+//                 S = Q K^T (Q, K K-major, 128-byte swizzle) into buffer t & 1, and
+//                 O += P V (P from TMEM, V MN-major), in the order QK0 QK1 | PV0 QK2 |
+//                 PV1 QK3 | ..., so the next-but-one S is computed while the softmax works
+//                 on this one; the warp zeroes V rows past the last valid key so that
+//                 masked keys contribute exactly 0.
+//   warps 0-7     online softmax: warp w takes TMEM lane quarter w & 3 (32 rows) and key
+//                 half w >> 2; the halves of a row agree on its max through shared memory.
+//                 P = 2^((s - m) c) goes back into the half's own S columns as packed bf16
+//                 (the PV A operand).  O is rescaled in TMEM only when the row max grows
+//                 by more than 2^8, after the previous PV has finished.
+// TMEM columns: S0 [0,128) S1 [128,256) O [256,384).
 //
 // Splits: each CTA covers a contiguous range of key tiles (the tree tile counts as
 // one) and keeps unnormalised partials (O, m, l).  One split writes the output
@@ -51,12 +51,13 @@ constexpr int KT = 128;                   // keys per tile
 constexpr int HALF = 16384;               // one 64-dim half of a 128-row tile (bytes)
 constexpr int TILE = 2 * HALF;            // one K or V tile
 constexpr int NTHREADS = 320;
-constexpr int SM_Q = 0;                   // 2 M-tiles x 32 KB
-constexpr int SM_K = 2 * TILE;            // 2 stages
-constexpr int SM_V = 4 * TILE;            // 2 stages
-constexpr int SMEM_BYTES = 6 * TILE + 1024;
-__device__ __forceinline__ uint32_t col_s(int i) { return static_cast<uint32_t>(i) * 128u; }          // S_i / P_i
-__device__ __forceinline__ uint32_t col_o(int i) { return 256u + static_cast<uint32_t>(i) * 128u; }  // O_i
+constexpr int SM_Q = 0;                   // the 128-row M-tile, 32 KB
+constexpr int SM_K = TILE;                // 2 stages
+constexpr int SM_V = 3 * TILE;            // 2 stages
+constexpr int SMEM_BYTES = 5 * TILE + 1024;
+// TMEM columns: S / P of tile t in buffer t & 1, then the O accumulator
+__device__ __forceinline__ uint32_t col_s(int j) { return static_cast<uint32_t>(j) * 128u; }
+constexpr uint32_t COL_O = 256u;
 constexpr float kRescaleLog2 = 8.f;       // lazy rescale threshold (log2 units)
 constexpr int kMergeBatch = 20;           // group merge: splits whose rows are loaded at once
 
@@ -239,28 +240,28 @@ __device__ __forceinline__ float max64(const uint32_t (&a)[32], const uint32_t (
   return max3(max3(n[0], n[1], n[2]), max3(n[3], n[4], n[5]), n[6]);
 }
 
-template <bool PRECISE>
-__device__ __forceinline__ void issue_qk(uint32_t tb, const uint8_t* sQ, const uint8_t* sK, int i) {
+// S (TMEM columns scol) = Q K^T over the 8 K-steps of 16 head dims.
+__device__ __forceinline__ void issue_qk(uint32_t tb, const uint8_t* sQ, const uint8_t* sK, uint32_t scol) {
   constexpr uint32_t idesc = idesc_bf16_f32(128, KT, 0, 0);
 #pragma unroll
   for (int ks = 0; ks < 8; ++ks) {
     const uint32_t off = (ks >> 2) * HALF + (ks & 3) * 32;
-    mma_ss(tb + col_s(i), smem_desc_sw128(smem_u32(sQ + i * TILE) + off, 16, 1024),
-           smem_desc_sw128(smem_u32(sK) + off, 16, 1024), idesc, ks > 0);
+    mma_ss(tb + scol, smem_desc_sw128(smem_u32(sQ) + off, 16, 1024), smem_desc_sw128(smem_u32(sK) + off, 16, 1024),
+           idesc, ks > 0);
   }
 }
 
-// O_i += P_i V over the 8 K-steps of 16 keys; the P of keys 64 h + 16 k .. sits in
-// S_i's columns 64 h + 8 k .. (the precise low parts 32 columns further on).
+// O += P V over the 8 K-steps of 16 keys; the P of keys 64 h + 16 k .. sits in columns
+// scol + 64 h + 8 k .. (the precise low parts 32 columns further on).
 template <bool PRECISE>
-__device__ __forceinline__ void issue_pv(uint32_t tb, const uint8_t* sV, int i, bool first) {
+__device__ __forceinline__ void issue_pv(uint32_t tb, const uint8_t* sV, uint32_t scol, bool first) {
   constexpr uint32_t idesc = idesc_bf16_f32(128, 128, 0, 1);
 #pragma unroll
   for (int ks = 0; ks < 8; ++ks) {
     const uint64_t bd = smem_desc_sw128(smem_u32(sV) + ks * 2048, HALF, 1024);
-    const uint32_t acol = col_s(i) + (ks >> 2) * 64 + (ks & 3) * 8;
-    mma_ts(tb + col_o(i), tb + acol, bd, idesc, (first && ks == 0) ? 0u : 1u);
-    if constexpr (PRECISE) mma_ts(tb + col_o(i), tb + acol + 32, bd, idesc, 1u);
+    const uint32_t acol = scol + (ks >> 2) * 64 + (ks & 3) * 8;
+    mma_ts(tb + COL_O, tb + acol, bd, idesc, (first && ks == 0) ? 0u : 1u);
+    if constexpr (PRECISE) mma_ts(tb + COL_O, tb + acol + 32, bd, idesc, 1u);
   }
 }
 
@@ -269,7 +270,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     tree_attn_tc_kernel(const __grid_constant__ Tmaps tm, const TcArgs a) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  __shared__ uint64_t bar_q, k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[2], p_full[2], o_full;
+  __shared__ uint64_t bar_q, k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[2], p_full[2], o_done, o_full;
   __shared__ uint32_t tmem_base;
   __shared__ int s_abort;
   __shared__ float s_red[2][2][2][128];  // [tile parity][M-tile][key half][row] half-row maxima
@@ -292,6 +293,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       mbar_init(&s_full[s], 1);
       mbar_init(&p_full[s], 256);
     }
+    mbar_init(&o_done, 1);
     mbar_init(&o_full, 1);
     s_abort = 0;
     fence_barrier_init();
@@ -336,21 +338,21 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     }
   } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
+    // S of tile t goes to TMEM buffer t & 1: QK(0) QK(1) | PV(0) QK(2) | PV(1) QK(3) | ...
+    // so the tensor cores compute the next-but-one S while the softmax works on this one.
     bool ok = ti.n_tiles > 0;
     if (ok && lane == 0) ok = wait_parity(&bar_q, 0, a.err, ERR_Q);
     ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-    auto qk = [&](int t) {  // both M-tiles of tile t; lane 0
+    auto qk = [&](int t) {  // lane 0; K stage and S buffer t & 1
       const int s = t & 1;
       if (!wait_parity(&k_full[s], (t >> 1) & 1, a.err, ERR_KFULL)) return false;
       tc_fence_after();
-      for (int i = 0; i < n_mt; ++i) {
-        issue_qk<PRECISE>(tb, sQ, smem + SM_K + s * TILE, i);
-        mma_commit(&s_full[i]);
-      }
+      issue_qk(tb, sQ, smem + SM_K + s * TILE, col_s(s));
+      mma_commit(&s_full[s]);
       mma_commit(&k_empty[s]);
       return true;
     };
-    if (ok && lane == 0) ok = qk(0);
+    if (ok && lane == 0) ok = qk(0) && (ti.n_tiles < 2 || qk(1));
     ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
     for (int t = 0; t < ti.n_tiles && ok; ++t) {
       const int s = t & 1;
@@ -369,34 +371,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       }
       __syncwarp();
       if (lane == 0) {
-        uint8_t* sv = smem + SM_V + s * TILE;
-        for (int i = 0; i < n_mt && ok; ++i) {
-          ok = wait_parity(&p_full[i], t & 1, a.err, ERR_P);
-          if (!ok) break;
-          tc_fence_after();
-          issue_pv<PRECISE>(tb, sv, i, t == 0);
-          if (i == 0 && t + 1 < ti.n_tiles) {
-            // next tile's S0 as soon as PV0 is queued (tensor core stays busy while
-            // warpgroup 1 finishes its softmax)
-            const int s1 = (t + 1) & 1;
-            if (!wait_parity(&k_full[s1], ((t + 1) >> 1) & 1, a.err, ERR_KFULL)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-            issue_qk<PRECISE>(tb, sQ, smem + SM_K + s1 * TILE, 0);
-            mma_commit(&s_full[0]);
-            if (n_mt == 1) mma_commit(&k_empty[s1]);
-          }
-        }
+        ok = wait_parity(&p_full[s], (t >> 1) & 1, a.err, ERR_P);
         if (ok) {
+          tc_fence_after();
+          issue_pv<PRECISE>(tb, smem + SM_V + s * TILE, col_s(s), t == 0);
           mma_commit(&v_empty[s]);
-          if (n_mt == 2 && t + 1 < ti.n_tiles) {
-            const int s1 = (t + 1) & 1;
-            issue_qk<PRECISE>(tb, sQ, smem + SM_K + s1 * TILE, 1);
-            mma_commit(&s_full[1]);
-            mma_commit(&k_empty[s1]);
-          }
+          mma_commit(&o_done);
+          if (t + 2 < ti.n_tiles) ok = qk(t + 2);
         }
       }
       ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
@@ -440,7 +421,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 #pragma unroll
       for (int i = 0; i < 2; ++i) {
         if (i >= n_mt) break;
-        const bool got = __all_sync(0xffffffffu, wait_parity(&s_full[i], t & 1, a.err, ERR_S));
+        const bool got = __all_sync(0xffffffffu, wait_parity(&s_full[t & 1], (t >> 1) & 1, a.err, ERR_S));
         tc_fence_after();
         // pass 1: max of this half's 64 scores over the kept keys
         const uint32_t k0 = !vrow[i] ? 0u : (tree ? tw[i][0] : low_bits(nv - 64 * hf));
@@ -449,8 +430,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         float mx = -INFINITY;
         if (got) {
           uint32_t s0[32], s1[32];
-          tmem_ld32(lb + col_s(i) + 64 * hf, s0);
-          tmem_ld32(lb + col_s(i) + 64 * hf + 32, s1);
+          tmem_ld32(lb + col_s(t & 1) + 64 * hf, s0);
+          tmem_ld32(lb + col_s(t & 1) + 64 * hf + 32, s1);
           tmem_ld_wait();
           if (!full) {
             mask_keys(s0, k0);
@@ -472,15 +453,22 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const bool scale_o = move && m_ref[i] != -INFINITY;
         const float alpha = scale_o ? ex2((m_ref[i] - m_new) * sl2) : 1.f;
         if (__any_sync(0xffffffffu, scale_o)) {
+          // O must hold every earlier tile: wait for PV(t - 1) (PV(t - 2) finished
+          // before S of tile t did).  A timeout only records ERR_O: leaving the loop here
+          // would desert the named barriers the other softmax warps wait on.
+          __syncwarp();
+          (void)wait_parity(&o_done, (t - 1) & 1, a.err, ERR_O);
+          __syncwarp();
+          tc_fence_after();
           l[i] *= alpha;
 #pragma unroll
           for (int c = 0; c < 2; ++c) {
             uint32_t o[32];
-            tmem_ld32(lb + col_o(i) + 64 * hf + 32 * c, o);
+            tmem_ld32(lb + COL_O + 64 * hf + 32 * c, o);
             tmem_ld_wait();
 #pragma unroll
             for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha);
-            tmem_st32(lb + col_o(i) + 64 * hf + 32 * c, o);
+            tmem_st32(lb + COL_O + 64 * hf + 32 * c, o);
           }
           tmem_st_wait();
         }
@@ -508,7 +496,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
               hi[j] = *reinterpret_cast<uint32_t*>(&u);
               ls2[j & 1] = add_f32x2(ls2[j & 1], f32x2(__float_as_uint(p0), __float_as_uint(p1)));
             }
-            tmem_st16(lb + col_s(i) + 64 * hf + 16 * c, hi);
+            tmem_st16(lb + col_s(t & 1) + 64 * hf + 16 * c, hi);
           } else {
             // P = hi + lo, both bf16; the low parts go 32 columns after the high ones
             uint32_t lo[16];
@@ -523,14 +511,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
               lo[j] = *reinterpret_cast<uint32_t*>(&w);
               ls[j & 3] += (h0 + __uint_as_float(lo[j] << 16)) + (h1 + __uint_as_float(lo[j] & 0xffff0000u));
             }
-            tmem_st16(lb + col_s(i) + 64 * hf + 16 * c, hi);
-            tmem_st16(lb + col_s(i) + 64 * hf + 32 + 16 * c, lo);
+            tmem_st16(lb + col_s(t & 1) + 64 * hf + 16 * c, hi);
+            tmem_st16(lb + col_s(t & 1) + 64 * hf + 32 + 16 * c, lo);
           }
         };
         {
           uint32_t s0[32], s1[32];
-          tmem_ld32(lb + col_s(i) + 64 * hf, s0);
-          tmem_ld32(lb + col_s(i) + 64 * hf + 32, s1);
+          tmem_ld32(lb + col_s(t & 1) + 64 * hf, s0);
+          tmem_ld32(lb + col_s(t & 1) + 64 * hf + 32, s1);
           tmem_ld_wait();
           if (!full) {
             mask_keys(s0, k0);
@@ -549,7 +537,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
         tmem_st_wait();
         tc_fence_before();
-        mbar_arrive(&p_full[i]);
+        mbar_arrive(&p_full[t & 1]);
       }
     }
     // ---- epilogue: O from TMEM to the output (one split) or the partials
@@ -574,8 +562,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         uint8_t* so = smem + SM_K + i * 4 * HALF;
         if (a.part_bf16) {
           uint32_t o0[32], o1[32];
-          tmem_ld32(lb + col_o(i) + 64 * hf, o0);
-          tmem_ld32(lb + col_o(i) + 64 * hf + 32, o1);
+          tmem_ld32(lb + COL_O + 64 * hf, o0);
+          tmem_ld32(lb + COL_O + 64 * hf + 32, o1);
           tmem_ld_wait();
           uint8_t* dst = so + hf * HALF + r_local * 128;
 #pragma unroll
@@ -595,7 +583,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           for (int cc = 0; cc < 2; ++cc) {
             const int c = 2 * hf + cc;
             uint32_t o[32];
-            tmem_ld32(lb + col_o(i) + 32 * c, o);
+            tmem_ld32(lb + COL_O + 32 * c, o);
             tmem_ld_wait();
             uint8_t* dst = so + c * HALF + r_local * 128;
 #pragma unroll
@@ -639,7 +627,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           const int c = 2 * hf + cc;
           uint32_t o[32];
           if (all_done) {
-            tmem_ld32(lb + col_o(i) + 32 * c, o);
+            tmem_ld32(lb + COL_O + 32 * c, o);
             tmem_ld_wait();
           } else {
 #pragma unroll
