@@ -59,7 +59,6 @@ constexpr int SMEM_BYTES = 5 * TILE + 1024;
 __device__ __forceinline__ uint32_t col_s(int j) { return static_cast<uint32_t>(j) * 128u; }
 constexpr uint32_t COL_O = 256u;
 constexpr float kRescaleLog2 = 8.f;       // lazy rescale threshold (log2 units)
-constexpr int kMergeBatch = 20;           // group merge: splits whose rows are loaded at once
 
 enum : int { ERR_Q = 1, ERR_KFULL = 2, ERR_KEMPTY = 4, ERR_VFULL = 8, ERR_VEMPTY = 16, ERR_S = 32, ERR_P = 64, ERR_O = 128,
              ERR_GROUP = 256 };
@@ -116,82 +115,111 @@ __device__ __forceinline__ int tile_valid(const TcArgs& a, const TileInfo& ti, i
   return a.R;
 }
 
-// Partial-O row `prow`, columns 4 lane .. 4 lane + 3, through L2: raw bf16 (uint2) or
-// fp32 (float4) words, converted only where they are used.
-template <bool BF16>
-struct PartWords {
-  using T = typename std::conditional<BF16, uint2, float4>::type;
-  static __device__ __forceinline__ T load(const TcArgs& a, size_t prow, int lane) {
-    if constexpr (BF16)
-      return __ldcg(reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(a.part_o) + prow * 128) + lane);
-    else
-      return __ldcg(reinterpret_cast<const float4*>(static_cast<const float*>(a.part_o) + prow * 128) + lane);
-  }
-  static __device__ __forceinline__ float4 f32(const T& w) {
-    if constexpr (BF16)
-      return make_float4(__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xffff0000u), __uint_as_float(w.y << 16),
-                         __uint_as_float(w.y & 0xffff0000u));
-    else
-      return w;
-  }
-};
+// Merge of one output row from the group's split partials, by a half-warp (16 lanes,
+// `hl` = lane within the half; every shuffle stays inside the half): lane s holds
+// split s's (m, l) (splits beyond 16 in further rounds), M = max m_s,
+// w_s = 2^((m_s - M) c), L = sum w_s l_s, O = sum w_s O_s / L.  Lane hl owns columns
+// 8 hl .. 8 hl + 7.  The partial rows of up to kMergeBatch splits are requested before
+// any is used (split indices past the last are clamped; their weight is 0), so a row
+// costs about one L2 round trip.  grow < 0: nothing to write (the loads stay in bounds).
+constexpr int kMergeBatch = 16;
 
-// Merge of one output row from the group's split partials, by one warp: lane s holds
-// split s's (m, l) (two per lane), M = max m_s, w_s = 2^((m_s - M) c), L = sum w_s l_s,
-// O = sum w_s O_s / L.  The first kMergeBatch partial rows are requested before any
-// is used (split indices past the last are clamped; their weight is 0), so the row
-// costs about one L2 round trip.
+__device__ __forceinline__ void load_part8(const TcArgs& a, size_t prow, int hl, bool bf16, uint4 (&w)[2]) {
+  if (bf16) {
+    w[0] = __ldcg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.part_o) + prow * 128) + hl);
+  } else {
+    const uint4* src = reinterpret_cast<const uint4*>(static_cast<const float*>(a.part_o) + prow * 128) + 2 * hl;
+    w[0] = __ldcg(src);
+    w[1] = __ldcg(src + 1);
+  }
+}
+
+__device__ __forceinline__ void part8_f32(const uint4 (&w)[2], bool bf16, float (&x)[8]) {
+  if (bf16) {
+    const uint32_t u[4] = {w[0].x, w[0].y, w[0].z, w[0].w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      x[2 * k] = __uint_as_float(u[k] << 16);
+      x[2 * k + 1] = __uint_as_float(u[k] & 0xffff0000u);
+    }
+  } else {
+    x[0] = __uint_as_float(w[0].x);
+    x[1] = __uint_as_float(w[0].y);
+    x[2] = __uint_as_float(w[0].z);
+    x[3] = __uint_as_float(w[0].w);
+    x[4] = __uint_as_float(w[1].x);
+    x[5] = __uint_as_float(w[1].y);
+    x[6] = __uint_as_float(w[1].z);
+    x[7] = __uint_as_float(w[1].w);
+  }
+}
+
 template <bool BF16>
-__device__ __forceinline__ void merge_row(const TcArgs& a, int bh, int h, int b, int grow, int lane, float sl2) {
-  using PW = PartWords<BF16>;
-  const size_t base = static_cast<size_t>(bh) * a.splits * a.rows_pad + grow;
+__device__ __forceinline__ void merge_row_hw(const TcArgs& a, int bh, int h, int b, int grow, int hl, float sl2) {
+  const unsigned full = 0xffffffffu;
+  const size_t base = static_cast<size_t>(bh) * a.splits * a.rows_pad + max(grow, 0);
   const size_t sstride = a.rows_pad;
-  typename PW::T v[kMergeBatch];
+  constexpr int NB = BF16 ? kMergeBatch : kMergeBatch / 2;  // fp32 rows take two words per lane
+  uint4 v[NB][2];
 #pragma unroll
-  for (int u = 0; u < kMergeBatch; ++u) v[u] = PW::load(a, base + min(u, a.splits - 1) * sstride, lane);
-  float2 ml[2];
+  for (int u = 0; u < NB; ++u) load_part8(a, base + min(u, a.splits - 1) * sstride, hl, BF16, v[u]);
+  float2 ml[4];
 #pragma unroll
-  for (int k = 0; k < 2; ++k) {
-    const int sp = lane + 32 * k;
+  for (int k = 0; k < 4; ++k) {
+    const int sp = hl + 16 * k;
     ml[k] = sp < a.splits ? __ldcg(reinterpret_cast<const float2*>(a.part_ml + (base + sp * sstride) * 2))
                           : make_float2(-INFINITY, 0.f);
   }
-  const float M = warp_max(fmaxf(ml[0].x, ml[1].x));
-  float w2[2];
+  float M = fmaxf(fmaxf(ml[0].x, ml[1].x), fmaxf(ml[2].x, ml[3].x));
 #pragma unroll
-  for (int k = 0; k < 2; ++k) w2[k] = (ml[k].x == -INFINITY) ? 0.f : ex2((ml[k].x - M) * sl2);
-  const float L = warp_sum(ml[0].y * w2[0] + ml[1].y * w2[1]);
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int o = 8; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(full, M, o, 16));
+  float w4[4], L = 0.f;
 #pragma unroll
-  for (int u = 0; u < kMergeBatch; ++u) {
-    const float ws = __shfl_sync(0xffffffffu, w2[0], u);  // 0 for u >= splits
-    const float4 x = PW::f32(v[u]);
-    acc.x = fmaf(ws, x.x, acc.x);
-    acc.y = fmaf(ws, x.y, acc.y);
-    acc.z = fmaf(ws, x.z, acc.z);
-    acc.w = fmaf(ws, x.w, acc.w);
+  for (int k = 0; k < 4; ++k) {
+    w4[k] = (ml[k].x == -INFINITY) ? 0.f : ex2((ml[k].x - M) * sl2);
+    L += ml[k].y * w4[k];
   }
-  for (int sp = kMergeBatch; sp < a.splits; ++sp) {  // more splits than one batch
-    const float ws = __shfl_sync(0xffffffffu, sp < 32 ? w2[0] : w2[1], sp & 31);
-    const float4 x = PW::f32(PW::load(a, base + sp * sstride, lane));
-    acc.x = fmaf(ws, x.x, acc.x);
-    acc.y = fmaf(ws, x.y, acc.y);
-    acc.z = fmaf(ws, x.z, acc.z);
-    acc.w = fmaf(ws, x.w, acc.w);
+#pragma unroll
+  for (int o = 8; o > 0; o >>= 1) L += __shfl_xor_sync(full, L, o, 16);
+  float acc[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+#pragma unroll
+  for (int u = 0; u < NB; ++u) {
+    const float ws = __shfl_sync(full, w4[0], u, 16);  // 0 for u >= splits
+    float x[8];
+    part8_f32(v[u], BF16, x);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) acc[e] = fmaf(ws, x[e], acc[e]);
   }
+  for (int sp = NB; sp < a.splits; ++sp) {  // more splits than one batch
+    const int k = sp >> 4;
+    const float ws = __shfl_sync(full, k == 0 ? w4[0] : (k == 1 ? w4[1] : (k == 2 ? w4[2] : w4[3])), sp & 15, 16);
+    uint4 t[2];
+    load_part8(a, base + sp * sstride, hl, BF16, t);
+    float x[8];
+    part8_f32(t, BF16, x);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) acc[e] = fmaf(ws, x[e], acc[e]);
+  }
+  if (grow < 0) return;
   const float inv = 1.f / L;
   const int node = grow / a.G, hq = h * a.G + grow % a.G;
-  const size_t orow = (static_cast<size_t>(b * a.R + node) * a.Hq + hq) * 128 + 4 * lane;
+  const size_t orow = (static_cast<size_t>(b * a.R + node) * a.Hq + hq) * 128 + 8 * hl;
   if (a.out_f32) {
-    *reinterpret_cast<float4*>(static_cast<float*>(a.out) + orow) =
-        make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+    float4* dst = reinterpret_cast<float4*>(static_cast<float*>(a.out) + orow);
+    dst[0] = make_float4(acc[0] * inv, acc[1] * inv, acc[2] * inv, acc[3] * inv);
+    dst[1] = make_float4(acc[4] * inv, acc[5] * inv, acc[6] * inv, acc[7] * inv);
   } else {
-    __nv_bfloat162 u0 = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
-    __nv_bfloat162 u1 = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
-    *reinterpret_cast<uint2*>(static_cast<uint16_t*>(a.out) + orow) =
-        make_uint2(*reinterpret_cast<uint32_t*>(&u0), *reinterpret_cast<uint32_t*>(&u1));
+    uint32_t wo[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      __nv_bfloat162 u2 = __floats2bfloat162_rn(acc[2 * k] * inv, acc[2 * k + 1] * inv);
+      wo[k] = *reinterpret_cast<uint32_t*>(&u2);
+    }
+    *reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.out) + orow) = make_uint4(wo[0], wo[1], wo[2], wo[3]);
   }
-  if (a.lse && lane == 0) a.lse[static_cast<size_t>(b * a.R + node) * a.Hq + hq] = a.scale * M + logf(L);
+  if (a.lse && hl == 0) a.lse[static_cast<size_t>(b * a.R + node) * a.Hq + hq] = a.scale * M + logf(L);
 }
 
 // Counts this split into its group and waits (at most 2 s, then ERR_GROUP) until all
@@ -702,11 +730,16 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       if (s_go) {
         const int n = min(a.rows_per_cta, a.R * a.G - rb * a.rows_per_cta);
         const int hi = (split + 1) * n / a.splits;
-        for (int lr = split * n / a.splits + warp; lr < hi; lr += 8) {
+        // a half-warp per row; both halves of a warp loop together (shuffles are
+        // warp-collective), the spare half on a row of its own block with no output
+        const int lo = split * n / a.splits;
+        for (int s0 = lo + 2 * warp; s0 < hi; s0 += 16) {
+          const int lr = s0 + (lane >> 4);
+          const int grow = lr < hi ? rb * a.rows_per_cta + lr : -1;
           if (a.part_bf16)
-            merge_row<true>(a, bh, h, b, rb * a.rows_per_cta + lr, lane, sl2);
+            merge_row_hw<true>(a, bh, h, b, grow < 0 ? -1 : grow, lane & 15, sl2);
           else
-            merge_row<false>(a, bh, h, b, rb * a.rows_per_cta + lr, lane, sl2);
+            merge_row_hw<false>(a, bh, h, b, grow < 0 ? -1 : grow, lane & 15, sl2);
         }
       }
     }
