@@ -15,6 +15,7 @@ struct StaticShape {
   int32_t rows;
   int8_t parent[128];
   int8_t depth[128];
+  uint8_t lrank[128];  // a node's rank among the nodes of its depth, in index order
 };
 
 struct TreeBuildPlan {

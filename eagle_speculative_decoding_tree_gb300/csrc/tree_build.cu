@@ -14,16 +14,19 @@
 // softmax(row / T) (non-greedy).
 //
 // Kernels
-//   tree_chunk_kernel   one CTA per (request x frontier row, 4096-token chunk):
-//                       chunk max, sum exp (T = 1 and T), and the chunk's top-16 by
-//                       (logit desc, id asc) -- one streaming pass over the logits.
+//   tree_chunk_kernel   one CTA per (request x frontier row, 4096-token chunk): the
+//                       chunk max, sum exp (T = 1 and T) and the chunk's top-16 by
+//                       (logit desc, id asc), from one read of the logits held in
+//                       registers (16 per thread).
 //   tree_select_kernel  one CTA per request: merges the chunk results per row,
 //                       extends the pool, picks the frontier (bitonic sort in shared
 //                       memory) and, at the last level, emits the tree arrays.
 //
-// Precision: chunk sums are compensated fp32, merged in double; cumulative scores
-// are kept in double so that fp32 and fp64 selections agree unless two scores at a
-// boundary are within 1e-5 (reported as a near-tie).
+// Precision: chunk sums are compensated fp32, merged as float-float (about 48
+// significant bits on the fp32 pipe; this GPU's fp64 pipe is narrow); ln Z is one
+// double log per row.  Cumulative scores are float-float, so that the selections
+// agree with an fp64 computation unless two scores at a boundary are within 1e-5
+// (reported as a near-tie).
 #include <limits.h>
 
 #include "common.cuh"
@@ -33,14 +36,17 @@ namespace eagle {
 namespace {
 
 constexpr int kThreads = 256;
+constexpr int NW = kThreads / 32;
 constexpr int K = kMaxTopK;
-constexpr double kIcdfNearEps = 1e-7;
+constexpr int kPer = kVocabChunk / kThreads;  // logits per thread in the chunk pass
+constexpr float kIcdfNearEps = 1e-7f;
+static_assert(kPer == K, "the chunk pass sorts one thread's logits as a K-entry list");
 
 struct ChunkPart {
   float m;        // chunk max logit
   float pad;
-  double s1;      // sum exp(x - m)
-  double sT;      // sum exp((x - m) / T)
+  ff s1;          // sum exp(x - m)
+  ff sT;          // sum exp((x - m) / T)
   float tv[K];    // top-K logits of the chunk, best first
   int ti[K];      // their token ids (INT_MAX = empty)
 };
@@ -59,87 +65,103 @@ __device__ __forceinline__ ChunkPart* parts(const TreeBuildPlan& p, uint8_t* ws)
   return reinterpret_cast<ChunkPart*>(ws + p.off_part);
 }
 
+// Order of (value, id) pairs: best first.  Two float-float values compare as reals.
+__device__ __forceinline__ bool ff_eq(ff a, ff b) { return a.hi == b.hi && a.lo == b.lo; }
+__device__ __forceinline__ bool before_ff(ff va, int ia, ff vb, int ib) {
+  return ff_gt(va, vb) || (ff_eq(va, vb) && ia < ib);
+}
+
+// Compare-exchange of two list entries so that entry i comes before entry j.
+__device__ __forceinline__ void cas(float& vi, int& ii, float& vj, int& ij) {
+  const bool sw = before(vj, ij, vi, ii);
+  const float tv = sw ? vj : vi;
+  const int t = sw ? ij : ii;
+  vj = sw ? vi : vj;
+  ij = sw ? ii : ij;
+  vi = tv;
+  ii = t;
+}
+
+// Bitonic sorting network over K registers, best first (indices are compile-time
+// constants once the loops unroll, so the arrays stay in registers).
+__device__ __forceinline__ void sort_regs(float (&v)[K], int (&id)[K]) {
+#pragma unroll
+  for (int k = 2; k <= K; k <<= 1) {
+#pragma unroll
+    for (int j = k >> 1; j > 0; j >>= 1) {
+#pragma unroll
+      for (int i = 0; i < K; ++i) {
+        const int l = i ^ j;
+        if (l > i) {
+          if ((i & k) == 0)
+            cas(v[i], id[i], v[l], id[l]);
+          else
+            cas(v[l], id[l], v[i], id[i]);
+        }
+      }
+    }
+  }
+}
+
 // ------------------------------------------------------------------ chunk pass
 template <bool TOPK>
-__global__ void __launch_bounds__(kThreads) tree_chunk_kernel(const TreeBuildPlan p, const BuildArgs a) {
+__global__ void __launch_bounds__(kThreads, 2) tree_chunk_kernel(const TreeBuildPlan p, const BuildArgs a) {
   const int bf = blockIdx.x, c = blockIdx.y;
   const int b = bf / a.F, f = bf % a.F;
   const int lo = c * kVocabChunk;
   const int hi = min(p.V, lo + kVocabChunk);
   const size_t row = static_cast<size_t>(bf) * p.V;
   const float invT = 1.f / (p.temperature > 0.f ? p.temperature : 1.f);
-
-  float m = -INFINITY;
-  CSum s1, sT;
-  float tv[K];
-  int ti[K];
-#pragma unroll
-  for (int j = 0; j < K; ++j) {
-    tv[j] = -INFINITY;
-    ti[j] = INT_MAX;
-  }
-  for (int v = lo + threadIdx.x; v < hi; v += kThreads) {
-    const float x = load_elem(a.logits, row + v, p.dtype);
-    if (x > m) {
-      if (m != -INFINITY) {
-        s1.scale(expf(m - x));
-        sT.scale(expf((m - x) * invT));
-      }
-      m = x;
-    }
-    s1.add(expf(x - m));
-    sT.add(expf((x - m) * invT));
-    if (TOPK && before(x, v, tv[K - 1], ti[K - 1])) {
-      float cv = x;
-      int ci = v;
-#pragma unroll
-      for (int j = 0; j < K; ++j) {
-        const bool bt = before(cv, ci, tv[j], ti[j]);
-        const float ov = tv[j];
-        const int oi = ti[j];
-        tv[j] = bt ? cv : ov;
-        ti[j] = bt ? ci : oi;
-        cv = bt ? ov : cv;
-        ci = bt ? oi : ci;
-      }
-    }
-  }
-  // block reduction of (m, s1, sT): sums rescaled to the warp max, in double
-  __shared__ float sm[kThreads / 32];
-  __shared__ double ss1[kThreads / 32], ssT[kThreads / 32];
-  __shared__ float wv[kThreads / 32];
-  __shared__ int wi[kThreads / 32];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const float M = warp_max(m);
-  double d1 = (m == -INFINITY) ? 0.0 : s1.total() * static_cast<double>(expf(m - M));
-  double dT = (m == -INFINITY) ? 0.0 : sT.total() * static_cast<double>(expf((m - M) * invT));
-  d1 = warp_sum_d(d1);
-  dT = warp_sum_d(dT);
+
+  __shared__ float sm[NW];
+  __shared__ ff ss1[NW], ssT[NW];
+  __shared__ float wlv[NW][K];
+  __shared__ int wli[NW][K];
+
+  // all loads first: element v = lo + threadIdx.x + kThreads * e (coalesced per e)
+  float x[kPer];
+  int xi[kPer];
+#pragma unroll
+  for (int e = 0; e < kPer; ++e) {
+    const int v = lo + threadIdx.x + kThreads * e;
+    x[e] = v < hi ? load_elem(a.logits, row + v, p.dtype) : -INFINITY;
+    xi[e] = v < hi ? v : INT_MAX;
+  }
+  // chunk max (two passes over registers: no online rescale)
+  float m = x[0];
+#pragma unroll
+  for (int e = 1; e < kPer; ++e) m = fmaxf(m, x[e]);
+  m = warp_max(m);
+  if (lane == 0) sm[warp] = m;
+  __syncthreads();
+  float BM = sm[0];
+#pragma unroll
+  for (int w = 1; w < NW; ++w) BM = fmaxf(BM, sm[w]);
+  CSum s1, sT;
+  if (BM != -INFINITY) {
+#pragma unroll
+    for (int e = 0; e < kPer; ++e) {
+      s1.add(expf(x[e] - BM));
+      sT.add(expf((x[e] - BM) * invT));
+    }
+  }
+  const ff d1 = warp_sum_ff(csum_ff(s1));
+  const ff dT = warp_sum_ff(csum_ff(sT));
   if (lane == 0) {
-    sm[warp] = M;
     ss1[warp] = d1;
     ssT[warp] = dT;
   }
-  __syncthreads();
   ChunkPart* out = parts(p, a.ws) + (static_cast<size_t>(b) * p.f_max + f) * p.n_chunks + c;
-  if (threadIdx.x == 0) {
-    float BM = -INFINITY;
-    for (int w = 0; w < kThreads / 32; ++w) BM = fmaxf(BM, sm[w]);
-    double t1 = 0.0, tT = 0.0;
-    for (int w = 0; w < kThreads / 32; ++w) {
-      if (sm[w] == -INFINITY) continue;
-      t1 += ss1[w] * static_cast<double>(expf(sm[w] - BM));
-      tT += ssT[w] * static_cast<double>(expf((sm[w] - BM) * invT));
-    }
-    out->m = BM;
-    out->s1 = t1;
-    out->sT = tT;
-  }
   if constexpr (TOPK) {
-    // block top-K: K rounds of block argmax over the threads' list heads
+    // each thread sorts its K logits; each warp takes its best K by K rounds of warp
+    // argmax over the lanes' list heads; the chunk's best K of the NW warp lists are
+    // found by rank: an entry's rank is the count of entries before it in every list.
+    sort_regs(x, xi);
+#pragma unroll 1
     for (int r = 0; r < K; ++r) {
-      float bv = tv[0];
-      int bi = ti[0];
+      float bv = x[0];
+      int bi = xi[0];
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) {
         const float v2 = __shfl_xor_sync(0xffffffffu, bv, o);
@@ -149,31 +171,56 @@ __global__ void __launch_bounds__(kThreads) tree_chunk_kernel(const TreeBuildPla
           bi = i2;
         }
       }
-      __syncthreads();
       if (lane == 0) {
-        wv[warp] = bv;
-        wi[warp] = bi;
+        wlv[warp][r] = bv;
+        wli[warp][r] = bi;
       }
-      __syncthreads();
-      bv = wv[0];
-      bi = wi[0];
-      for (int w = 1; w < kThreads / 32; ++w)
-        if (before(wv[w], wi[w], bv, bi)) {
-          bv = wv[w];
-          bi = wi[w];
-        }
-      if (threadIdx.x == 0) {
-        out->tv[r] = bv;
-        out->ti[r] = bi;
-      }
-      if (bi != INT_MAX && ti[0] == bi) {  // the owner pops its head
+      if (bi != INT_MAX && xi[0] == bi) {  // the owner pops its head
 #pragma unroll
         for (int j = 0; j < K - 1; ++j) {
-          tv[j] = tv[j + 1];
-          ti[j] = ti[j + 1];
+          x[j] = x[j + 1];
+          xi[j] = xi[j + 1];
         }
-        tv[K - 1] = -INFINITY;
-        ti[K - 1] = INT_MAX;
+        x[K - 1] = -INFINITY;
+        xi[K - 1] = INT_MAX;
+      }
+    }
+    if (threadIdx.x < K) {  // slots no real entry reaches stay empty
+      out->tv[threadIdx.x] = -INFINITY;
+      out->ti[threadIdx.x] = INT_MAX;
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    ff t1 = ff_make(0.f), tT = ff_make(0.f);
+    for (int w = 0; w < NW; ++w) {
+      t1 = ff_add(t1, ss1[w]);
+      tT = ff_add(tT, ssT[w]);
+    }
+    out->m = BM;
+    out->s1 = t1;
+    out->sT = tT;
+  }
+  if constexpr (TOPK) {
+    if (threadIdx.x < NW * K) {
+      const int w0 = threadIdx.x / K, r0 = threadIdx.x % K;
+      const float cv = wlv[w0][r0];
+      const int ci = wli[w0][r0];
+      if (ci != INT_MAX) {
+        int rank = r0;
+        for (int w = 0; w < NW; ++w) {
+          if (w == w0) continue;
+          int n = 0;  // entries of list w before (cv, ci): binary search of a sorted list
+#pragma unroll
+          for (int step = K / 2; step > 0; step >>= 1)
+            if (before(wlv[w][n + step - 1], wli[w][n + step - 1], cv, ci)) n += step;
+          if (n == K - 1 && before(wlv[w][K - 1], wli[w][K - 1], cv, ci)) n = K;
+          rank += n;
+        }
+        if (rank < K) {
+          out->tv[rank] = cv;
+          out->ti[rank] = ci;
+        }
       }
     }
   }
@@ -181,21 +228,21 @@ __global__ void __launch_bounds__(kThreads) tree_chunk_kernel(const TreeBuildPla
 
 // ------------------------------------------------------------------ select helpers
 // Block bitonic sort of n2 (power of two) entries, best first by (key desc, idx asc).
-__device__ void bitonic_sort(double* key, int* idx, int n2) {
+__device__ void bitonic_sort(ff* key, int* idx, int n2) {
   for (int k = 2; k <= n2; k <<= 1) {
     for (int j = k >> 1; j > 0; j >>= 1) {
       for (int i = threadIdx.x; i < n2; i += blockDim.x) {
         const int ixj = i ^ j;
         if (ixj > i) {
           const bool up = (i & k) == 0;
-          const bool sw = up ? before(key[ixj], idx[ixj], key[i], idx[i]) : before(key[i], idx[i], key[ixj], idx[ixj]);
+          const ff ki = key[i], kj = key[ixj];
+          const int ii = idx[i], ij = idx[ixj];
+          const bool sw = up ? before_ff(kj, ij, ki, ii) : before_ff(ki, ii, kj, ij);
           if (sw) {
-            const double tk = key[i];
-            key[i] = key[ixj];
-            key[ixj] = tk;
-            const int t = idx[i];
-            idx[i] = idx[ixj];
-            idx[ixj] = t;
+            key[i] = kj;
+            key[ixj] = ki;
+            idx[i] = ij;
+            idx[ixj] = ii;
           }
         }
       }
@@ -204,29 +251,63 @@ __device__ void bitonic_sort(double* key, int* idx, int n2) {
   }
 }
 
+// Exclusive ranks, in index order, of the entries of fr[0, n) that are non-zero:
+// fr[i] becomes that rank, or -1 for a zero entry.  Block-wide; ends synchronised.
+__device__ void block_flag_ranks(int* fr, int n, int* s_cnt) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  int running = 0;
+  for (int base = 0; base < n; base += kThreads) {
+    const int i = base + threadIdx.x;
+    const int fl = (i < n) ? fr[i] : 0;
+    const unsigned bal = __ballot_sync(0xffffffffu, fl != 0);
+    __syncthreads();  // readers of s_cnt from the previous chunk are done
+    if (lane == 0) s_cnt[warp] = __popc(bal);
+    __syncthreads();
+    int off = running, tot = 0;
+    for (int w = 0; w < NW; ++w) {
+      if (w < warp) off += s_cnt[w];
+      tot += s_cnt[w];
+    }
+    if (i < n) fr[i] = fl ? off + __popc(bal & ((1u << lane) - 1u)) : -1;
+    running += tot;
+  }
+  __syncthreads();
+}
+
+// ln z for a float-float z > 0, as float-float (one double log).
+__device__ __forceinline__ ff ff_log(ff z) {
+  const double d = log(static_cast<double>(z.hi) + static_cast<double>(z.lo));
+  const float h = static_cast<float>(d);
+  return ff{h, static_cast<float>(d - static_cast<double>(h))};
+}
+
 // Row statistics merged over chunks by one warp: M, ln Z (T = 1) and the mass at
-// temperature T (for draws), in double.
+// temperature T (for draws), as float-float.
 struct RowStats {
   float M;
-  double lnZ1, WT;
+  ff lnZ1, WT;
 };
 
 __device__ RowStats row_stats(const ChunkPart* cp, int n_chunks, float invT) {
   float M = -INFINITY;
   for (int c = threadIdx.x & 31; c < n_chunks; c += 32) M = fmaxf(M, cp[c].m);
   M = warp_max(M);
-  double z1 = 0.0, zT = 0.0;
+  ff z1 = ff_make(0.f), zT = ff_make(0.f);
   for (int c = threadIdx.x & 31; c < n_chunks; c += 32) {
-    if (cp[c].m == -INFINITY) continue;
-    z1 += cp[c].s1 * static_cast<double>(expf(cp[c].m - M));
-    zT += cp[c].sT * static_cast<double>(expf((cp[c].m - M) * invT));
+    const ChunkPart& q = cp[c];
+    if (q.m == -INFINITY) continue;
+    z1 = ff_add(z1, ff_mul(q.s1, expf(q.m - M)));
+    zT = ff_add(zT, ff_mul(q.sT, expf((q.m - M) * invT)));
   }
   RowStats r;
   r.M = M;
-  r.lnZ1 = log(warp_sum_d(z1));
-  r.WT = warp_sum_d(zT);
+  r.lnZ1 = ff_log(warp_sum_ff(z1));
+  r.WT = warp_sum_ff(zT);
   return r;
 }
+
+// ln q(t) = (x_t - M) - ln Z for a logit x_t of the row (x - M exact as float-float).
+__device__ __forceinline__ ff log_q(float x, const RowStats& rs) { return ff_sub(two_sum(x, -rs.M), rs.lnZ1); }
 
 // Warp merge of the chunks' top-K lists: writes the best `cnt` (token ids) to tok[].
 __device__ void merge_topk(const ChunkPart* cp, int n_chunks, int cnt, int* tok, float* val) {
@@ -268,28 +349,35 @@ __device__ void merge_topk(const ChunkPart* cp, int n_chunks, int cnt, int* tok,
   __syncwarp();
 }
 
+__device__ __forceinline__ ff ff_shfl(ff v, int src) {
+  return ff{__shfl_sync(0xffffffffu, v.hi, src), __shfl_sync(0xffffffffu, v.lo, src)};
+}
+__device__ __forceinline__ ff ff_shfl_up(ff v, int o) {
+  return ff{__shfl_up_sync(0xffffffffu, v.hi, o), __shfl_up_sync(0xffffffffu, v.lo, o)};
+}
+
 // Warp inverse-CDF draw over one logit row with weights exp((x - M) / T): the chunk
 // masses pick the chunk that holds the crossing, then the lanes scan that chunk
-// (lane offsets in double, local running sums in fp32).  Returns the token; *near =
-// 1 when the draw lands within 1e-7 of the mass of a bin edge.
+// (running sums as float-float).  Returns the token; *near = 1 when the draw lands
+// within 1e-7 of the mass of a bin edge.
 __device__ int warp_draw(const void* logits, size_t row, int dtype, int V, const ChunkPart* cp, int n_chunks, float M,
-                         float invT, double W, float u, int* near) {
+                         float invT, ff W, float u, int* near) {
   const int lane = threadIdx.x & 31;
-  const double target = static_cast<double>(u) * W;
+  const ff target = ff_mul(W, u);
   int cstar = -1, fallback = 0;
-  double base = 0.0;
+  ff base = ff_make(0.f);
   if (lane == 0) {
-    double cum = 0.0;
+    ff cum = ff_make(0.f);
     int last_pos = -1;
     for (int c = 0; c < n_chunks; ++c) {
-      const double w = (cp[c].m == -INFINITY) ? 0.0 : cp[c].sT * static_cast<double>(expf((cp[c].m - M) * invT));
-      if (w > 0.0) last_pos = c;
-      if (cum + w > target) {
+      const ff w = (cp[c].m == -INFINITY) ? ff_make(0.f) : ff_mul(cp[c].sT, expf((cp[c].m - M) * invT));
+      if (w.hi > 0.f) last_pos = c;
+      if (ff_gt(ff_add(cum, w), target)) {
         cstar = c;
         base = cum;
         break;
       }
-      cum += w;
+      cum = ff_add(cum, w);
     }
     if (cstar < 0) {  // nothing crosses (rounding): the last positive weight
       cstar = last_pos < 0 ? 0 : last_pos;
@@ -298,33 +386,33 @@ __device__ int warp_draw(const void* logits, size_t row, int dtype, int V, const
   }
   cstar = __shfl_sync(0xffffffffu, cstar, 0);
   fallback = __shfl_sync(0xffffffffu, fallback, 0);
-  base = __shfl_sync(0xffffffffu, base, 0);
+  base = ff_shfl(base, 0);
   const int lo = cstar * kVocabChunk, hi = min(V, lo + kVocabChunk);
   const int n = hi - lo;
   const int seg = (n + 31) / 32;
   const int a0 = lo + lane * seg, a1 = min(hi, a0 + seg);
-  double my = 0.0;
-  for (int v = a0; v < a1; ++v) my += static_cast<double>(expf((load_elem(logits, row + v, dtype) - M) * invT));
-  double incl = my;
+  ff my = ff_make(0.f);
+  for (int v = a0; v < a1; ++v) my = ff_add(my, expf((load_elem(logits, row + v, dtype) - M) * invT));
+  ff incl = my;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    const double t = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += t;
+    const ff t = ff_shfl_up(incl, o);
+    if (lane >= o) incl = ff_add(incl, t);
   }
-  const double lbase = base + incl - my;
-  const double rel = fallback ? INFINITY : target - lbase;
-  double cum = 0.0;
+  const ff lbase = ff_sub(ff_add(base, incl), my);
+  const ff rel = fallback ? ff_make(INFINITY) : ff_sub(target, lbase);
+  ff cum = ff_make(0.f);
   int found = -1;
-  double prev_edge = 0.0, next_edge = 0.0;
+  ff prev_edge = ff_make(0.f), next_edge = ff_make(0.f);
   int last_pos = -1;
   for (int v = a0; v < a1; ++v) {
     const float w = expf((load_elem(logits, row + v, dtype) - M) * invT);
     if (w > 0.f) last_pos = v;
-    const double nc = cum + static_cast<double>(w);
-    if (found < 0 && w > 0.f && nc > rel) {
+    const ff nc = ff_add(cum, w);
+    if (found < 0 && w > 0.f && ff_gt(nc, rel)) {
       found = v;
-      prev_edge = lbase + cum;
-      next_edge = lbase + nc;
+      prev_edge = ff_add(lbase, cum);
+      next_edge = ff_add(lbase, nc);
     }
     cum = nc;
   }
@@ -334,9 +422,10 @@ __device__ int warp_draw(const void* logits, size_t row, int dtype, int V, const
   if (ball) {
     const int src = __ffs(ball) - 1;
     tok = __shfl_sync(0xffffffffu, found, src);
-    const double pe = __shfl_sync(0xffffffffu, prev_edge, src);
-    const double ne = __shfl_sync(0xffffffffu, next_edge, src);
-    nr = (target - pe < kIcdfNearEps * W || ne - target < kIcdfNearEps * W) ? 1 : 0;
+    const ff pe = ff_shfl(prev_edge, src);
+    const ff ne = ff_shfl(next_edge, src);
+    const float win = kIcdfNearEps * ff_float(W);
+    nr = (ff_float(ff_sub(target, pe)) < win || ff_float(ff_sub(ne, target)) < win) ? 1 : 0;
   } else {
     const unsigned bl = __ballot_sync(0xffffffffu, last_pos >= 0);
     const int src = bl ? 31 - __clz(bl) : 0;
@@ -348,22 +437,21 @@ __device__ int warp_draw(const void* logits, size_t row, int dtype, int V, const
   return tok;
 }
 
-__global__ void __launch_bounds__(kThreads) tree_select_kernel(const TreeBuildPlan p, const BuildArgs a) {
+__global__ void __launch_bounds__(kThreads, 1) tree_select_kernel(const TreeBuildPlan p, const BuildArgs a) {
   const int b = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  constexpr int NW = kThreads / 32;
   uint8_t* ws = a.ws;
   int32_t* state = reinterpret_cast<int32_t*>(ws + p.off_state) + b * 4;  // [0] n_pool, [1] near
   const ChunkPart* cps = parts(p, ws) + static_cast<size_t>(b) * p.f_max * p.n_chunks;
   const float invT = 1.f / (p.temperature > 0.f ? p.temperature : 1.f);
 
-  __shared__ double skey[kMaxPool];
+  __shared__ ff skey[kMaxPool];
   __shared__ int sidx[kMaxPool];
   __shared__ int srow[kMaxPool];
   __shared__ int stok[NW][K];
   __shared__ float sval[NW][K];
+  __shared__ int s_cnt[NW];
   __shared__ int s_near;
-  __shared__ uint64_t smask[kMaxRows][2];
   __shared__ int spar[kMaxRows];
 
   if (threadIdx.x == 0) {
@@ -378,7 +466,7 @@ __global__ void __launch_bounds__(kThreads) tree_select_kernel(const TreeBuildPl
   if (p.mode == EAGLE_TREE_DYNAMIC) {
     int32_t* ptok = reinterpret_cast<int32_t*>(ws + p.off_pool_tok) + static_cast<size_t>(b) * p.pool_cap;
     int32_t* ppar = reinterpret_cast<int32_t*>(ws + p.off_pool_par) + static_cast<size_t>(b) * p.pool_cap;
-    double* psc = reinterpret_cast<double*>(ws + p.off_pool_score) + static_cast<size_t>(b) * p.pool_cap;
+    ff* psc = reinterpret_cast<ff*>(ws + p.off_pool_score) + static_cast<size_t>(b) * p.pool_cap;
     int32_t* pdep = reinterpret_cast<int32_t*>(ws + p.off_pool_depth) + static_cast<size_t>(b) * p.pool_cap;
     int32_t* front = reinterpret_cast<int32_t*>(ws + p.off_front) + static_cast<size_t>(b) * K;
     const int base = state[0];
@@ -389,12 +477,12 @@ __global__ void __launch_bounds__(kThreads) tree_select_kernel(const TreeBuildPl
       const RowStats rs = row_stats(cp, p.n_chunks, invT);
       merge_topk(cp, p.n_chunks, k, stok[warp], sval[warp]);
       const int pidx = (a.level == 1) ? -1 : front[f];
-      const double spar_score = (pidx < 0) ? 0.0 : psc[pidx];
+      const ff spar_score = (pidx < 0) ? ff_make(0.f) : psc[pidx];
       if (lane < k) {
         const int i = base + f * k + lane;
         ptok[i] = stok[warp][lane];
         ppar[i] = pidx;
-        psc[i] = spar_score + (static_cast<double>(sval[warp][lane] - rs.M) - rs.lnZ1);
+        psc[i] = ff_add(spar_score, log_q(sval[warp][lane], rs));
         pdep[i] = a.level;
       }
       __syncwarp();
@@ -405,29 +493,30 @@ __global__ void __launch_bounds__(kThreads) tree_select_kernel(const TreeBuildPl
     int n2 = 1;
     while (n2 < n_new) n2 <<= 1;
     for (int j = threadIdx.x; j < n2; j += kThreads) {
-      skey[j] = j < n_new ? psc[base + j] : -INFINITY;
+      skey[j] = j < n_new ? psc[base + j] : ff_make(-INFINITY);
       sidx[j] = j < n_new ? base + j : INT_MAX;
     }
     __syncthreads();
     bitonic_sort(skey, sidx, n2);
     // a near-tie at the boundary, unless it is an exact tie between siblings (same
-    // parent, same logit), which both fp32 and fp64 break by pool index
-    if (threadIdx.x == 0 && n_new > k && skey[k - 1] - skey[k] < kNearTieEps &&
-        !(skey[k - 1] == skey[k] && ppar[sidx[k - 1]] == ppar[sidx[k]]))
+    // parent, same logit), which both sides break by pool index
+    if (threadIdx.x == 0 && n_new > k && ff_float(ff_sub(skey[k - 1], skey[k])) < kNearTieEps &&
+        !(ff_eq(skey[k - 1], skey[k]) && ppar[sidx[k - 1]] == ppar[sidx[k]]))
       s_near += 1;
     for (int j = threadIdx.x; j < n_new; j += kThreads) srow[j] = 0;
     __syncthreads();
     for (int j = threadIdx.x; j < k; j += kThreads) srow[sidx[j] - base] = 1;
     __syncthreads();
+    block_flag_ranks(srow, n_new, s_cnt);
+    for (int j = threadIdx.x; j < n_new; j += kThreads) {
+      const int slot = srow[j];
+      if (slot < 0) continue;
+      front[slot] = base + j;
+      a.out.frontier_tok[static_cast<size_t>(b) * p.f_max + slot] = ptok[base + j];
+      a.out.frontier_slot[static_cast<size_t>(b) * p.f_max + slot] = j / k;
+    }
+    __syncthreads();
     if (threadIdx.x == 0) {
-      int slot = 0;
-      for (int j = 0; j < n_new; ++j) {
-        if (!srow[j]) continue;
-        front[slot] = base + j;
-        a.out.frontier_tok[static_cast<size_t>(b) * p.f_max + slot] = ptok[base + j];
-        a.out.frontier_slot[static_cast<size_t>(b) * p.f_max + slot] = j / k;
-        ++slot;
-      }
       state[0] = base + n_new;
       state[1] += s_near;
       s_near = 0;
@@ -436,41 +525,37 @@ __global__ void __launch_bounds__(kThreads) tree_select_kernel(const TreeBuildPl
     if (a.level != p.depth) return;
 
     // ---- last level: best N of the pool, rows in pool order
-    const int np = state[0];
+    const int np = base + n_new;
     const int N = p.N;
     n2 = 1;
     while (n2 < np) n2 <<= 1;
     for (int j = threadIdx.x; j < n2; j += kThreads) {
-      skey[j] = j < np ? psc[j] : -INFINITY;
+      skey[j] = j < np ? psc[j] : ff_make(-INFINITY);
       sidx[j] = j < np ? j : INT_MAX;
     }
     __syncthreads();
     bitonic_sort(skey, sidx, n2);
-    if (threadIdx.x == 0 && np > N && skey[N - 1] - skey[N] < kNearTieEps &&
-        !(skey[N - 1] == skey[N] && ppar[sidx[N - 1]] == ppar[sidx[N]]))
+    if (threadIdx.x == 0 && np > N && ff_float(ff_sub(skey[N - 1], skey[N])) < kNearTieEps &&
+        !(ff_eq(skey[N - 1], skey[N]) && ppar[sidx[N - 1]] == ppar[sidx[N]]))
       state[1] += 1;
     for (int j = threadIdx.x; j < np; j += kThreads) srow[j] = 0;
     __syncthreads();
     for (int j = threadIdx.x; j < N; j += kThreads) srow[sidx[j]] = 1;
     __syncthreads();
-    if (threadIdx.x == 0) {  // rows in pool order (one pass over the pool)
-      int r = 1;
-      for (int j = 0; j < np; ++j) srow[j] = srow[j] ? r++ : -1;
-    }
-    __syncthreads();
+    block_flag_ranks(srow, np, s_cnt);  // row of a selected pool entry = its rank + 1
     const size_t ob = static_cast<size_t>(b) * p.R;
     const int L = a.seq_len[b];
     for (int j = threadIdx.x; j < np; j += kThreads) {
-      const int r = srow[j];
-      if (r < 0) continue;
+      if (srow[j] < 0) continue;
+      const int r = srow[j] + 1;
       const int pp = ppar[j];
-      const int pr = (pp < 0) ? 0 : (srow[pp] > 0 ? srow[pp] : 0);
+      const int pr = (pp < 0) ? 0 : (srow[pp] >= 0 ? srow[pp] + 1 : 0);
       spar[r] = pr;
       a.out.tokens[ob + r] = ptok[j];
       a.out.parent[ob + r] = pr;
       a.out.depth[ob + r] = pdep[j];
       a.out.pos_id[ob + r] = L + pdep[j];
-      a.out.score[ob + r] = static_cast<float>(psc[j]);
+      a.out.score[ob + r] = ff_float(psc[j]);
     }
     if (threadIdx.x == 0) {
       spar[0] = -1;
@@ -484,19 +569,19 @@ __global__ void __launch_bounds__(kThreads) tree_select_kernel(const TreeBuildPl
   } else {
     // ---- static shape
     int32_t* ntok = reinterpret_cast<int32_t*>(ws + p.off_node_tok) + static_cast<size_t>(b) * p.R;
-    double* nsc = reinterpret_cast<double*>(ws + p.off_node_score) + static_cast<size_t>(b) * p.R;
+    ff* nsc = reinterpret_cast<ff*>(ws + p.off_node_score) + static_cast<size_t>(b) * p.R;
     const bool sampled = p.mode == EAGLE_TREE_STATIC_SAMPLED;
     if (a.level == 1 && threadIdx.x == 0) {
       ntok[0] = a.root_tok[b];
-      nsc[0] = 0.0;
+      nsc[0] = ff_make(0.f);
     }
     __syncthreads();
     // frontier row f = the f-th node of depth level-1; one warp per row
     int near_local = 0;
     for (int f = warp; f < a.F; f += NW) {
-      int n = -1, cnt = -1;
+      int n = -1;
       for (int i = 0; i < p.R; ++i)
-        if (p.shape.depth[i] == a.level - 1 && ++cnt == f) {
+        if (p.shape.depth[i] == a.level - 1 && p.shape.lrank[i] == f) {
           n = i;
           break;
         }
@@ -522,7 +607,7 @@ __global__ void __launch_bounds__(kThreads) tree_select_kernel(const TreeBuildPl
         }
         if (lane == 0) {
           ntok[ch] = tok;
-          nsc[ch] = nsc[n] + (static_cast<double>(load_elem(a.logits, row + tok, p.dtype) - rs.M) - rs.lnZ1);
+          nsc[ch] = ff_add(nsc[n], log_q(load_elem(a.logits, row + tok, p.dtype), rs));
         }
         ++j;
       }
@@ -530,20 +615,15 @@ __global__ void __launch_bounds__(kThreads) tree_select_kernel(const TreeBuildPl
     }
     if (lane == 0 && near_local) atomicAdd(&s_near, near_local);
     __syncthreads();
-    if (threadIdx.x == 0) {
-      state[1] += s_near;
-      // next frontier: the nodes of depth `level`, with their parent's row in this level's input
-      int slot = 0;
-      for (int i = 0; i < p.R; ++i) {
-        if (p.shape.depth[i] != a.level) continue;
-        const int par = p.shape.parent[i];
-        int prow = 0;
-        for (int q = 0; q < par; ++q) prow += (p.shape.depth[q] == a.level - 1);
-        a.out.frontier_tok[static_cast<size_t>(b) * p.f_max + slot] = ntok[i];
-        a.out.frontier_slot[static_cast<size_t>(b) * p.f_max + slot] = prow;
-        ++slot;
-      }
+    // next frontier: the nodes of depth `level` in index order, with their parent's
+    // row in this level's input (the parent's rank within its depth)
+    for (int i = threadIdx.x; i < p.R; i += kThreads) {
+      if (p.shape.depth[i] != a.level) continue;
+      const int slot = p.shape.lrank[i];
+      a.out.frontier_tok[static_cast<size_t>(b) * p.f_max + slot] = ntok[i];
+      a.out.frontier_slot[static_cast<size_t>(b) * p.f_max + slot] = p.shape.lrank[p.shape.parent[i]];
     }
+    if (threadIdx.x == 0) state[1] += s_near;
     __syncthreads();
     if (a.level != p.depth) return;
     const size_t ob = static_cast<size_t>(b) * p.R;
@@ -554,30 +634,25 @@ __global__ void __launch_bounds__(kThreads) tree_select_kernel(const TreeBuildPl
       a.out.parent[ob + i] = p.shape.parent[i];
       a.out.depth[ob + i] = p.shape.depth[i];
       a.out.pos_id[ob + i] = L + p.shape.depth[i];
-      a.out.score[ob + i] = static_cast<float>(nsc[i]);
+      a.out.score[ob + i] = ff_float(nsc[i]);
     }
     __syncthreads();
   }
-  // ancestor masks: row i = row parent(i) | bit i (parents come first)
-  if (threadIdx.x == 0) {
-    for (int i = 0; i < p.R; ++i) {
-      uint64_t w0 = 0, w1 = 0;
-      if (i > 0) {
-        w0 = smask[spar[i]][0];
-        w1 = smask[spar[i]][1];
-      }
-      if (i < 64)
-        w0 |= 1ull << i;
-      else
-        w1 |= 1ull << (i - 64);
-      smask[i][0] = w0;
-      smask[i][1] = w1;
-    }
-  }
-  __syncthreads();
+  // ancestor masks: row i has bits i and those of its ancestors (each row walks up
+  // the parent chain; parents come first, so at most R steps)
+  const size_t mb = static_cast<size_t>(b) * p.R;
   for (int i = threadIdx.x; i < p.R; i += kThreads) {
-    a.out.anc_mask[(static_cast<size_t>(b) * p.R + i) * p.W] = smask[i][0];
-    if (p.W > 1) a.out.anc_mask[(static_cast<size_t>(b) * p.R + i) * p.W + 1] = smask[i][1];
+    uint64_t w0 = 0, w1 = 0;
+    int j = i;
+    for (int steps = 0; j >= 0 && steps < p.R; ++steps) {
+      if (j < 64)
+        w0 |= 1ull << j;
+      else
+        w1 |= 1ull << (j - 64);
+      j = spar[j];
+    }
+    a.out.anc_mask[(mb + i) * p.W] = w0;
+    if (p.W > 1) a.out.anc_mask[(mb + i) * p.W + 1] = w1;
   }
   if (threadIdx.x == 0) a.out.near_tie[b] = state[1];
 }
@@ -615,6 +690,8 @@ void plan_tree_build(const eagle_tree_desc* d, TreeBuildPlan* p) {
       if (p->shape.depth[i] > maxd) maxd = p->shape.depth[i];
     }
     p->depth = maxd;
+    int seen[kMaxRows] = {0};
+    for (int i = 0; i < p->R && i < kMaxRows; ++i) p->shape.lrank[i] = static_cast<uint8_t>(seen[p->shape.depth[i]]++);
     int fmax = 1;
     for (int dd = 0; dd <= maxd; ++dd) {
       int c = 0;
@@ -631,7 +708,7 @@ void plan_tree_build(const eagle_tree_desc* d, TreeBuildPlan* p) {
   p->off_pool_par = off;
   off = align256(off + cap * 4);
   p->off_pool_score = off;
-  off = align256(off + cap * 8);
+  off = align256(off + cap * sizeof(ff));
   p->off_pool_depth = off;
   off = align256(off + cap * 4);
   p->off_state = off;
@@ -643,7 +720,7 @@ void plan_tree_build(const eagle_tree_desc* d, TreeBuildPlan* p) {
   p->off_node_tok = off;
   off = align256(off + static_cast<size_t>(p->B) * p->R * 4);
   p->off_node_score = off;
-  off = align256(off + static_cast<size_t>(p->B) * p->R * 8);
+  off = align256(off + static_cast<size_t>(p->B) * p->R * sizeof(ff));
   p->total = off;
 }
 

@@ -55,6 +55,7 @@ class GpuTreeBuilder:
         self.depth = w.depth if w.tree_mode == "dynamic" else self.desc.depth
         self.root_tok = None
         self.seq_len = None
+        self.levels = []  # (level, device logits, device uniforms) of every expand call
 
     def set_context(self, root_tok: np.ndarray, seq_len: np.ndarray):
         self.root_tok = torch.from_numpy(np.asarray(root_tok, np.int32)).to(self.device)
@@ -66,6 +67,7 @@ class GpuTreeBuilder:
         lg = _to_dev(logits, self.w.dtype, self.device)
         ud = None if u_draft is None else torch.from_numpy(np.asarray(u_draft, np.float32)).to(self.device)
         B.eagle_tree_build(self.desc, level, lg, ud, self.root_tok, self.seq_len, self.ws, self.out)
+        self.levels = [lv for lv in self.levels if lv[0] < level] + [(level, lg, ud)]
         if self.w.tree_mode == "dynamic":
             F = self.w.top_k
         else:  # the nodes created at this level (depth == level), in row order
@@ -77,6 +79,11 @@ class GpuTreeBuilder:
         tok = self.out.frontier_tok[:, :F].cpu().numpy()
         slot = self.out.frontier_slot[:, :F].cpu().numpy()
         return tok, slot
+
+    def replay(self, stream=None):
+        """Enqueue the whole build again (every level, inputs already on the device)."""
+        for level, lg, ud in self.levels:
+            B.eagle_tree_build(self.desc, level, lg, ud, self.root_tok, self.seq_len, self.ws, self.out, stream)
 
     def finalize(self, root_tok: np.ndarray, seq_len: np.ndarray):
         o = self.out
@@ -133,9 +140,10 @@ class VerifyStep:
         self.root_hashes = [synth.root_hash(w.config_id, b) for b in range(Bn)]
         ua, uf, ud = synth.step_uniforms(w, Bn, w.rows)
         self.u_draft_host = ud
+        self.builder = None
         if tree is None:
-            tree, _ = build_tree(w, Bn, self.root_tok, self.root_hashes, self.seq_len0,
-                                 ud if w.tree_mode == "static_sampled" else None, device)
+            tree, self.builder = build_tree(w, Bn, self.root_tok, self.root_hashes, self.seq_len0,
+                                            ud if w.tree_mode == "static_sampled" else None, device)
         self.tree = tree
         R = tree["tokens"].shape[1]
         self.R = R
