@@ -52,9 +52,12 @@ constexpr int HALF = 16384;               // one 64-dim half of a 128-row tile (
 constexpr int TILE = 2 * HALF;            // one K or V tile
 constexpr int NTHREADS = 320;
 constexpr int SM_Q = 0;                   // the 128-row M-tile, 32 KB
-constexpr int SM_K = TILE;                // 2 stages
-constexpr int SM_V = 3 * TILE;            // 2 stages
-constexpr int SMEM_BYTES = 5 * TILE + 1024;
+constexpr int KST = 2;                    // K ring stages
+constexpr int VST = 2;                    // V ring stages
+constexpr int SM_K = TILE;
+constexpr int SM_V = SM_K + KST * TILE;
+constexpr int SMEM_BYTES = SM_V + VST * TILE + 1024;
+static_assert(KST >= 2, "the partial staging area reuses two K stages");
 // TMEM columns: S / P of tile t in buffer t & 1, then the O accumulator
 __device__ __forceinline__ uint32_t col_s(int j) { return static_cast<uint32_t>(j) * 128u; }
 constexpr uint32_t COL_O = 256u;
@@ -298,7 +301,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     tree_attn_tc_kernel(const __grid_constant__ Tmaps tm, const TcArgs a) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  __shared__ uint64_t bar_q, k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[2], p_full[2], o_done, o_full;
+  __shared__ uint64_t bar_q, k_full[KST], k_empty[KST], v_full[VST], v_empty[VST], s_full[2], p_full[2], o_done, o_full;
   __shared__ uint32_t tmem_base;
   __shared__ int s_abort;
   __shared__ float s_red[2][2][2][128];  // [tile parity][M-tile][key half][row] half-row maxima
@@ -308,16 +311,25 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   const int split = blockIdx.x, bh = blockIdx.y, rb = blockIdx.z;
   const int b = bh / a.Hkv, h = bh % a.Hkv;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const TileInfo ti = tile_info(a, b, split);
   const int n_mt = a.n_mt;
 
+  // prologue: nothing read from global memory before griddep_wait below
+  if (warp == 8 && lane == 0) {
+    prefetch_tmap(&tm.q);
+    prefetch_tmap(&tm.kc);
+    prefetch_tmap(&tm.vc);
+  }
   if (threadIdx.x == 0) {
     mbar_init(&bar_q, 1);
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < KST; ++s) {
       mbar_init(&k_full[s], 1);
       mbar_init(&k_empty[s], 1);
+    }
+    for (int s = 0; s < VST; ++s) {
       mbar_init(&v_full[s], 1);
       mbar_init(&v_empty[s], 1);
+    }
+    for (int s = 0; s < 2; ++s) {
       mbar_init(&s_full[s], 1);
       mbar_init(&p_full[s], 256);
     }
@@ -332,24 +344,30 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   }
   __syncthreads();
   tc_fence_after();
-  const uint32_t tb = tmem_base;
+  // the inputs (and the workspace counters) belong to the preceding kernel in the
+  // stream until it completes
+  griddep_wait();
+  griddep_launch_dependents();
   uint8_t* sQ = smem + SM_Q;
+  // Q does not depend on the sequence length: its load goes out before seq_len is read
+  // (the MMA warp always waits for it, so no copy is in flight at exit)
+  if (warp == 8 && lane == 0) {
+    mbar_arrive_expect_tx(&bar_q, n_mt * TILE);
+    for (int i = 0; i < n_mt; ++i) {
+      const int node0 = (rb * a.rows_per_cta + i * 128) / a.G;
+      for (int hh = 0; hh < 2; ++hh)
+        tma_load_3d(sQ + i * TILE + hh * HALF, &tm.q, 64 * hh, h * a.G, b * a.R + node0, &bar_q);
+    }
+  }
+  const TileInfo ti = tile_info(a, b, split);
+  const uint32_t tb = tmem_base;
 
   if (warp == 8) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0 && ti.n_tiles > 0) {
-      prefetch_tmap(&tm.q);
-      prefetch_tmap(&tm.kc);
-      prefetch_tmap(&tm.vc);
-      mbar_arrive_expect_tx(&bar_q, n_mt * TILE);
-      for (int i = 0; i < n_mt; ++i) {
-        const int node0 = (rb * a.rows_per_cta + i * 128) / a.G;
-        for (int hh = 0; hh < 2; ++hh)
-          tma_load_3d(sQ + i * TILE + hh * HALF, &tm.q, 64 * hh, h * a.G, b * a.R + node0, &bar_q);
-      }
       const uint64_t policy = policy_evict_first();
       for (int t = 0; t < ti.n_tiles; ++t) {
-        const int s = t & 1, use = t >> 1;
+        const int s = t % KST, use = t / KST, sv = t % VST, usev = t / VST;
         const bool tree = t >= ti.n_pt;
         const CUtensorMap* mk = tree ? &tm.tk : &tm.kc;
         const CUtensorMap* mv = tree ? &tm.tv : &tm.vc;
@@ -358,42 +376,42 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         mbar_arrive_expect_tx(&k_full[s], TILE);
         tma_load_2d_hint(smem + SM_K + s * TILE, mk, 0, y, &k_full[s], policy);
         tma_load_2d_hint(smem + SM_K + s * TILE + HALF, mk, 64, y, &k_full[s], policy);
-        if (use > 0 && !wait_parity(&v_empty[s], (use - 1) & 1, a.err, ERR_VEMPTY)) break;
-        mbar_arrive_expect_tx(&v_full[s], TILE);
-        tma_load_2d_hint(smem + SM_V + s * TILE, mv, 0, y, &v_full[s], policy);
-        tma_load_2d_hint(smem + SM_V + s * TILE + HALF, mv, 64, y, &v_full[s], policy);
+        if (usev > 0 && !wait_parity(&v_empty[sv], (usev - 1) & 1, a.err, ERR_VEMPTY)) break;
+        mbar_arrive_expect_tx(&v_full[sv], TILE);
+        tma_load_2d_hint(smem + SM_V + sv * TILE, mv, 0, y, &v_full[sv], policy);
+        tma_load_2d_hint(smem + SM_V + sv * TILE + HALF, mv, 64, y, &v_full[sv], policy);
       }
     }
   } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
     // S of tile t goes to TMEM buffer t & 1: QK(0) QK(1) | PV(0) QK(2) | PV(1) QK(3) | ...
     // so the tensor cores compute the next-but-one S while the softmax works on this one.
-    bool ok = ti.n_tiles > 0;
-    if (ok && lane == 0) ok = wait_parity(&bar_q, 0, a.err, ERR_Q);
-    ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-    auto qk = [&](int t) {  // lane 0; K stage and S buffer t & 1
-      const int s = t & 1;
-      if (!wait_parity(&k_full[s], (t >> 1) & 1, a.err, ERR_KFULL)) return false;
+    bool ok = true;
+    if (lane == 0) ok = wait_parity(&bar_q, 0, a.err, ERR_Q);
+    ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0 && ti.n_tiles > 0;
+    auto qk = [&](int t) {  // lane 0; K stage t % KST, S buffer t & 1
+      const int s = t % KST;
+      if (!wait_parity(&k_full[s], (t / KST) & 1, a.err, ERR_KFULL)) return false;
       tc_fence_after();
-      issue_qk(tb, sQ, smem + SM_K + s * TILE, col_s(s));
-      mma_commit(&s_full[s]);
+      issue_qk(tb, sQ, smem + SM_K + s * TILE, col_s(t & 1));
+      mma_commit(&s_full[t & 1]);
       mma_commit(&k_empty[s]);
       return true;
     };
     if (ok && lane == 0) ok = qk(0) && (ti.n_tiles < 2 || qk(1));
     ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
     for (int t = 0; t < ti.n_tiles && ok; ++t) {
-      const int s = t & 1;
+      const int s = t & 1, sv = t % VST;
       // V of tile t: wait, then zero the rows past the last valid key
-      ok = wait_parity(&v_full[s], (t >> 1) & 1, a.err, ERR_VFULL);
+      ok = wait_parity(&v_full[sv], (t / VST) & 1, a.err, ERR_VFULL);
       ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
       if (!ok) break;
       const int nv = tile_valid(a, ti, t);
       if (nv < KT) {
-        uint8_t* sv = smem + SM_V + s * TILE;
+        uint8_t* vt = smem + SM_V + sv * TILE;
         for (int idx = lane; idx < (KT - nv) * 16; idx += 32) {
           const int row = nv + (idx >> 4), part = idx & 15;
-          *reinterpret_cast<uint4*>(sv + (part >> 3) * HALF + row * 128 + (part & 7) * 16) = make_uint4(0, 0, 0, 0);
+          *reinterpret_cast<uint4*>(vt + (part >> 3) * HALF + row * 128 + (part & 7) * 16) = make_uint4(0, 0, 0, 0);
         }
         fence_proxy_async_smem();
       }
@@ -402,8 +420,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         ok = wait_parity(&p_full[s], (t >> 1) & 1, a.err, ERR_P);
         if (ok) {
           tc_fence_after();
-          issue_pv<PRECISE>(tb, smem + SM_V + s * TILE, col_s(s), t == 0);
-          mma_commit(&v_empty[s]);
+          issue_pv<PRECISE>(tb, smem + SM_V + sv * TILE, col_s(s), t == 0);
+          mma_commit(&v_empty[sv]);
           mma_commit(&o_done);
           if (t + 2 < ti.n_tiles) ok = qk(t + 2);
         }
@@ -801,13 +819,18 @@ cudaError_t launch_tc(const Tmaps& tm, const TcArgs& a, dim3 grid, cudaStream_t 
   cfg.blockDim = dim3(NTHREADS, 1, 1);
   cfg.dynamicSmemBytes = SMEM_BYTES;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
+  // programmatic: the prologue (barriers, TMEM, descriptor prefetch) overlaps the
+  // tail of the preceding kernel; the kernel waits for it before reading anything
+  cudaLaunchAttribute attr[2];
+  unsigned n = 0;
+  attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[n++].val.programmaticStreamSerializationAllowed = 1;
   if (a.coop) {
-    attr[0].id = cudaLaunchAttributeCooperative;
-    attr[0].val.cooperative = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    attr[n].id = cudaLaunchAttributeCooperative;
+    attr[n++].val.cooperative = 1;
   }
+  cfg.attrs = attr;
+  cfg.numAttrs = n;
   e = cudaLaunchKernelEx(&cfg, tree_attn_tc_kernel<PRECISE>, tm, a);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();

@@ -42,14 +42,15 @@ constexpr int kPer = kVocabChunk / kThreads;  // logits per thread in the chunk 
 constexpr float kIcdfNearEps = 1e-7f;
 static_assert(kPer == K, "the chunk pass sorts one thread's logits as a K-entry list");
 
-struct ChunkPart {
-  float m;        // chunk max logit
-  float pad;
-  ff s1;          // sum exp(x - m)
-  ff sT;          // sum exp((x - m) / T)
+struct __align__(16) ChunkPart {
   float tv[K];    // top-K logits of the chunk, best first
   int ti[K];      // their token ids (INT_MAX = empty)
+  ff s1;          // sum exp(x - m)
+  ff sT;          // sum exp((x - m) / T)
+  float m;        // chunk max logit
+  float pad[3];
 };
+static_assert(sizeof(ChunkPart) % 16 == 0, "chunk lists are read as 16-byte vectors");
 
 struct BuildArgs {
   const void* logits;
@@ -312,6 +313,62 @@ __device__ __forceinline__ ff log_q(float x, const RowStats& rs) { return ff_sub
 // Warp merge of the chunks' top-K lists: writes the best `cnt` (token ids) to tok[].
 __device__ void merge_topk(const ChunkPart* cp, int n_chunks, int cnt, int* tok, float* val) {
   const int lane = threadIdx.x & 31;
+  if (n_chunks <= 32) {
+    // lane c holds chunk c's whole list in registers (read once, 16-byte vectors)
+    float lv[K];
+    int li[K];
+    if (lane < n_chunks) {
+      const float4* pv = reinterpret_cast<const float4*>(cp[lane].tv);
+      const int4* pi = reinterpret_cast<const int4*>(cp[lane].ti);
+#pragma unroll
+      for (int q = 0; q < K / 4; ++q) {
+        const float4 v = pv[q];
+        const int4 i = pi[q];
+        lv[4 * q] = v.x;
+        lv[4 * q + 1] = v.y;
+        lv[4 * q + 2] = v.z;
+        lv[4 * q + 3] = v.w;
+        li[4 * q] = i.x;
+        li[4 * q + 1] = i.y;
+        li[4 * q + 2] = i.z;
+        li[4 * q + 3] = i.w;
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < K; ++j) {
+        lv[j] = -INFINITY;
+        li[j] = INT_MAX;
+      }
+    }
+    for (int r = 0; r < cnt; ++r) {
+      float bv = lv[0];
+      int bi = li[0];
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const float v2 = __shfl_xor_sync(0xffffffffu, bv, o);
+        const int i2 = __shfl_xor_sync(0xffffffffu, bi, o);
+        if (before(v2, i2, bv, bi)) {
+          bv = v2;
+          bi = i2;
+        }
+      }
+      if (lane == 0) {
+        tok[r] = bi;
+        val[r] = bv;
+      }
+      if (bi != INT_MAX && li[0] == bi) {  // the owner pops its head
+#pragma unroll
+        for (int j = 0; j < K - 1; ++j) {
+          lv[j] = lv[j + 1];
+          li[j] = li[j + 1];
+        }
+        lv[K - 1] = -INFINITY;
+        li[K - 1] = INT_MAX;
+      }
+    }
+    __syncwarp();
+    return;
+  }
   int head[4] = {0, 0, 0, 0};  // per owned chunk (lane, lane+32, ...)
   for (int r = 0; r < cnt; ++r) {
     float bv = -INFINITY;
