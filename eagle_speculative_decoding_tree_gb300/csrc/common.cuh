@@ -108,6 +108,23 @@ __device__ __forceinline__ ff ff_mul(ff a, float b) {
   return fast_two_sum(p, e);
 }
 
+// a * b for float-float a and b (the hi products' rounding error recovered by fma).
+__device__ __forceinline__ ff ff_mul(ff a, ff b) {
+  const float p = a.hi * b.hi;
+  float e = fmaf(a.hi, b.hi, -p);
+  e = fmaf(a.hi, b.lo, e);
+  e = fmaf(a.lo, b.hi, e);
+  return fast_two_sum(p, e);
+}
+
+// a / b for b != 0: a first quotient q1 = a.hi / b.hi, then the remainder a - q1 b
+// divided again; about 44 significant bits.
+__device__ __forceinline__ ff ff_div(ff a, ff b) {
+  const float q1 = a.hi / b.hi;
+  const ff r = ff_add(a, ff_neg(ff_mul(b, q1)));
+  return fast_two_sum(q1, r.hi / b.hi);
+}
+
 __device__ __forceinline__ bool ff_gt(ff a, ff b) { return a.hi > b.hi || (a.hi == b.hi && a.lo > b.lo); }
 __device__ __forceinline__ float ff_float(ff a) { return a.hi + a.lo; }
 

@@ -23,6 +23,7 @@ struct TreeBuildPlan {
   float temperature;
   int n_chunks;   // vocabulary chunks per row
   int f_max;      // widest frontier
+  int kc;         // entries of each chunk's top list that a level can use (top-k modes)
   int pool_cap;   // dynamic pool capacity per request
   StaticShape shape;
   // workspace carve-up (byte offsets)

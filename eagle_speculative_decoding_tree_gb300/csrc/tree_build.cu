@@ -23,8 +23,8 @@
 //                       memory) and, at the last level, emits the tree arrays.
 //
 // Precision: chunk sums are compensated fp32, merged as float-float (about 48
-// significant bits on the fp32 pipe; this GPU's fp64 pipe is narrow); ln Z is one
-// double log per row.  Cumulative scores are float-float, so that the selections
+// significant bits on the fp32 pipe; this GPU's fp64 pipe is narrow), and ln Z is a
+// float-float logarithm.  Cumulative scores are float-float, so that the selections
 // agree with an fp64 computation unless two scores at a boundary are within 1e-5
 // (reported as a near-tie).
 #include <limits.h>
@@ -72,9 +72,14 @@ __device__ __forceinline__ bool before_ff(ff va, int ia, ff vb, int ib) {
   return ff_gt(va, vb) || (ff_eq(va, vb) && ia < ib);
 }
 
+// (value desc, id asc) order without short-circuit evaluation (no branches).
+__device__ __forceinline__ bool before_nb(float va, int ia, float vb, int ib) {
+  return (va > vb) | ((va == vb) & (ia < ib));
+}
+
 // Compare-exchange of two list entries so that entry i comes before entry j.
 __device__ __forceinline__ void cas(float& vi, int& ii, float& vj, int& ij) {
-  const bool sw = before(vj, ij, vi, ii);
+  const bool sw = before_nb(vj, ij, vi, ii);
   const float tv = sw ? vj : vi;
   const int t = sw ? ij : ii;
   vj = sw ? vi : vj;
@@ -104,8 +109,47 @@ __device__ __forceinline__ void sort_regs(float (&v)[K], int (&id)[K]) {
   }
 }
 
+// A thread's kPer logits of the chunk [lo, hi) and their ids (-inf / INT_MAX past hi):
+// bf16 as two runs of 8 (lo + 2048 g + 8 t ..), fp32 as four runs of 4 (lo + 1024 g +
+// 4 t ..), each run one 16-byte load when `vec` (the row base is 16-byte aligned).
+template <bool BF16>
+__device__ __forceinline__ void load_chunk(const void* logits, size_t row, int lo, int hi, bool vec, float (&x)[kPer],
+                                           int (&xi)[kPer]) {
+  constexpr int RUN = BF16 ? 8 : 4;
+  constexpr int NRUN = kPer / RUN;
+#pragma unroll
+  for (int g = 0; g < NRUN; ++g) {
+    const int v0 = lo + g * kThreads * RUN + RUN * threadIdx.x;
+    if (vec && v0 + RUN <= hi) {
+      if constexpr (BF16) {
+        const uint4 w = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(logits) + row + v0));
+        const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          x[g * RUN + 2 * j] = __uint_as_float(u[j] << 16);
+          x[g * RUN + 2 * j + 1] = __uint_as_float(u[j] & 0xffff0000u);
+        }
+      } else {
+        const float4 w = __ldg(reinterpret_cast<const float4*>(static_cast<const float*>(logits) + row + v0));
+        x[g * RUN] = w.x;
+        x[g * RUN + 1] = w.y;
+        x[g * RUN + 2] = w.z;
+        x[g * RUN + 3] = w.w;
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < RUN; ++j) {
+        const int v = v0 + j;
+        x[g * RUN + j] = v < hi ? load_elem(logits, row + v, BF16 ? EAGLE_BF16 : EAGLE_F32) : -INFINITY;
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < RUN; ++j) xi[g * RUN + j] = (v0 + j < hi) ? v0 + j : INT_MAX;
+  }
+}
+
 // ------------------------------------------------------------------ chunk pass
-template <bool TOPK>
+template <bool TOPK, bool BF16>
 __global__ void __launch_bounds__(kThreads, 2) tree_chunk_kernel(const TreeBuildPlan p, const BuildArgs a) {
   const int bf = blockIdx.x, c = blockIdx.y;
   const int b = bf / a.F, f = bf % a.F;
@@ -120,15 +164,11 @@ __global__ void __launch_bounds__(kThreads, 2) tree_chunk_kernel(const TreeBuild
   __shared__ float wlv[NW][K];
   __shared__ int wli[NW][K];
 
-  // all loads first: element v = lo + threadIdx.x + kThreads * e (coalesced per e)
+  // all loads first
   float x[kPer];
   int xi[kPer];
-#pragma unroll
-  for (int e = 0; e < kPer; ++e) {
-    const int v = lo + threadIdx.x + kThreads * e;
-    x[e] = v < hi ? load_elem(a.logits, row + v, p.dtype) : -INFINITY;
-    xi[e] = v < hi ? v : INT_MAX;
-  }
+  const bool vec = (reinterpret_cast<uintptr_t>(a.logits) & 15u) == 0 && (p.V % (BF16 ? 8 : 4)) == 0;
+  load_chunk<BF16>(a.logits, row, lo, hi, vec, x, xi);
   // chunk max (two passes over registers: no online rescale)
   float m = x[0];
 #pragma unroll
@@ -155,22 +195,23 @@ __global__ void __launch_bounds__(kThreads, 2) tree_chunk_kernel(const TreeBuild
   }
   ChunkPart* out = parts(p, a.ws) + (static_cast<size_t>(b) * p.f_max + f) * p.n_chunks + c;
   if constexpr (TOPK) {
-    // each thread sorts its K logits; each warp takes its best K by K rounds of warp
-    // argmax over the lanes' list heads; the chunk's best K of the NW warp lists are
-    // found by rank: an entry's rank is the count of entries before it in every list.
+    // each thread sorts its K logits; each warp takes its best kc by kc rounds of warp
+    // argmax over the lanes' list heads (a level takes at most kc tokens of a row, so
+    // at most kc of one chunk); the chunk's best kc of the NW warp lists are found by
+    // rank: an entry's rank is the count of entries before it in every list.
     sort_regs(x, xi);
+    const int kc = p.kc;
 #pragma unroll 1
-    for (int r = 0; r < K; ++r) {
+    for (int r = 0; r < kc; ++r) {
       float bv = x[0];
       int bi = xi[0];
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) {
         const float v2 = __shfl_xor_sync(0xffffffffu, bv, o);
         const int i2 = __shfl_xor_sync(0xffffffffu, bi, o);
-        if (before(v2, i2, bv, bi)) {
-          bv = v2;
-          bi = i2;
-        }
+        const bool tk = before_nb(v2, i2, bv, bi);
+        bv = tk ? v2 : bv;
+        bi = tk ? i2 : bi;
       }
       if (lane == 0) {
         wlv[warp][r] = bv;
@@ -185,6 +226,10 @@ __global__ void __launch_bounds__(kThreads, 2) tree_chunk_kernel(const TreeBuild
         x[K - 1] = -INFINITY;
         xi[K - 1] = INT_MAX;
       }
+    }
+    for (int r = kc + lane; r < K; r += 32) {  // the warp list past kc: empty
+      wlv[warp][r] = -INFINITY;
+      wli[warp][r] = INT_MAX;
     }
     if (threadIdx.x < K) {  // slots no real entry reaches stay empty
       out->tv[threadIdx.x] = -INFINITY;
@@ -209,16 +254,16 @@ __global__ void __launch_bounds__(kThreads, 2) tree_chunk_kernel(const TreeBuild
       const int ci = wli[w0][r0];
       if (ci != INT_MAX) {
         int rank = r0;
+#pragma unroll
         for (int w = 0; w < NW; ++w) {
-          if (w == w0) continue;
           int n = 0;  // entries of list w before (cv, ci): binary search of a sorted list
 #pragma unroll
           for (int step = K / 2; step > 0; step >>= 1)
-            if (before(wlv[w][n + step - 1], wli[w][n + step - 1], cv, ci)) n += step;
-          if (n == K - 1 && before(wlv[w][K - 1], wli[w][K - 1], cv, ci)) n = K;
-          rank += n;
+            n += before_nb(wlv[w][n + step - 1], wli[w][n + step - 1], cv, ci) ? step : 0;
+          n += (n == K - 1 && before_nb(wlv[w][K - 1], wli[w][K - 1], cv, ci)) ? 1 : 0;
+          rank += (w == w0) ? 0 : n;
         }
-        if (rank < K) {
+        if (rank < p.kc) {
           out->tv[rank] = cv;
           out->ti[rank] = ci;
         }
@@ -275,11 +320,38 @@ __device__ void block_flag_ranks(int* fr, int n, int* s_cnt) {
   __syncthreads();
 }
 
-// ln z for a float-float z > 0, as float-float (one double log).
+// Float-float constants split on the host: hi = the nearest float, lo = the rest.
+constexpr float split_hi(double d) { return static_cast<float>(d); }
+constexpr float split_lo(double d) { return static_cast<float>(d - static_cast<double>(static_cast<float>(d))); }
+constexpr double kLn2 = 0.693147180559945309417232121458;
+__constant__ float kLogSeries[9][2] = {
+    {split_hi(1.0), split_lo(1.0)},           {split_hi(1.0 / 3), split_lo(1.0 / 3)},
+    {split_hi(1.0 / 5), split_lo(1.0 / 5)},   {split_hi(1.0 / 7), split_lo(1.0 / 7)},
+    {split_hi(1.0 / 9), split_lo(1.0 / 9)},   {split_hi(1.0 / 11), split_lo(1.0 / 11)},
+    {split_hi(1.0 / 13), split_lo(1.0 / 13)}, {split_hi(1.0 / 15), split_lo(1.0 / 15)},
+    {split_hi(1.0 / 17), split_lo(1.0 / 17)}};
+__constant__ float kLn2Split[2] = {split_hi(kLn2), split_lo(kLn2)};
+
+// ln z for a float-float z > 0 (finite, normal), as float-float, on the fp32 pipe.
+// z = 2^k w with w in [1/sqrt 2, sqrt 2); ln z = k ln 2 + ln w and, with
+// t = (w - 1) / (w + 1) (|t| < 0.172), ln w = 2 atanh t = 2 (t + t^3/3 + t^5/5 + ...);
+// the series stops after t^17 (remainder below 1e-15 of ln w).
 __device__ __forceinline__ ff ff_log(ff z) {
-  const double d = log(static_cast<double>(z.hi) + static_cast<double>(z.lo));
-  const float h = static_cast<float>(d);
-  return ff{h, static_cast<float>(d - static_cast<double>(h))};
+  int e;
+  float w_hi = frexpf(z.hi, &e);  // z.hi = w_hi 2^e, w_hi in [0.5, 1)
+  int k = e;
+  if (w_hi < 0.70710678f) {
+    w_hi *= 2.f;
+    k -= 1;
+  }
+  const ff w = ff{w_hi, ldexpf(z.lo, -k)};
+  const ff t = ff_div(ff_add(w, -1.f), ff_add(w, 1.f));
+  const ff t2 = ff_mul(t, t);
+  ff sum = ff{kLogSeries[8][0], kLogSeries[8][1]};
+#pragma unroll
+  for (int i = 7; i >= 0; --i) sum = ff_add(ff_mul(sum, t2), ff{kLogSeries[i][0], kLogSeries[i][1]});
+  const ff lnw = ff_mul(ff_mul(t, sum), 2.f);
+  return ff_add(ff_mul(ff{kLn2Split[0], kLn2Split[1]}, static_cast<float>(k)), lnw);
 }
 
 // Row statistics merged over chunks by one warp: M, ln Z (T = 1) and the mass at
@@ -546,24 +618,25 @@ __global__ void __launch_bounds__(kThreads, 1) tree_select_kernel(const TreeBuil
     }
     __syncthreads();
     const int n_new = a.F * k;
-    // next frontier: best k of the new candidates, kept in pool order
-    int n2 = 1;
-    while (n2 < n_new) n2 <<= 1;
-    for (int j = threadIdx.x; j < n2; j += kThreads) {
-      skey[j] = j < n_new ? psc[base + j] : ff_make(-INFINITY);
-      sidx[j] = j < n_new ? base + j : INT_MAX;
+    // next frontier: best k of the new candidates, kept in pool order.  A candidate's
+    // rank is the number of candidates before it by (score desc, pool index asc).
+    for (int j = threadIdx.x; j < n_new; j += kThreads) skey[j] = psc[base + j];
+    __syncthreads();
+    for (int j = threadIdx.x; j < n_new; j += kThreads) {
+      const ff kj = skey[j];
+      int r = 0;
+      for (int i = 0; i < n_new; ++i) r += before_ff(skey[i], i, kj, j) ? 1 : 0;
+      if (r == k - 1 || r == k) sidx[r - (k - 1)] = j;  // the two candidates at the boundary
+      srow[j] = r < k ? 1 : 0;
     }
     __syncthreads();
-    bitonic_sort(skey, sidx, n2);
     // a near-tie at the boundary, unless it is an exact tie between siblings (same
     // parent, same logit), which both sides break by pool index
-    if (threadIdx.x == 0 && n_new > k && ff_float(ff_sub(skey[k - 1], skey[k])) < kNearTieEps &&
-        !(ff_eq(skey[k - 1], skey[k]) && ppar[sidx[k - 1]] == ppar[sidx[k]]))
-      s_near += 1;
-    for (int j = threadIdx.x; j < n_new; j += kThreads) srow[j] = 0;
-    __syncthreads();
-    for (int j = threadIdx.x; j < k; j += kThreads) srow[sidx[j] - base] = 1;
-    __syncthreads();
+    if (threadIdx.x == 0 && n_new > k) {
+      const ff ka = skey[sidx[0]], kb = skey[sidx[1]];
+      if (ff_float(ff_sub(ka, kb)) < kNearTieEps && !(ff_eq(ka, kb) && ppar[base + sidx[0]] == ppar[base + sidx[1]]))
+        s_near += 1;
+    }
     block_flag_ranks(srow, n_new, s_cnt);
     for (int j = threadIdx.x; j < n_new; j += kThreads) {
       const int slot = srow[j];
@@ -584,7 +657,7 @@ __global__ void __launch_bounds__(kThreads, 1) tree_select_kernel(const TreeBuil
     // ---- last level: best N of the pool, rows in pool order
     const int np = base + n_new;
     const int N = p.N;
-    n2 = 1;
+    int n2 = 1;
     while (n2 < np) n2 <<= 1;
     for (int j = threadIdx.x; j < n2; j += kThreads) {
       skey[j] = j < np ? psc[j] : ff_make(-INFINITY);
@@ -731,6 +804,7 @@ void plan_tree_build(const eagle_tree_desc* d, TreeBuildPlan* p) {
     p->N = d->total_tokens;
     p->R = d->total_tokens + 1;
     p->f_max = d->top_k;
+    p->kc = d->top_k;
     p->pool_cap = d->top_k + (d->depth - 1) * d->top_k * d->top_k;
     p->shape.rows = 0;
   } else {
@@ -756,6 +830,13 @@ void plan_tree_build(const eagle_tree_desc* d, TreeBuildPlan* p) {
       if (c > fmax) fmax = c;
     }
     p->f_max = fmax;
+    int kmax = 1;  // most children of one node
+    for (int i = 0; i < p->R; ++i) {
+      int c = 0;
+      for (int j = i + 1; j < p->R; ++j) c += (p->shape.parent[j] == i);
+      if (c > kmax) kmax = c;
+    }
+    p->kc = kmax < K ? kmax : K;
   }
   p->W = (p->R + 63) / 64;
   size_t off = 0;
@@ -802,10 +883,18 @@ cudaError_t launch_tree_build(const TreeBuildPlan& p, int level, const void* log
   a.level = level;
   a.F = frontier_rows(p, level);
   dim3 grid(p.B * a.F, p.n_chunks);
-  if (p.mode == EAGLE_TREE_STATIC_SAMPLED)
-    tree_chunk_kernel<false><<<grid, kThreads, 0, s>>>(p, a);
-  else
-    tree_chunk_kernel<true><<<grid, kThreads, 0, s>>>(p, a);
+  const bool bf16 = p.dtype != EAGLE_F32;
+  if (p.mode == EAGLE_TREE_STATIC_SAMPLED) {
+    if (bf16)
+      tree_chunk_kernel<false, true><<<grid, kThreads, 0, s>>>(p, a);
+    else
+      tree_chunk_kernel<false, false><<<grid, kThreads, 0, s>>>(p, a);
+  } else {
+    if (bf16)
+      tree_chunk_kernel<true, true><<<grid, kThreads, 0, s>>>(p, a);
+    else
+      tree_chunk_kernel<true, false><<<grid, kThreads, 0, s>>>(p, a);
+  }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   tree_select_kernel<<<p.B, kThreads, 0, s>>>(p, a);
