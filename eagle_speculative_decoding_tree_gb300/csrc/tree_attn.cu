@@ -39,6 +39,7 @@ struct AttnArgs {
   float* part_o;   // [B*Hkv][splits][rows_pad][D]
   float* part_ml;  // [B*Hkv][splits][rows_pad][2]
   int B, R, Hq, Hkv, G, P, W, splits, rows_pad;
+  int tps;         // > 0: fixed-size splits of tps 128-key units (tcgen05 partials)
   int out_f32;     // 1: write fp32 output rows
   float scale, scale_log2;
 };
@@ -362,17 +363,26 @@ __global__ void __launch_bounds__(128) tree_attn_combine_kernel(const AttnArgs a
   const size_t base = static_cast<size_t>(bh) * a.splits * a.rows_pad + r;
   const size_t sstride = static_cast<size_t>(a.rows_pad) * D;
   const float* po0 = a.part_o + base * D + lane * PER;
+  // splits that hold units of this request (fixed-size splits: ceil(U / tps) of them,
+  // U = its 128-key prefix tiles + the tree tile); the rest wrote nothing
+  int n_act = a.splits;
+  if (a.tps > 0) {
+    int L = a.seq_len[b];
+    L = L < 0 ? 0 : (L > a.P ? a.P : L);
+    const int U = (L + 127) / 128 + 1;
+    n_act = min(a.splits, (U + a.tps - 1) / a.tps);
+  }
   float2 ml[2];
 #pragma unroll
   for (int k = 0; k < 2; ++k) {
     const int s = lane + 32 * k;
-    ml[k] = s < a.splits ? *reinterpret_cast<const float2*>(a.part_ml + (base + static_cast<size_t>(s) * a.rows_pad) * 2)
-                         : make_float2(-INFINITY, 0.f);
+    ml[k] = s < n_act ? *reinterpret_cast<const float2*>(a.part_ml + (base + static_cast<size_t>(s) * a.rows_pad) * 2)
+                      : make_float2(-INFINITY, 0.f);
   }
   float v[BATCH][PER];
 #pragma unroll
   for (int u = 0; u < BATCH; ++u) {
-    if (u < a.splits) {
+    if (u < n_act) {
       const float* po = po0 + static_cast<size_t>(u) * sstride;
       if constexpr (PER == 4) {
         const float4 t = *reinterpret_cast<const float4*>(po);
@@ -404,13 +414,13 @@ __global__ void __launch_bounds__(128) tree_attn_combine_kernel(const AttnArgs a
 #pragma unroll
     for (int e = 0; e < PER; ++e) acc[e] = fmaf(w, v[u][e], acc[e]);
   }
-  for (int s0 = BATCH; s0 < a.splits; s0 += 8) {  // splits beyond 32: eight at a time
+  for (int s0 = BATCH; s0 < n_act; s0 += 8) {  // splits beyond 32: eight at a time
     float x[8][PER], wv[8];
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
       const int s = s0 + u;
       wv[u] = __shfl_sync(0xffffffffu, w2[1], s & 31);
-      const bool in = s < a.splits;
+      const bool in = s < n_act;
       const float* po = po0 + static_cast<size_t>(in ? s : 0) * sstride;
 #pragma unroll
       for (int e = 0; e < PER; ++e) x[u][e] = in ? po[e] : 0.f;
@@ -523,6 +533,8 @@ void plan_tree_attn(const eagle_attn_desc* d, int num_sms, AttnPlan* p) {
   p->tc = false;
   p->coop = false;
   p->part_bf16 = false;
+  p->tps = 0;
+  p->lpt = false;
   const int RG = p->R * p->G;
   if (p->dtype == EAGLE_F32) {
     p->rows_per_cta = 4;
@@ -553,11 +565,26 @@ void plan_tree_attn(const eagle_attn_desc* d, int num_sms, AttnPlan* p) {
   if (splits > max_tiles) splits = max_tiles;
   if (splits > 64) splits = 64;
   if (splits < 1) splits = 1;
-  p->splits = splits;
   // tcgen05 with splits: when the whole grid fits on the SMs at once (one CTA per SM)
   // the kernel merges the partials itself (cooperative launch); else the combine
   // kernel does.
   p->coop = p->tc && splits > 1 && static_cast<long long>(base) * splits <= num_sms;
+  if (p->tc && !p->coop && d->num_splits <= 0) {
+    // more groups than a cooperative grid holds (batched, ragged requests): each
+    // request's key range is cut into fixed pieces of T 128-key units (the tree tile
+    // counts as one), so a long request spreads over several CTAs and a short one
+    // takes few; T = 16 while the groups alone fill under two waves of SMs, else 32.
+    // The longest requests are dispatched first.
+    const int T = (base < 2 * num_sms) ? 16 : 32;
+    const int units = max_tiles + 1;
+    const int s2 = (units + T - 1) / T;
+    if (s2 > 1 && s2 <= 64) {
+      splits = s2;
+      p->tps = T;
+    }
+    p->lpt = p->B > 1;
+  }
+  p->splits = splits;
   // the kernel's own merge keeps partial O in bf16 unless the precise mode was asked for
   p->part_bf16 = p->coop && !p->precise;
   size_t off = p->tc ? 256 : 0;  // tcgen05: error word first
@@ -575,9 +602,11 @@ void plan_tree_attn(const eagle_attn_desc* d, int num_sms, AttnPlan* p) {
   p->total = off;
 }
 
-cudaError_t launch_tree_attn_combine(const AttnPlan& p, void* out, float* lse, const float* part_o,
-                                     const float* part_ml, cudaStream_t s) {
+cudaError_t launch_tree_attn_combine(const AttnPlan& p, const int32_t* seq_len, void* out, float* lse,
+                                     const float* part_o, const float* part_ml, cudaStream_t s) {
   AttnArgs a{};
+  a.seq_len = seq_len;
+  a.tps = p.tps;
   a.out = out;
   a.lse = lse;
   a.part_o = const_cast<float*>(part_o);
@@ -643,6 +672,7 @@ cudaError_t launch_tree_attn(const AttnPlan& p, const void* q, const void* k_cac
   a.W = p.W;
   a.splits = p.splits;
   a.rows_pad = p.rows_pad;
+  a.tps = 0;
   a.scale = p.scale;
   a.scale_log2 = p.scale * kLog2e;
   const int nw = p.rows_per_cta / 16;

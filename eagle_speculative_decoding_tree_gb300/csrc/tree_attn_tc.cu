@@ -77,6 +77,9 @@ struct TcArgs {
   int* err;
   int B, R, Hq, Hkv, G, P, W, splits, rows_pad, rows_per_cta, n_mt, out_f32;
   int coop;        // 1: the splits of a group merge their partials in this kernel
+  int tps;         // > 0: split s takes tile units [s tps, (s + 1) tps) of its request
+                   //      (splits past a request's last unit do nothing); 0: even splits
+  int lpt;         // 1: the request index of the grid is a rank in decreasing sequence length
   int* cnt;        // coop: [2][n_groups] published / finished splits per (request, KV head, row block)
   int n_groups;
   float scale, scale_log2;
@@ -95,21 +98,52 @@ struct TileInfo {
   int n_pt, t_begin, n_tiles, L;
 };
 
+__device__ __forceinline__ int clamp_len(const TcArgs& a, int L) { return L < 0 ? 0 : (L > a.P ? a.P : L); }
+
 __device__ __forceinline__ TileInfo tile_info(const TcArgs& a, int b, int split) {
   TileInfo ti;
-  int L = a.seq_len[b];
-  L = L < 0 ? 0 : (L > a.P ? a.P : L);
+  const int L = clamp_len(a, a.seq_len[b]);
   // units of work: the prefix tiles, then the tree tile; split s takes units
-  // [U s / S, U (s + 1) / S), so only the last split holds the tree tile
+  // [U s / S, U (s + 1) / S) (or [s tps, (s + 1) tps) when tps > 0), so only the last
+  // split that has units holds the tree tile
   const int n_pref = (L + KT - 1) / KT;
   const int U = n_pref + 1;
-  const int u0 = static_cast<int>(static_cast<long long>(U) * split / a.splits);
-  const int u1 = static_cast<int>(static_cast<long long>(U) * (split + 1) / a.splits);
+  int u0, u1;
+  if (a.tps > 0) {
+    u0 = min(U, split * a.tps);
+    u1 = min(U, u0 + a.tps);
+  } else {
+    u0 = static_cast<int>(static_cast<long long>(U) * split / a.splits);
+    u1 = static_cast<int>(static_cast<long long>(U) * (split + 1) / a.splits);
+  }
   ti.t_begin = u0;
   ti.n_pt = max(0, min(u1, n_pref) - u0);
   ti.n_tiles = u1 - u0;
   ti.L = L;
   return ti;
+}
+
+// The request of rank r when the requests are ordered by decreasing sequence length
+// (ties: lower index first).  Warp-collective; every lane returns the same value.
+__device__ int request_of_rank(const TcArgs& a, int r) {
+  const int lane = threadIdx.x & 31;
+  int res = 0;
+  for (int j0 = 0; j0 < a.B; j0 += 32) {
+    const int j = j0 + lane;
+    const int Lj = j < a.B ? clamp_len(a, a.seq_len[j]) : -1;
+    int rank = 0;
+    for (int i0 = 0; i0 < a.B; i0 += 32) {
+      const int own = (i0 + lane < a.B) ? clamp_len(a, a.seq_len[i0 + lane]) : -1;
+      for (int k = 0; k < 32; ++k) {
+        const int i = i0 + k;
+        const int Li = __shfl_sync(0xffffffffu, own, k);
+        rank += (i < a.B && (Li > Lj || (Li == Lj && i < j))) ? 1 : 0;
+      }
+    }
+    const unsigned m = __ballot_sync(0xffffffffu, j < a.B && rank == r);
+    if (m) res = j0 + __ffs(m) - 1;
+  }
+  return res;
 }
 
 // Valid keys of tile t (prefix keys before L; tree rows before R).
@@ -308,8 +342,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   __shared__ float s_l[2][2][128];        // [M-tile][key half][row] half-row sums
   __shared__ int s_go;                    // group merge: every split published in time
 
-  const int split = blockIdx.x, bh = blockIdx.y, rb = blockIdx.z;
-  const int b = bh / a.Hkv, h = bh % a.Hkv;
+  // grid: cooperative (splits, B Hkv, row blocks); otherwise (row blocks, splits, B Hkv),
+  // so that the row blocks of one key range, which read the same K/V tiles, are
+  // dispatched next to each other and share them through L2
+  const int split = a.coop ? blockIdx.x : blockIdx.y;
+  const int rb = a.coop ? blockIdx.z : blockIdx.x;
+  const int ybh = a.coop ? blockIdx.y : blockIdx.z;
+  const int h = ybh % a.Hkv;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n_mt = a.n_mt;
 
@@ -348,18 +387,26 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   // stream until it completes
   griddep_wait();
   griddep_launch_dependents();
+  // the request: ybh / Hkv, or (lpt) the request of that rank by decreasing length, so
+  // that the longest requests' CTAs are dispatched first
+  const int b = a.lpt ? request_of_rank(a, ybh / a.Hkv) : ybh / a.Hkv;
+  const int bh = b * a.Hkv + h;
   uint8_t* sQ = smem + SM_Q;
-  // Q does not depend on the sequence length: its load goes out before seq_len is read
-  // (the MMA warp always waits for it, so no copy is in flight at exit)
-  if (warp == 8 && lane == 0) {
+  auto load_q = [&]() {
     mbar_arrive_expect_tx(&bar_q, n_mt * TILE);
     for (int i = 0; i < n_mt; ++i) {
       const int node0 = (rb * a.rows_per_cta + i * 128) / a.G;
       for (int hh = 0; hh < 2; ++hh)
         tma_load_3d(sQ + i * TILE + hh * HALF, &tm.q, 64 * hh, h * a.G, b * a.R + node0, &bar_q);
     }
-  }
+  };
+  // Q does not depend on the sequence length: with even splits its load goes out before
+  // seq_len is read; with fixed-size splits only a CTA that has tiles loads it.  The MMA
+  // warp waits for every Q load, so no copy is in flight at exit.
+  if (a.tps == 0 && warp == 8 && lane == 0) load_q();
   const TileInfo ti = tile_info(a, b, split);
+  const bool q_loaded = a.tps == 0 || ti.n_tiles > 0;
+  if (a.tps > 0 && q_loaded && warp == 8 && lane == 0) load_q();
   const uint32_t tb = tmem_base;
 
   if (warp == 8) {
@@ -387,7 +434,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     // S of tile t goes to TMEM buffer t & 1: QK(0) QK(1) | PV(0) QK(2) | PV(1) QK(3) | ...
     // so the tensor cores compute the next-but-one S while the softmax works on this one.
     bool ok = true;
-    if (lane == 0) ok = wait_parity(&bar_q, 0, a.err, ERR_Q);
+    if (lane == 0 && q_loaded) ok = wait_parity(&bar_q, 0, a.err, ERR_Q);
     ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0 && ti.n_tiles > 0;
     auto qk = [&](int t) {  // lane 0; K stage t % KST, S buffer t & 1
       const int s = t % KST;
@@ -662,7 +709,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           *reinterpret_cast<float2*>(a.part_ml + prow * 2) = make_float2(m_ref[i], l_tot[i]);
         }
       }
-    } else {
+    } else if (!(a.tps > 0 && ti.n_tiles == 0)) {  // a split past its request's last unit writes nothing
 #pragma unroll
       for (int i = 0; i < 2; ++i) {
         if (i >= n_mt) break;
@@ -895,16 +942,18 @@ cudaError_t launch_tree_attn_tc(const AttnPlan& p, const void* q, const void* k_
   a.rows_per_cta = p.rows_per_cta;
   a.n_mt = p.rows_per_cta / 128;
   a.coop = p.coop ? 1 : 0;
+  a.tps = p.tps;
+  a.lpt = p.lpt ? 1 : 0;
   a.cnt = p.coop ? reinterpret_cast<int*>(w + p.off_cnt) : nullptr;
   a.n_groups = p.B * p.Hkv * p.row_blocks;
   a.out_f32 = p.out_dtype == EAGLE_F32;
   a.scale = p.scale;
   a.scale_log2 = p.scale * kLog2e;
   cudaError_t e;
-  dim3 grid(p.splits, p.B * p.Hkv, p.row_blocks);
+  const dim3 grid = p.coop ? dim3(p.splits, p.B * p.Hkv, p.row_blocks) : dim3(p.row_blocks, p.splits, p.B * p.Hkv);
   e = p.precise ? launch_tc<true>(tm, a, grid, s) : launch_tc<false>(tm, a, grid, s);
   if (e != cudaSuccess || !partials || p.coop) return e;
-  return launch_tree_attn_combine(p, out, lse, static_cast<const float*>(a.part_o), a.part_ml, s);
+  return launch_tree_attn_combine(p, seq_len, out, lse, static_cast<const float*>(a.part_o), a.part_ml, s);
 }
 
 }  // namespace eagle

@@ -109,6 +109,45 @@ __device__ __forceinline__ void sort_regs(float (&v)[K], int (&id)[K]) {
   }
 }
 
+// Order-preserving unsigned images of floats (-0 taken as +0, so equal floats map to
+// equal keys): a larger key is a larger value.
+__device__ __forceinline__ uint32_t ord32(float f) {
+  uint32_t u = __float_as_uint(f);
+  u = (u == 0x80000000u) ? 0u : u;
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float unord32(uint32_t o) {
+  return __uint_as_float((o & 0x80000000u) ? (o & 0x7fffffffu) : ~o);
+}
+// The same for a bf16 value (its 16 bits), and back.
+__device__ __forceinline__ uint32_t ord16(uint32_t b) {
+  b = (b == 0x8000u) ? 0u : b;
+  return (b & 0x8000u) ? (~b & 0xffffu) : (b | 0x8000u);
+}
+__device__ __forceinline__ float unord16(uint32_t o) {
+  return __uint_as_float(((o & 0x8000u) ? (o & 0x7fffu) : (~o & 0xffffu)) << 16);
+}
+
+// Descending sorting network over K packed keys in registers.
+__device__ __forceinline__ void sort_keys(uint32_t (&k)[K]) {
+#pragma unroll
+  for (int s = 2; s <= K; s <<= 1) {
+#pragma unroll
+    for (int j = s >> 1; j > 0; j >>= 1) {
+#pragma unroll
+      for (int i = 0; i < K; ++i) {
+        const int l = i ^ j;
+        if (l > i) {
+          const uint32_t a = k[i], b = k[l];
+          const bool first = (i & s) == 0;  // i takes the larger key
+          k[i] = first ? max(a, b) : min(a, b);
+          k[l] = first ? min(a, b) : max(a, b);
+        }
+      }
+    }
+  }
+}
+
 // A thread's kPer logits of the chunk [lo, hi) and their ids (-inf / INT_MAX past hi):
 // bf16 as two runs of 8 (lo + 2048 g + 8 t ..), fp32 as four runs of 4 (lo + 1024 g +
 // 4 t ..), each run one 16-byte load when `vec` (the row base is 16-byte aligned).
@@ -163,6 +202,7 @@ __global__ void __launch_bounds__(kThreads, 2) tree_chunk_kernel(const TreeBuild
   __shared__ ff ss1[NW], ssT[NW];
   __shared__ float wlv[NW][K];
   __shared__ int wli[NW][K];
+  __shared__ uint32_t wlk[NW][K];
 
   // all loads first
   float x[kPer];
@@ -194,7 +234,34 @@ __global__ void __launch_bounds__(kThreads, 2) tree_chunk_kernel(const TreeBuild
     ssT[warp] = dT;
   }
   ChunkPart* out = parts(p, a.ws) + (static_cast<size_t>(b) * p.f_max + f) * p.n_chunks + c;
-  if constexpr (TOPK) {
+  if constexpr (TOPK && BF16) {
+    // bf16: one 32-bit key per logit, (order-preserving bf16 bits << 12) | (4095 -
+    // offset in the chunk): a larger key is a larger logit, or an equal one with a
+    // lower id; 0 = empty.  Each thread sorts its keys, each warp takes its best kc by
+    // kc rounds of a warp max (redux) over the list heads, and the chunk's best kc of
+    // the warp lists are found by rank, as on the fp32 path below.
+    uint32_t key[K];
+#pragma unroll
+    for (int e = 0; e < kPer; ++e)
+      key[e] = (xi[e] == INT_MAX) ? 0u : ((ord16(__float_as_uint(x[e]) >> 16) << 12) | (4095u - (xi[e] - lo)));
+    sort_keys(key);
+    const int kc = p.kc;
+#pragma unroll 1
+    for (int r = 0; r < kc; ++r) {
+      const uint32_t best = __reduce_max_sync(0xffffffffu, key[0]);
+      if (lane == 0) wlk[warp][r] = best;
+      if (best != 0u && key[0] == best) {  // the owner pops its head
+#pragma unroll
+        for (int j = 0; j < K - 1; ++j) key[j] = key[j + 1];
+        key[K - 1] = 0u;
+      }
+    }
+    for (int r = kc + lane; r < K; r += 32) wlk[warp][r] = 0u;
+    if (threadIdx.x < K) {
+      out->tv[threadIdx.x] = -INFINITY;
+      out->ti[threadIdx.x] = INT_MAX;
+    }
+  } else if constexpr (TOPK) {
     // each thread sorts its K logits; each warp takes its best kc by kc rounds of warp
     // argmax over the lanes' list heads (a level takes at most kc tokens of a row, so
     // at most kc of one chunk); the chunk's best kc of the NW warp lists are found by
@@ -247,7 +314,27 @@ __global__ void __launch_bounds__(kThreads, 2) tree_chunk_kernel(const TreeBuild
     out->s1 = t1;
     out->sT = tT;
   }
-  if constexpr (TOPK) {
+  if constexpr (TOPK && BF16) {
+    if (threadIdx.x < NW * K) {
+      const int w0 = threadIdx.x / K, r0 = threadIdx.x % K;
+      const uint32_t ck = wlk[w0][r0];
+      if (ck != 0u) {
+        int rank = r0;
+#pragma unroll
+        for (int w = 0; w < NW; ++w) {
+          int n = 0;  // keys of list w above ck: binary search of a descending list
+#pragma unroll
+          for (int step = K / 2; step > 0; step >>= 1) n += (wlk[w][n + step - 1] > ck) ? step : 0;
+          n += (n == K - 1 && wlk[w][K - 1] > ck) ? 1 : 0;
+          rank += (w == w0) ? 0 : n;
+        }
+        if (rank < p.kc) {
+          out->tv[rank] = unord16(ck >> 12);
+          out->ti[rank] = lo + 4095 - static_cast<int>(ck & 4095u);
+        }
+      }
+    }
+  } else if constexpr (TOPK) {
     if (threadIdx.x < NW * K) {
       const int w0 = threadIdx.x / K, r0 = threadIdx.x % K;
       const float cv = wlv[w0][r0];
@@ -413,22 +500,17 @@ __device__ void merge_topk(const ChunkPart* cp, int n_chunks, int cnt, int* tok,
       }
     }
     for (int r = 0; r < cnt; ++r) {
-      float bv = lv[0];
-      int bi = li[0];
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        const float v2 = __shfl_xor_sync(0xffffffffu, bv, o);
-        const int i2 = __shfl_xor_sync(0xffffffffu, bi, o);
-        if (before(v2, i2, bv, bi)) {
-          bv = v2;
-          bi = i2;
-        }
-      }
+      // the best head: the largest value (warp max of its order-preserving image), then
+      // among equal values the lowest id
+      const uint32_t kv = ord32(lv[0]);
+      const uint32_t best = __reduce_max_sync(0xffffffffu, kv);
+      const uint32_t bid = __reduce_min_sync(0xffffffffu, kv == best ? static_cast<uint32_t>(li[0]) : 0xffffffffu);
+      const int bi = static_cast<int>(bid);
       if (lane == 0) {
         tok[r] = bi;
-        val[r] = bv;
+        val[r] = unord32(best);
       }
-      if (bi != INT_MAX && li[0] == bi) {  // the owner pops its head
+      if (bi != INT_MAX && kv == best && li[0] == bi) {  // the owner pops its head
 #pragma unroll
         for (int j = 0; j < K - 1; ++j) {
           lv[j] = lv[j + 1];

@@ -120,6 +120,17 @@ def test_tree_attention_ragged_batch():
     _check(w, 5, seq_len, 61, par, mask, [(b, b % 8) for b in range(5)])
 
 
+def test_tree_attention_ragged_fixed_splits():
+    """More (request, KV head, row block) groups than SMs: fixed-size key splits of 16
+    tiles per CTA, requests dispatched longest first, one request with no prefix."""
+    w = W["concurrency"].with_(prefix=2500, prefix_min=1, batch=10)
+    seq_len = synth.prefix_lengths(w, 10)
+    seq_len[3] = 0
+    seq_len[6] = 2500
+    par, mask = random_tree(61, seed=17)
+    _check(w, 10, seq_len, 61, par, mask, [(0, 1), (3, 5), (6, 7), (9, 0)])
+
+
 @pytest.mark.parametrize("name", ["vicuna7b", "llama8b", "long128k"])
 def test_tree_attention_full_size(name):
     """The benchmark's shapes and launch configuration; whole KV heads checked."""
