@@ -39,12 +39,6 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
-__device__ __forceinline__ double warp_sum_d(double v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  return v;
-}
-
 // Neumaier-compensated fp32 accumulation (Neumaier 1974): a running sum and the
 // rounding error it has dropped, so a thread's partial sum is exact to ~1 ulp.
 struct CSum {
@@ -58,7 +52,6 @@ struct CSum {
     s *= f;
     c *= f;
   }
-  __device__ __forceinline__ double total() const { return static_cast<double>(s) + static_cast<double>(c); }
 };
 
 // ------------------------------------------------------------------ float-float
@@ -142,9 +135,6 @@ __device__ __forceinline__ ff csum_ff(const CSum& a) { return two_sum(a.s, a.c);
 
 // (value desc, index asc) order: true if (va, ia) comes before (vb, ib).
 __device__ __forceinline__ bool before(float va, int ia, float vb, int ib) {
-  return va > vb || (va == vb && ia < ib);
-}
-__device__ __forceinline__ bool before(double va, int ia, double vb, int ib) {
   return va > vb || (va == vb && ia < ib);
 }
 
