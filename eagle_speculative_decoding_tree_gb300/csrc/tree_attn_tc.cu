@@ -516,13 +516,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         if (i >= n_mt) break;
         const bool got = __all_sync(0xffffffffu, wait_parity(&s_full[t & 1], (t >> 1) & 1, a.err, ERR_S));
         tc_fence_after();
-        // pass 1: max of this half's 64 scores over the kept keys
+        // the max of this half's 64 scores over the kept keys
         const uint32_t k0 = !vrow[i] ? 0u : (tree ? tw[i][0] : low_bits(nv - 64 * hf));
         const uint32_t k1 = !vrow[i] ? 0u : (tree ? tw[i][1] : low_bits(nv - 64 * hf - 32));
         const bool full = __all_sync(0xffffffffu, (k0 & k1) == 0xffffffffu);
+        // S of this half-row stays in registers from the max to the exponentials
         float mx = -INFINITY;
+        uint32_t s0[32], s1[32];
         if (got) {
-          uint32_t s0[32], s1[32];
           tmem_ld32(lb + col_s(t & 1) + 64 * hf, s0);
           tmem_ld32(lb + col_s(t & 1) + 64 * hf + 32, s1);
           tmem_ld_wait();
@@ -567,11 +568,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
         if (move) m_ref[i] = m_new;
         const float mu = (m_ref[i] == -INFINITY) ? 0.f : m_ref[i] * sl2;
-        // pass 2: S again from TMEM, P = 2^(s c - m c) as bf16 pairs (masked keys hold
+        // P = 2^(s c - m c) from the S held in registers, as bf16 pairs (masked keys hold
         // -inf and give exactly 0): keys 64 hf + 32 c .. + 31 go to columns
         // 64 hf + 16 c .. + 15; the precise path puts the low parts 32 columns further
-        // on.  Both chunks are read before either is written.  l sums the fp32 p (the
-        // precise path: hi + lo).
+        // on.  l sums the fp32 p (the precise path: hi + lo).
         float ls[4] = {0.f, 0.f, 0.f, 0.f};
         uint64_t ls2[2] = {0ull, 0ull};  // standard path: packed row-sum accumulators
         const uint64_t sl2x2 = f32x2(__float_as_uint(sl2), __float_as_uint(sl2));
@@ -608,18 +608,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             tmem_st16(lb + col_s(t & 1) + 64 * hf + 32 + 16 * c, lo);
           }
         };
-        {
-          uint32_t s0[32], s1[32];
-          tmem_ld32(lb + col_s(t & 1) + 64 * hf, s0);
-          tmem_ld32(lb + col_s(t & 1) + 64 * hf + 32, s1);
-          tmem_ld_wait();
-          if (!full) {
-            mask_keys(s0, k0);
-            mask_keys(s1, k1);
-          }
-          emit(s0, 0);
-          emit(s1, 1);
-        }
+        emit(s0, 0);
+        emit(s1, 1);
         if constexpr (!PRECISE) {
           float a0, a1, b0, b1;
           f32x2_split(ls2[0], a0, a1);
