@@ -573,9 +573,9 @@ void plan_tree_attn(const eagle_attn_desc* d, int num_sms, AttnPlan* p) {
     // more groups than a cooperative grid holds (batched, ragged requests): each
     // request's key range is cut into fixed pieces of T 128-key units (the tree tile
     // counts as one), so a long request spreads over several CTAs and a short one
-    // takes few; T = 16 while the groups alone fill under two waves of SMs, else 32.
+    // takes few; T = 32 while the groups alone fill under two waves of SMs, else 64.
     // The longest requests are dispatched first.
-    const int T = (base < 2 * num_sms) ? 16 : 32;
+    const int T = (base < 2 * num_sms) ? 32 : 64;
     const int units = max_tiles + 1;
     const int s2 = (units + T - 1) / T;
     if (s2 > 1 && s2 <= 64) {

@@ -181,8 +181,8 @@ def test_binding_refuses_cpu_tensors(lib):
     (dict(), 9, 1),                                                       # llama8b: 16 groups x 9 splits, one wave
     (dict(n_kv_heads=32, max_seq=2048 + 61), 4, 1),                       # vicuna7b (MHA): 32 groups x 4
     (dict(rows=8, max_seq=131072 + 8), 19, 1),                            # long128k chain: 8 groups x 19
-    (dict(batch=8, max_seq=16384), 9, 2),                                 # 128 groups: 16-tile splits + combine
-    (dict(batch=32, max_seq=16384), 5, 2),                                # 512 groups: 32-tile splits + combine
+    (dict(batch=8, max_seq=16384), 5, 2),                                 # 128 groups: 32-tile splits + combine
+    (dict(batch=32, max_seq=16384), 3, 2),                                # 512 groups: 64-tile splits + combine
     (dict(num_splits=7), 7, 1),                                           # forced, still one wave
     (dict(num_splits=20), 20, 2),                                         # forced past one wave
     (dict(dtype=0, out_dtype=0, head_dim=64), 1, 1),                      # fp32: one kernel, no splits

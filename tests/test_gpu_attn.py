@@ -121,12 +121,12 @@ def test_tree_attention_ragged_batch():
 
 
 def test_tree_attention_ragged_fixed_splits():
-    """More (request, KV head, row block) groups than SMs: fixed-size key splits of 16
+    """More (request, KV head, row block) groups than SMs: fixed-size key splits of 32
     tiles per CTA, requests dispatched longest first, one request with no prefix."""
-    w = W["concurrency"].with_(prefix=2500, prefix_min=1, batch=10)
+    w = W["concurrency"].with_(prefix=5000, prefix_min=1, batch=10)
     seq_len = synth.prefix_lengths(w, 10)
     seq_len[3] = 0
-    seq_len[6] = 2500
+    seq_len[6] = 5000
     par, mask = random_tree(61, seed=17)
     _check(w, 10, seq_len, 61, par, mask, [(0, 1), (3, 5), (6, 7), (9, 0)])
 
