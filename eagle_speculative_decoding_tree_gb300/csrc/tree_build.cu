@@ -567,81 +567,112 @@ __device__ __forceinline__ ff ff_shfl_up(ff v, int o) {
   return ff{__shfl_up_sync(0xffffffffu, v.hi, o), __shfl_up_sync(0xffffffffu, v.lo, o)};
 }
 
-// Warp inverse-CDF draw over one logit row with weights exp((x - M) / T): the chunk
-// masses pick the chunk that holds the crossing, then the lanes scan that chunk
-// (running sums as float-float).  Returns the token; *near = 1 when the draw lands
-// within 1e-7 of the mass of a bin edge.
+// Warp inclusive scan of a float-float value over the lanes.
+__device__ __forceinline__ ff warp_incl_scan(ff v) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const ff t = ff_shfl_up(v, o);
+    if (lane >= o) v = ff_add(v, t);
+  }
+  return v;
+}
+
+// Warp inverse-CDF draw over one logit row with weights w_v = exp((x_v - M) / T): the
+// smallest v whose running mass exceeds u W.  Three warp-parallel levels, each a scan over
+// the lanes with float-float sums: the chunk masses (32 chunks at a time) pick the
+// 4096-token chunk; 32 runs of <= 128 tokens of that chunk pick the run; 32 groups of <= 4
+// tokens of that run pick the group, whose lane finds the token.  The levels add the same
+// weights in different orders, which moves a sum by about 1e-14 of it; a draw that close to
+// an edge is flagged near anyway.  Returns the token; *near = 1 when u W lies
+// within 1e-7 W of an edge of the chosen bin, or when no bin crosses (rounding: the last
+// token with positive weight is taken).
 __device__ int warp_draw(const void* logits, size_t row, int dtype, int V, const ChunkPart* cp, int n_chunks, float M,
                          float invT, ff W, float u, int* near) {
   const int lane = threadIdx.x & 31;
   const ff target = ff_mul(W, u);
-  int cstar = -1, fallback = 0;
-  ff base = ff_make(0.f);
-  if (lane == 0) {
-    ff cum = ff_make(0.f);
-    int last_pos = -1;
-    for (int c = 0; c < n_chunks; ++c) {
-      const ff w = (cp[c].m == -INFINITY) ? ff_make(0.f) : ff_mul(cp[c].sT, expf((cp[c].m - M) * invT));
-      if (w.hi > 0.f) last_pos = c;
-      if (ff_gt(ff_add(cum, w), target)) {
-        cstar = c;
-        base = cum;
-        break;
-      }
-      cum = ff_add(cum, w);
-    }
-    if (cstar < 0) {  // nothing crosses (rounding): the last positive weight
-      cstar = last_pos < 0 ? 0 : last_pos;
-      fallback = 1;
-    }
-  }
-  cstar = __shfl_sync(0xffffffffu, cstar, 0);
-  fallback = __shfl_sync(0xffffffffu, fallback, 0);
-  base = ff_shfl(base, 0);
-  const int lo = cstar * kVocabChunk, hi = min(V, lo + kVocabChunk);
-  const int n = hi - lo;
-  const int seg = (n + 31) / 32;
-  const int a0 = lo + lane * seg, a1 = min(hi, a0 + seg);
-  ff my = ff_make(0.f);
-  for (int v = a0; v < a1; ++v) my = ff_add(my, expf((load_elem(logits, row + v, dtype) - M) * invT));
-  ff incl = my;
+  auto wt = [&](int v) { return expf((load_elem(logits, row + v, dtype) - M) * invT); };
+  auto group4 = [&](int g0, int g1) {  // mass of tokens [g0, g1), g1 - g0 <= 4, in order
+    ff m = ff_make(0.f);
 #pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const ff t = ff_shfl_up(incl, o);
-    if (lane >= o) incl = ff_add(incl, t);
-  }
-  const ff lbase = ff_sub(ff_add(base, incl), my);
-  const ff rel = fallback ? ff_make(INFINITY) : ff_sub(target, lbase);
-  ff cum = ff_make(0.f);
-  int found = -1;
-  ff prev_edge = ff_make(0.f), next_edge = ff_make(0.f);
-  int last_pos = -1;
-  for (int v = a0; v < a1; ++v) {
-    const float w = expf((load_elem(logits, row + v, dtype) - M) * invT);
-    if (w > 0.f) last_pos = v;
-    const ff nc = ff_add(cum, w);
-    if (found < 0 && w > 0.f && ff_gt(nc, rel)) {
-      found = v;
-      prev_edge = ff_add(lbase, cum);
-      next_edge = ff_add(lbase, nc);
+    for (int k = 0; k < 4; ++k) m = ff_add(m, (g0 + k < g1) ? wt(g0 + k) : 0.f);
+    return m;
+  };
+  // level 1: the chunk
+  int cstar = -1, last_chunk = -1;
+  ff base = ff_make(0.f), run = ff_make(0.f);
+  for (int c0 = 0; c0 < n_chunks; c0 += 32) {
+    const int c = c0 + lane;
+    const ff w = (c < n_chunks && cp[c].m != -INFINITY) ? ff_mul(cp[c].sT, expf((cp[c].m - M) * invT)) : ff_make(0.f);
+    const ff incl = ff_add(run, warp_incl_scan(w));
+    const unsigned pos = __ballot_sync(0xffffffffu, w.hi > 0.f);
+    if (pos) last_chunk = c0 + 31 - __clz(pos);
+    const unsigned cross = __ballot_sync(0xffffffffu, c < n_chunks && ff_gt(incl, target));
+    if (cross) {
+      const int src = __ffs(cross) - 1;
+      cstar = c0 + src;
+      base = ff_shfl(ff_sub(incl, w), src);
+      break;
     }
-    cum = nc;
+    run = ff_shfl(incl, 31);
   }
-  const unsigned ball = __ballot_sync(0xffffffffu, found >= 0);
-  int tok;
-  int nr = 0;
-  if (ball) {
-    const int src = __ffs(ball) - 1;
-    tok = __shfl_sync(0xffffffffu, found, src);
-    const ff pe = ff_shfl(prev_edge, src);
-    const ff ne = ff_shfl(next_edge, src);
-    const float win = kIcdfNearEps * ff_float(W);
-    nr = (ff_float(ff_sub(target, pe)) < win || ff_float(ff_sub(ne, target)) < win) ? 1 : 0;
-  } else {
-    const unsigned bl = __ballot_sync(0xffffffffu, last_pos >= 0);
-    const int src = bl ? 31 - __clz(bl) : 0;
-    tok = __shfl_sync(0xffffffffu, last_pos, src);
-    if (tok < 0) tok = lo;
+  bool fallback = cstar < 0;
+  if (fallback) cstar = last_chunk < 0 ? 0 : last_chunk;
+  const int lo = cstar * kVocabChunk, hi = min(V, lo + kVocabChunk);
+  // level 2: 32 runs of 128 tokens (32 groups of 4 each)
+  const int r0 = min(hi, lo + 128 * lane), r1 = min(hi, r0 + 128);
+  ff acc[4] = {ff_make(0.f), ff_make(0.f), ff_make(0.f), ff_make(0.f)};  // four chains of groups
+#pragma unroll 4
+  for (int q = 0; q < 32; ++q) {
+    const int g = r0 + 4 * q;
+    if (g < r1) acc[q & 3] = ff_add(acc[q & 3], group4(g, min(r1, g + 4)));
+  }
+  const ff my = ff_add(ff_add(acc[0], acc[1]), ff_add(acc[2], acc[3]));
+  const ff incl2 = ff_add(base, warp_incl_scan(my));
+  const unsigned cross2 = fallback ? 0u : __ballot_sync(0xffffffffu, my.hi > 0.f && ff_gt(incl2, target));
+  int tok = -1, nr = 0;
+  if (cross2) {
+    const int src = __ffs(cross2) - 1;
+    const ff rbase = ff_shfl(ff_sub(incl2, my), src);  // mass before the run
+    // level 3: the run's 32 groups of 4
+    const int s0 = lo + 128 * src, s1 = min(hi, s0 + 128);
+    const int g0 = min(s1, s0 + 4 * lane), g1 = min(s1, g0 + 4);
+    const ff gm = group4(g0, g1);
+    const ff incl3 = ff_add(rbase, warp_incl_scan(gm));
+    const unsigned cross3 = __ballot_sync(0xffffffffu, gm.hi > 0.f && ff_gt(incl3, target));
+    if (cross3) {
+      const int src3 = __ffs(cross3) - 1;
+      int found = -1;
+      ff pe = ff_make(0.f), ne = ff_make(0.f);
+      if (lane == src3) {
+        ff cum = ff_sub(incl3, gm);
+        for (int v = g0; v < g1; ++v) {
+          const float w = wt(v);
+          const ff nc = ff_add(cum, w);
+          if (found < 0 && w > 0.f && ff_gt(nc, target)) {
+            found = v;
+            pe = cum;
+            ne = nc;
+          }
+          cum = nc;
+        }
+      }
+      found = __shfl_sync(0xffffffffu, found, src3);
+      pe = ff_shfl(pe, src3);
+      ne = ff_shfl(ne, src3);
+      if (found >= 0) {
+        tok = found;
+        const float win = kIcdfNearEps * ff_float(W);
+        nr = (ff_float(ff_sub(target, pe)) < win || ff_float(ff_sub(ne, target)) < win) ? 1 : 0;
+      }
+    }
+  }
+  if (tok < 0) {  // nothing crosses (rounding): the last token of the chunk with positive weight
+    int last = -1;
+    for (int v = r0; v < r1; ++v)
+      if (wt(v) > 0.f) last = v;
+    const unsigned bl = __ballot_sync(0xffffffffu, last >= 0);
+    tok = bl ? __shfl_sync(0xffffffffu, last, 31 - __clz(bl)) : lo;
     nr = 1;
   }
   *near = nr;
