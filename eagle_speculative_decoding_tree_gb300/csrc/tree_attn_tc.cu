@@ -26,7 +26,14 @@
 // directly.  When the whole grid fits on the SMs at once the launch is cooperative:
 // every split stores its partial rows (TMA) and counts itself into its group
 // (request, KV head, row block); once the group is complete each CTA merges a slice
-// of the group's rows from L2.  Otherwise the shared combine kernel merges them.
+// of the group's rows from L2.  Otherwise the shared combine kernel merges them; then
+// (batched requests) a request's keys are cut into pieces of a fixed number of tiles,
+// the requests are taken longest first, and the grid puts the row blocks of one key
+// range next to each other so that they share its K/V tiles through L2.
+//
+// The launch is programmatic: barrier setup, TMEM allocation and descriptor prefetch
+// overlap the tail of the preceding kernel; nothing is read from global memory before
+// griddepcontrol.wait.
 //
 // Every wait is bounded; a timeout ORs a bit into the error word at the start of the
 // workspace (it stays set until the caller clears it) and the roles stop, so the
@@ -480,8 +487,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     // ------------------------------------------------------------ softmax, warps 0-7
     // All eight warps work on one M-tile at a time: warp w reads TMEM lane quarter
     // w & 3 (32 rows) and key half w >> 2 (keys / S columns [64 hf, 64 hf + 64)).  The
-    // two halves of a row agree on its max through shared memory; each half writes
-    // its P into its own S columns, so S stays in registers between the passes.
+    // two halves of a row agree on its max through shared memory; each half reads its
+    // S once, keeps it in registers across the exchange and writes its P into its own
+    // S columns.
     const int qd = warp & 3;
     const int hf = warp >> 2;
     const int r_local = qd * 32 + lane;      // row within an M-tile = TMEM lane
