@@ -171,7 +171,9 @@ typedef struct {
   int32_t max_seq;     /* P: cache capacity per request (rows of the K/V cache) */
   float scale;         /* softmax scale, usually 1/sqrt(D) */
   int32_t dtype;       /* element type of q, caches and tree K/V */
-  int32_t num_splits;  /* prefix splits per (request, KV head); 0 = choose from the SM count */
+  int32_t num_splits;  /* prefix splits per (request, KV head); 0 = choose: from the SM count
+                          when the grid fits on the SMs at once, else key pieces of a fixed
+                          number of tiles per request */
   int32_t out_dtype;   /* element type of out: EAGLE_F32, or EAGLE_BF16 when dtype is EAGLE_BF16 */
   int32_t precision;   /* EAGLE_ATTN_STANDARD or EAGLE_ATTN_PRECISE (ignored for fp32 inputs) */
   int32_t engine;      /* EAGLE_ENGINE_AUTO (tensor-core tcgen05 kernel where supported) or
@@ -192,7 +194,9 @@ typedef struct {
  * inside it gives up; the word stays set until the caller clears it, and the outputs
  * of the calls made since it was last zero are not valid (re-zero the whole workspace
  * before further use).  When the splits merge inside the kernel its launch is
- * cooperative (all CTAs resident at once, one per SM).
+ * cooperative (all CTAs resident at once, one per SM).  The tcgen05 launch is
+ * programmatic: its setup may overlap the preceding kernel in the stream, and it reads
+ * its inputs (and ws) only once that kernel has completed.
  * Unsupported: head_dim not 64/128, R > 128, Hq % Hkv != 0, B * Hkv > 65535, bf16 out
  * with fp32 inputs. */
 int eagle_tree_attn(const eagle_attn_desc* d, const void* q, const void* k_cache, const void* v_cache,
