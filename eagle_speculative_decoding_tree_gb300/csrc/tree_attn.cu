@@ -573,16 +573,18 @@ void plan_tree_attn(const eagle_attn_desc* d, int num_sms, AttnPlan* p) {
     // more groups than a cooperative grid holds (batched, ragged requests): each
     // request's key range is cut into fixed pieces of T 128-key units (the tree tile
     // counts as one), so a long request spreads over several CTAs and a short one
-    // takes few; T = 32 while the groups alone fill under two waves of SMs, else 64.
-    // The longest requests are dispatched first.
-    const int T = (base < 2 * num_sms) ? 32 : 64;
+    // takes few; T = 32 while the groups alone fill under two waves of SMs, else 64,
+    // and larger when a request would need more than 64 pieces.  Up to 64 requests,
+    // the longest are dispatched first (each CTA ranks the lengths: B^2 / 32 steps).
     const int units = max_tiles + 1;
+    int T = (base < 2 * num_sms) ? 32 : 64;
+    if ((units + T - 1) / T > 64) T = (units + 63) / 64;
     const int s2 = (units + T - 1) / T;
-    if (s2 > 1 && s2 <= 64) {
+    if (s2 > 1) {
       splits = s2;
       p->tps = T;
     }
-    p->lpt = p->B > 1;
+    p->lpt = p->B > 1 && p->B <= 64;
   }
   p->splits = splits;
   // the kernel's own merge keeps partial O in bf16 unless the precise mode was asked for

@@ -183,6 +183,7 @@ def test_binding_refuses_cpu_tensors(lib):
     (dict(rows=8, max_seq=131072 + 8), 19, 1),                            # long128k chain: 8 groups x 19
     (dict(batch=8, max_seq=16384), 5, 2),                                 # 128 groups: 32-tile splits + combine
     (dict(batch=32, max_seq=16384), 3, 2),                                # 512 groups: 64-tile splits + combine
+    (dict(batch=16, max_seq=1 << 20), 64, 2),                            # 1M-token cache: 129-tile pieces
     (dict(num_splits=7), 7, 1),                                           # forced, still one wave
     (dict(num_splits=20), 20, 2),                                         # forced past one wave
     (dict(dtype=0, out_dtype=0, head_dim=64), 1, 1),                      # fp32: one kernel, no splits
