@@ -149,6 +149,16 @@ def test_tree_attention_full_size_concurrency_batch8():
     _check(w, 8, seq_len, w.rows, par, mask, [(0, 0), (7, 7), (3, 2)], strict_standard=True)
 
 
+def test_tree_attention_full_size_concurrency_batch32():
+    """The batch-32 benchmark shape: 64-tile key pieces, longest requests first; the
+    longest and shortest requests among the checked heads."""
+    w = W["concurrency"].with_(batch=32)
+    seq_len = synth.prefix_lengths(w, 32)
+    par, mask = random_tree(w.rows, seed=13)
+    heads = [(0, 0), (31, 7), (int(np.argmax(seq_len)), 3), (int(np.argmin(seq_len)), 5)]
+    _check(w, 32, seq_len, w.rows, par, mask, heads, strict_standard=True)
+
+
 @pytest.mark.gpu
 def test_tree_attention_workspace_reuse():
     """Calls on one workspace: identical outputs, group counters back at zero, no timeouts."""
