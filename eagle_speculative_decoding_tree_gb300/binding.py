@@ -24,7 +24,7 @@ EAGLE_F32, EAGLE_BF16 = 0, 1
 EAGLE_TREE_DYNAMIC, EAGLE_TREE_STATIC_TOPK, EAGLE_TREE_STATIC_SAMPLED = 0, 1, 2
 EAGLE_PROPOSAL_DELTA, EAGLE_PROPOSAL_SAMPLED = 0, 1
 EAGLE_WS_TREE_BUILD, EAGLE_WS_TREE_ATTN, EAGLE_WS_ACCEPT = 1, 2, 3
-EAGLE_ATTN_STANDARD, EAGLE_ATTN_PRECISE = 0, 1
+EAGLE_ATTN_PRECISE, EAGLE_ATTN_FAST = 0, 1
 EAGLE_ENGINE_AUTO, EAGLE_ENGINE_MMA_SYNC = 0, 1
 EAGLE_STATUS_BAD_TREE, EAGLE_STATUS_PATH_OVERFLOW, EAGLE_STATUS_CACHE_FULL, EAGLE_STATUS_BAD_TOKEN = 1, 2, 4, 8
 
@@ -50,7 +50,8 @@ class AttnDesc(ctypes.Structure):
     _fields_ = [("batch", ctypes.c_int32), ("rows", ctypes.c_int32), ("n_q_heads", ctypes.c_int32),
                 ("n_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32), ("max_seq", ctypes.c_int32),
                 ("scale", ctypes.c_float), ("dtype", ctypes.c_int32), ("num_splits", ctypes.c_int32),
-                ("out_dtype", ctypes.c_int32), ("precision", ctypes.c_int32), ("engine", ctypes.c_int32)]
+                ("out_dtype", ctypes.c_int32), ("precision", ctypes.c_int32), ("engine", ctypes.c_int32),
+                ("fault_test", ctypes.c_int32)]
 
 
 class AcceptDesc(ctypes.Structure):
@@ -86,7 +87,7 @@ def load() -> ctypes.CDLL:
         L = ctypes.CDLL(_build.LIB)
         vp, i32, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
         L.eagle_tree_build.argtypes = [ctypes.POINTER(TreeDesc), i32, vp, vp, vp, vp, vp, sz, ctypes.POINTER(TreeOut), vp]
-        L.eagle_tree_attn.argtypes = [ctypes.POINTER(AttnDesc), vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+        L.eagle_tree_attn.argtypes = [ctypes.POINTER(AttnDesc), vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
         L.eagle_accept.argtypes = [ctypes.POINTER(AcceptDesc), vp, vp, vp, vp, vp, vp, ctypes.POINTER(AcceptOut), vp,
                                    sz, vp]
         L.eagle_accept_noalloc.argtypes = [ctypes.POINTER(AcceptDesc), vp, vp, vp, vp, vp, vp,
@@ -249,13 +250,16 @@ def eagle_tree_build(desc: TreeDesc, level: int, frontier_logits: torch.Tensor, 
 
 
 def eagle_tree_attn(desc: AttnDesc, q, k_cache, v_cache, tree_k, tree_v, seq_len, anc_mask, out,
-                    lse: Optional[torch.Tensor], ws: Optional[torch.Tensor], stream=None) -> None:
-    """One layer of tree attention (see eagle.h: eagle_tree_attn)."""
+                    lse: Optional[torch.Tensor], ws: Optional[torch.Tensor], stream=None,
+                    n_nodes: Optional[torch.Tensor] = None) -> None:
+    """One layer of tree attention (see eagle.h: eagle_tree_attn); n_nodes [B] int32
+    gives each request's tree size (None: every request has desc.rows rows)."""
     ws_ptr = _ptr(ws, name="ws") if ws is not None else None
     ws_bytes = ws.numel() * ws.element_size() if ws is not None else 0
     _check("eagle_tree_attn", load().eagle_tree_attn(
         ctypes.byref(desc), _ptr(q, FLOATS, "q"), _ptr(k_cache, FLOATS, "k_cache"), _ptr(v_cache, FLOATS, "v_cache"),
         _ptr(tree_k, FLOATS, "tree_k"), _ptr(tree_v, FLOATS, "tree_v"), _ptr(seq_len, torch.int32, "seq_len"),
+        _ptr(n_nodes, torch.int32, "n_nodes"),
         _ptr(anc_mask, torch.int64, "anc_mask"), _ptr(out, FLOATS, "out"), _ptr(lse, torch.float32, "lse"),
         ws_ptr, ws_bytes, _stream(stream)))
 

@@ -79,7 +79,8 @@ int check_attn_desc(const eagle_attn_desc* d) {
   if (d->head_dim != 64 && d->head_dim != 128) return EAGLE_ERR_UNSUPPORTED;
   if (d->rows > kMaxRows || !dtype_ok(d->dtype) || !dtype_ok(d->out_dtype)) return EAGLE_ERR_UNSUPPORTED;
   if (d->dtype == EAGLE_F32 && d->out_dtype != EAGLE_F32) return EAGLE_ERR_UNSUPPORTED;
-  if (d->precision != EAGLE_ATTN_STANDARD && d->precision != EAGLE_ATTN_PRECISE) return EAGLE_ERR_INVALID_ARG;
+  if (d->precision != EAGLE_ATTN_PRECISE && d->precision != EAGLE_ATTN_FAST) return EAGLE_ERR_INVALID_ARG;
+  if (d->fault_test != 0 && d->fault_test != 1) return EAGLE_ERR_INVALID_ARG;
   return EAGLE_OK;
 }
 
@@ -194,20 +195,21 @@ int eagle_tree_build(const eagle_tree_desc* d, int level, const void* frontier_l
 }
 
 int eagle_tree_attn(const eagle_attn_desc* d, const void* q, const void* k_cache, const void* v_cache,
-                    const void* tree_k, const void* tree_v, const int32_t* seq_len, const uint64_t* anc_mask,
-                    void* out, float* lse, void* ws, size_t ws_bytes, void* stream) {
+                    const void* tree_k, const void* tree_v, const int32_t* seq_len, const int32_t* n_nodes,
+                    const uint64_t* anc_mask, void* out, float* lse, void* ws, size_t ws_bytes, void* stream) {
   int rc = check_attn_desc(d);
   if (rc != EAGLE_OK) return rc;
   if (!q || !k_cache || !v_cache || !tree_k || !tree_v || !seq_len || !anc_mask || !out)
     return EAGLE_ERR_INVALID_ARG;
   if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(tree_k, 16) ||
       !aligned(tree_v, 16) || !aligned(out, 16) || !aligned(anc_mask, 8) || (lse && !aligned(lse, 4)) ||
+      (n_nodes && !aligned(n_nodes, 4)) ||
       (ws && !aligned(ws, 16)))
     return EAGLE_ERR_ALIGNMENT;
   AttnPlan p;
   plan_tree_attn(d, num_sms(), &p);
   if (p.total > 0 && (!ws || ws_bytes < p.total)) return EAGLE_ERR_WORKSPACE;
-  return cuda_status(launch_tree_attn(p, q, k_cache, v_cache, tree_k, tree_v, seq_len, anc_mask, out, lse, ws,
+  return cuda_status(launch_tree_attn(p, q, k_cache, v_cache, tree_k, tree_v, seq_len, n_nodes, anc_mask, out, lse, ws,
                           static_cast<cudaStream_t>(stream)));
 }
 

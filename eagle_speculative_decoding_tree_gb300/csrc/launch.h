@@ -48,7 +48,7 @@ struct AttnPlan {
   int rows_pad;      // row_blocks * rows_per_cta
   bool coop;         // tcgen05, splits > 1, grid fits on the SMs at once: the splits of a
                      // (request, KV head, row block) merge their partials in the kernel
-  bool part_bf16;    // coop with standard precision: partial O kept as bf16
+  bool fault_test;   // test hook: the in-kernel split group waits for a split that never comes
   int tps;           // tcgen05 without coop: tile units per split (0: even splits)
   bool lpt;          // tcgen05 without coop, B > 1: longest requests dispatched first
   size_t off_err, off_cnt, off_o, off_ml, total;
@@ -58,14 +58,15 @@ int report_cuda_error(cudaError_t e);
 
 void plan_tree_attn(const eagle_attn_desc* d, int num_sms, AttnPlan* p);
 // Merge split partials into out / lse (shared by the mma.sync and tcgen05 kernels).
-cudaError_t launch_tree_attn_combine(const AttnPlan& p, const int32_t* seq_len, void* out, float* lse,
-                                     const float* part_o, const float* part_ml, cudaStream_t s);
+cudaError_t launch_tree_attn_combine(const AttnPlan& p, const int32_t* seq_len, const int32_t* n_nodes, void* out,
+                                     float* lse, const float* part_o, const float* part_ml, cudaStream_t s);
 // The tcgen05 kernel (plan.tc); ws holds the error word and the partials.
 cudaError_t launch_tree_attn_tc(const AttnPlan& p, const void* q, const void* k_cache, const void* v_cache,
                                 const void* tree_k, const void* tree_v, const int32_t* seq_len,
-                                const uint64_t* anc_mask, void* out, float* lse, void* ws, cudaStream_t s);
+                                const int32_t* n_nodes, const uint64_t* anc_mask, void* out, float* lse, void* ws,
+                                cudaStream_t s);
 cudaError_t launch_tree_attn(const AttnPlan& p, const void* q, const void* k_cache, const void* v_cache,
-                             const void* tree_k, const void* tree_v, const int32_t* seq_len,
+                             const void* tree_k, const void* tree_v, const int32_t* seq_len, const int32_t* n_nodes,
                              const uint64_t* anc_mask, void* out, float* lse, void* ws, cudaStream_t s);
 
 // ------------------------------------------------------------------ accept

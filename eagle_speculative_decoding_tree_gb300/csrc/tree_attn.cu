@@ -33,6 +33,7 @@ struct AttnArgs {
   const uint16_t* tk;
   const uint16_t* tv;
   const int32_t* seq_len;
+  const int32_t* n_nodes;  // [B] tree rows per request (NULL: all R)
   const uint64_t* anc_mask;
   void* out;       // [B][R][Hq][D], bf16 or fp32 (out_f32)
   float* lse;
@@ -46,6 +47,13 @@ struct AttnArgs {
 
 // Store two adjacent output elements (bf16 pair or fp32 pair).
 __device__ __forceinline__ void store_out2(const AttnArgs& a, size_t idx, float v0, float v1);
+
+// Tree rows of request b: n_nodes[b] clamped to [0, R], or R without n_nodes.
+__device__ __forceinline__ int request_rows(const int32_t* n_nodes, int b, int R) {
+  if (!n_nodes) return R;
+  const int n = n_nodes[b];
+  return n < 0 ? 0 : (n > R ? R : n);
+}
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -124,11 +132,12 @@ __global__ void __launch_bounds__(NW * 32, (NW == 4) ? 2 : 1) tree_attn_mma_kern
   const int t_begin = static_cast<int>(static_cast<long long>(n_pref) * split / a.splits);
   const int t_end = static_cast<int>(static_cast<long long>(n_pref) * (split + 1) / a.splits);
   const int n_pt = t_end - t_begin;
-  const int n_tt = (split == a.splits - 1) ? (a.R + BN - 1) / BN : 0;
+  const int Rb = request_rows(a.n_nodes, b, a.R);
+  const int n_tt = (split == a.splits - 1) ? (Rb + BN - 1) / BN : 0;
   const int n_tiles = n_pt + n_tt;
 
-  // ---- the two rows this thread's accumulators cover
-  const int RG = a.R * a.G;
+  // ---- the two rows this thread's accumulators cover (rows of nodes >= Rb are idle)
+  const int RG = Rb * a.G;
   int node[2], head[2];
   bool valid[2];
   uint64_t mw[2][2];
@@ -170,7 +179,7 @@ __global__ void __launch_bounds__(NW * 32, (NW == 4) ? 2 : 1) tree_attn_mma_kern
       start = (t - n_pt) * BN;
       kb = a.tk + kv_head * a.R * D;
       vb = a.tv + kv_head * a.R * D;
-      nvalid = a.R - start;
+      nvalid = Rb - start;
     }
     const uint32_t sk = smem_addr(smem + stage * 2 * TILE);
     for (int c = threadIdx.x; c < BN * CH; c += NW * 32) {
@@ -235,7 +244,7 @@ __global__ void __launch_bounds__(NW * 32, (NW == 4) ? 2 : 1) tree_attn_mma_kern
         bool ok;
         if (is_tree) {
           const uint64_t w = (key < 64) ? mw[i][0] : mw[i][1];
-          ok = key < a.R && ((w >> (key & 63)) & 1ull);
+          ok = key < Rb && ((w >> (key & 63)) & 1ull);
         } else {
           ok = key < L;
         }
@@ -357,8 +366,8 @@ __global__ void __launch_bounds__(128) tree_attn_combine_kernel(const AttnArgs a
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int r = blockIdx.x * 4 + warp;
   const int bh = blockIdx.y;
-  if (r >= a.R * a.G) return;
   const int b = bh / a.Hkv, h = bh % a.Hkv;
+  if (r >= request_rows(a.n_nodes, b, a.R) * a.G) return;
   const int nd = r / a.G, hq = h * a.G + r % a.G;
   const size_t base = static_cast<size_t>(bh) * a.splits * a.rows_pad + r;
   const size_t sstride = static_cast<size_t>(a.rows_pad) * D;
@@ -443,7 +452,8 @@ template <int D>
 __global__ void __launch_bounds__(128) tree_attn_f32_kernel(const float* __restrict__ q, const float* __restrict__ kc,
                                                             const float* __restrict__ vc, const float* __restrict__ tk,
                                                             const float* __restrict__ tv, const int32_t* seq_len,
-                                                            const uint64_t* anc_mask, float* out, float* lse, int B,
+                                                            const int32_t* n_nodes, const uint64_t* anc_mask,
+                                                            float* out, float* lse, int B,
                                                             int R, int Hq, int Hkv, int P, int W, float scale) {
   constexpr int PER = D / 32;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -453,6 +463,8 @@ __global__ void __launch_bounds__(128) tree_attn_f32_kernel(const float* __restr
   const int i = static_cast<int>((id / Hq) % R);
   const int b = static_cast<int>(id / (static_cast<long long>(Hq) * R));
   const int G = Hq / Hkv, h = hq / G;
+  const int Rb = request_rows(n_nodes, b, R);
+  if (i >= Rb) return;  // rows past the request's tree are not computed
   int L = seq_len[b];
   L = L < 0 ? 0 : (L > P ? P : L);
   float qv[PER], ov[PER];
@@ -478,7 +490,7 @@ __global__ void __launch_bounds__(128) tree_attn_f32_kernel(const float* __restr
   };
   const size_t kvh = static_cast<size_t>(b) * Hkv + h;
   for (int j = 0; j < L; ++j) visit(kc + (kvh * P + j) * D, vc + (kvh * P + j) * D);
-  for (int t = 0; t < R; ++t) {
+  for (int t = 0; t < Rb; ++t) {
     const uint64_t w = anc_mask[(static_cast<size_t>(b) * R + i) * W + (t >> 6)];
     if ((w >> (t & 63)) & 1ull) visit(tk + (kvh * R + t) * D, tv + (kvh * R + t) * D);
   }
@@ -529,10 +541,10 @@ void plan_tree_attn(const eagle_attn_desc* d, int num_sms, AttnPlan* p) {
   p->scale = d->scale;
   p->out_dtype = d->out_dtype;
   p->precise = d->precision == EAGLE_ATTN_PRECISE;
+  p->fault_test = d->fault_test == 1;
   p->off_err = p->off_cnt = p->off_o = p->off_ml = p->total = 0;
   p->tc = false;
   p->coop = false;
-  p->part_bf16 = false;
   p->tps = 0;
   p->lpt = false;
   const int RG = p->R * p->G;
@@ -547,7 +559,7 @@ void plan_tree_attn(const eagle_attn_desc* d, int num_sms, AttnPlan* p) {
   p->tc = d->engine == EAGLE_ENGINE_AUTO && p->D == 128 && (128 % p->G) == 0;
   int key_tile, slots_per_sm;
   if (p->tc) {
-    p->rows_per_cta = 128;  // one M-tile: TMEM holds two S buffers and O
+    p->rows_per_cta = 128;  // one M-tile: TMEM holds two S buffers and two O accumulators
     key_tile = 128;
     slots_per_sm = 1;  // one CTA per SM: it holds all 512 TMEM columns
   } else {
@@ -587,8 +599,6 @@ void plan_tree_attn(const eagle_attn_desc* d, int num_sms, AttnPlan* p) {
     p->lpt = p->B > 1 && p->B <= 64;
   }
   p->splits = splits;
-  // the kernel's own merge keeps partial O in bf16 unless the precise mode was asked for
-  p->part_bf16 = p->coop && !p->precise;
   size_t off = p->tc ? 256 : 0;  // tcgen05: error word first
   if (p->coop) {
     p->off_cnt = off;
@@ -597,17 +607,18 @@ void plan_tree_attn(const eagle_attn_desc* d, int num_sms, AttnPlan* p) {
   if (splits > 1) {
     const size_t rows = static_cast<size_t>(p->B) * p->Hkv * splits * p->rows_pad;
     p->off_o = off;
-    off += ((rows * p->D * (p->part_bf16 ? 2 : 4)) + 255) / 256 * 256;
+    off += ((rows * p->D * 4) + 255) / 256 * 256;  // fp32 partial O
     p->off_ml = off;
     off += rows * 2 * 4;
   }
   p->total = off;
 }
 
-cudaError_t launch_tree_attn_combine(const AttnPlan& p, const int32_t* seq_len, void* out, float* lse,
-                                     const float* part_o, const float* part_ml, cudaStream_t s) {
+cudaError_t launch_tree_attn_combine(const AttnPlan& p, const int32_t* seq_len, const int32_t* n_nodes, void* out,
+                                     float* lse, const float* part_o, const float* part_ml, cudaStream_t s) {
   AttnArgs a{};
   a.seq_len = seq_len;
+  a.n_nodes = n_nodes;
   a.tps = p.tps;
   a.out = out;
   a.lse = lse;
@@ -634,21 +645,22 @@ cudaError_t launch_tree_attn_combine(const AttnPlan& p, const int32_t* seq_len, 
 }
 
 cudaError_t launch_tree_attn(const AttnPlan& p, const void* q, const void* k_cache, const void* v_cache,
-                             const void* tree_k, const void* tree_v, const int32_t* seq_len,
+                             const void* tree_k, const void* tree_v, const int32_t* seq_len, const int32_t* n_nodes,
                              const uint64_t* anc_mask, void* out, float* lse, void* ws, cudaStream_t s) {
-  if (p.tc) return launch_tree_attn_tc(p, q, k_cache, v_cache, tree_k, tree_v, seq_len, anc_mask, out, lse, ws, s);
+  if (p.tc)
+    return launch_tree_attn_tc(p, q, k_cache, v_cache, tree_k, tree_v, seq_len, n_nodes, anc_mask, out, lse, ws, s);
   if (p.dtype == EAGLE_F32) {
     const long long rows = static_cast<long long>(p.B) * p.R * p.Hq;
     const int grid = static_cast<int>((rows + 3) / 4);
     if (p.D == 64)
       tree_attn_f32_kernel<64><<<grid, 128, 0, s>>>(
           static_cast<const float*>(q), static_cast<const float*>(k_cache), static_cast<const float*>(v_cache),
-          static_cast<const float*>(tree_k), static_cast<const float*>(tree_v), seq_len, anc_mask,
+          static_cast<const float*>(tree_k), static_cast<const float*>(tree_v), seq_len, n_nodes, anc_mask,
           static_cast<float*>(out), lse, p.B, p.R, p.Hq, p.Hkv, p.P, p.W, p.scale);
     else
       tree_attn_f32_kernel<128><<<grid, 128, 0, s>>>(
           static_cast<const float*>(q), static_cast<const float*>(k_cache), static_cast<const float*>(v_cache),
-          static_cast<const float*>(tree_k), static_cast<const float*>(tree_v), seq_len, anc_mask,
+          static_cast<const float*>(tree_k), static_cast<const float*>(tree_v), seq_len, n_nodes, anc_mask,
           static_cast<float*>(out), lse, p.B, p.R, p.Hq, p.Hkv, p.P, p.W, p.scale);
     return cudaGetLastError();
   }
@@ -659,6 +671,7 @@ cudaError_t launch_tree_attn(const AttnPlan& p, const void* q, const void* k_cac
   a.tk = static_cast<const uint16_t*>(tree_k);
   a.tv = static_cast<const uint16_t*>(tree_v);
   a.seq_len = seq_len;
+  a.n_nodes = n_nodes;
   a.anc_mask = anc_mask;
   a.out = out;
   a.out_f32 = p.out_dtype == EAGLE_F32;

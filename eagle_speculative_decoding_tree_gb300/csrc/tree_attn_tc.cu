@@ -7,22 +7,27 @@
 //
 // One CTA per (request, KV head, split, 128-row block), 320 threads, warp-specialised:
 //   warp 8        TMA producer: Q once (one box per 64-dim half: the G query heads of
-//                 128 / G nodes), then K and V tiles of 128 keys through two-stage rings.
+//                 128 / G nodes), then K and V tiles of 128 keys through rings of
+//                 KST / VST stages.
 //   warp 9        allocates the TMEM columns and issues tcgen05.mma from lane 0:
-//                 S = Q K^T (Q, K K-major, 128-byte swizzle) into buffer t & 1, and
-//                 O += P V (P from TMEM, V MN-major), in the order QK0 QK1 | PV0 QK2 |
-//                 PV1 QK3 | ..., so the next-but-one S is computed while the softmax works
-//                 on this one; the warp zeroes V rows past the last valid key so that
-//                 masked keys contribute exactly 0.
-//   warps 0-7     online softmax: warp w takes TMEM lane quarter w & 3 (32 rows) and key
-//                 half w >> 2; the halves of a row agree on its max through shared memory.
-//                 P = 2^((s - m) c) goes back into the half's own S columns as packed bf16
-//                 (the PV A operand).  O is rescaled in TMEM only when the row max grows
-//                 by more than 2^8, after the previous PV has finished.
-// TMEM columns: S0 [0,128) S1 [128,256) O [256,384).
+//                 S(t) = Q K(t)^T into buffer t & 1 (Q, K K-major, 128-byte swizzle) and
+//                 O(t & 1) += P(t) V(t) (P from TMEM, V MN-major), in the order
+//                 QK0 QK1 | PV0 QK2 | PV1 QK3 | ...; it zeroes V rows past the last
+//                 valid key so that masked keys contribute exactly 0.
+//   warps 0-3     softmax of the even tiles, warps 4-7 of the odd tiles.  Each thread
+//                 owns one row (its TMEM lane) and all 128 keys of a tile, so a row's
+//                 maximum needs no exchange between threads; the two warpgroups keep
+//                 separate running states (m, l, O) and work on alternate tiles at the
+//                 same time, so the tensor cores compute one tile's products while
+//                 the other tile's softmax runs.  P = 2^((s - m) c) goes back into the
+//                 tile's S columns as bf16 (precise: hi + lo, two bf16 terms, about 16
+//                 significant bits; the PV product then takes one extra MMA per
+//                 K-step).  O is rescaled in TMEM only when the row max grows by more
+//                 than 2^8.  The two states merge in the epilogue.
+// TMEM columns: S0 [0,128) S1 [128,256) O0 [256,384) O1 [384,512).
 //
 // Splits: each CTA covers a contiguous range of key tiles (the tree tile counts as
-// one) and keeps unnormalised partials (O, m, l).  One split writes the output
+// one) and keeps unnormalised fp32 partials (O, m, l).  One split writes the output
 // directly.  When the whole grid fits on the SMs at once the launch is cooperative:
 // every split stores its partial rows (TMA) and counts itself into its group
 // (request, KV head, row block); once the group is complete each CTA merges a slice
@@ -60,14 +65,14 @@ constexpr int TILE = 2 * HALF;            // one K or V tile
 constexpr int NTHREADS = 320;
 constexpr int SM_Q = 0;                   // the 128-row M-tile, 32 KB
 constexpr int KST = 2;                    // K ring stages
-constexpr int VST = 2;                    // V ring stages
+constexpr int VST = 3;                    // V ring stages
 constexpr int SM_K = TILE;
 constexpr int SM_V = SM_K + KST * TILE;
 constexpr int SMEM_BYTES = SM_V + VST * TILE + 1024;
-static_assert(KST >= 2, "the partial staging area reuses two K stages");
-// TMEM columns: S / P of tile t in buffer t & 1, then the O accumulator
+static_assert(KST * TILE >= 4 * HALF, "the fp32 partial staging area reuses the K stages");
+// TMEM columns: S / P of tile t in buffer t & 1, then the two O accumulators
 __device__ __forceinline__ uint32_t col_s(int j) { return static_cast<uint32_t>(j) * 128u; }
-constexpr uint32_t COL_O = 256u;
+__device__ __forceinline__ uint32_t col_o(int j) { return 256u + static_cast<uint32_t>(j) * 128u; }
 constexpr float kRescaleLog2 = 8.f;       // lazy rescale threshold (log2 units)
 
 enum : int { ERR_Q = 1, ERR_KFULL = 2, ERR_KEMPTY = 4, ERR_VFULL = 8, ERR_VEMPTY = 16, ERR_S = 32, ERR_P = 64, ERR_O = 128,
@@ -75,20 +80,22 @@ enum : int { ERR_Q = 1, ERR_KFULL = 2, ERR_KEMPTY = 4, ERR_VFULL = 8, ERR_VEMPTY
 
 struct TcArgs {
   const int32_t* seq_len;
+  const int32_t* n_nodes;  // [B] tree rows per request (NULL: all R)
   const uint64_t* anc_mask;
   void* out;
   float* lse;
-  void* part_o;    // [B*Hkv][splits][rows_pad][128], bf16 when part_bf16 else fp32
-  int part_bf16;
+  float* part_o;   // [B*Hkv][splits][rows_pad][128] fp32
   float* part_ml;  // [B*Hkv][splits][rows_pad][2]
   int* err;
-  int B, R, Hq, Hkv, G, P, W, splits, rows_pad, rows_per_cta, n_mt, out_f32;
+  int B, R, Hq, Hkv, G, P, W, splits, rows_pad, out_f32;
   int coop;        // 1: the splits of a group merge their partials in this kernel
   int tps;         // > 0: split s takes tile units [s tps, (s + 1) tps) of its request
                    //      (splits past a request's last unit do nothing); 0: even splits
   int lpt;         // 1: the request index of the grid is a rank in decreasing sequence length
   int* cnt;        // coop: [2][n_groups] published / finished splits per (request, KV head, row block)
   int n_groups;
+  int group_need;  // splits a group waits for (splits; one more under the failure test hook)
+  unsigned long long group_limit_ns;
   float scale, scale_log2;
 };
 
@@ -98,14 +105,21 @@ struct Tmaps {
   CUtensorMap vc;
   CUtensorMap tk;  // [B*Hkv*R][128], box {64, 128}
   CUtensorMap tv;
-  CUtensorMap po;  // partial O [B*Hkv*splits*rows_pad][128]: fp32 box {32, 128} or bf16 box {64, 128}
+  CUtensorMap po;  // partial O [B*Hkv*splits*rows_pad][128] fp32, box {32, 128}
 };
 
 struct TileInfo {
-  int n_pt, t_begin, n_tiles, L;
+  int n_pt, t_begin, n_tiles, L, Rb;
 };
 
 __device__ __forceinline__ int clamp_len(const TcArgs& a, int L) { return L < 0 ? 0 : (L > a.P ? a.P : L); }
+
+// Tree rows of request b (n_nodes[b] clamped to [0, R]; all R rows without n_nodes).
+__device__ __forceinline__ int rows_of(const TcArgs& a, int b) {
+  if (!a.n_nodes) return a.R;
+  const int n = a.n_nodes[b];
+  return n < 0 ? 0 : (n > a.R ? a.R : n);
+}
 
 __device__ __forceinline__ TileInfo tile_info(const TcArgs& a, int b, int split) {
   TileInfo ti;
@@ -127,6 +141,7 @@ __device__ __forceinline__ TileInfo tile_info(const TcArgs& a, int b, int split)
   ti.n_pt = max(0, min(u1, n_pref) - u0);
   ti.n_tiles = u1 - u0;
   ti.L = L;
+  ti.Rb = rows_of(a, b);
   return ti;
 }
 
@@ -153,60 +168,34 @@ __device__ int request_of_rank(const TcArgs& a, int r) {
   return res;
 }
 
-// Valid keys of tile t (prefix keys before L; tree rows before R).
-__device__ __forceinline__ int tile_valid(const TcArgs& a, const TileInfo& ti, int t) {
+// Valid keys of tile t (prefix keys before L; tree rows before the request's row count).
+__device__ __forceinline__ int tile_valid(const TileInfo& ti, int t) {
   if (t < ti.n_pt) return min(KT, ti.L - (ti.t_begin + t) * KT);
-  return a.R;
+  return ti.Rb;
 }
 
-// Merge of one output row from the group's split partials, by a half-warp (16 lanes,
-// `hl` = lane within the half; every shuffle stays inside the half): lane s holds
-// split s's (m, l) (splits beyond 16 in further rounds), M = max m_s,
+// Merge of one output row from the group's fp32 split partials, by a half-warp (16
+// lanes, `hl` = lane within the half; every shuffle stays inside the half): lane s
+// holds split s's (m, l) (splits beyond 16 in further rounds), M = max m_s,
 // w_s = 2^((m_s - M) c), L = sum w_s l_s, O = sum w_s O_s / L.  Lane hl owns columns
 // 8 hl .. 8 hl + 7.  The partial rows of up to kMergeBatch splits are requested before
 // any is used (split indices past the last are clamped; their weight is 0), so a row
 // costs about one L2 round trip.  grow < 0: nothing to write (the loads stay in bounds).
-constexpr int kMergeBatch = 16;
+constexpr int kMergeBatch = 8;
 
-__device__ __forceinline__ void load_part8(const TcArgs& a, size_t prow, int hl, bool bf16, uint4 (&w)[2]) {
-  if (bf16) {
-    w[0] = __ldcg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.part_o) + prow * 128) + hl);
-  } else {
-    const uint4* src = reinterpret_cast<const uint4*>(static_cast<const float*>(a.part_o) + prow * 128) + 2 * hl;
-    w[0] = __ldcg(src);
-    w[1] = __ldcg(src + 1);
-  }
+__device__ __forceinline__ void load_part8(const TcArgs& a, size_t prow, int hl, float4 (&w)[2]) {
+  const float4* src = reinterpret_cast<const float4*>(a.part_o + prow * 128) + 2 * hl;
+  w[0] = __ldcg(src);
+  w[1] = __ldcg(src + 1);
 }
 
-__device__ __forceinline__ void part8_f32(const uint4 (&w)[2], bool bf16, float (&x)[8]) {
-  if (bf16) {
-    const uint32_t u[4] = {w[0].x, w[0].y, w[0].z, w[0].w};
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      x[2 * k] = __uint_as_float(u[k] << 16);
-      x[2 * k + 1] = __uint_as_float(u[k] & 0xffff0000u);
-    }
-  } else {
-    x[0] = __uint_as_float(w[0].x);
-    x[1] = __uint_as_float(w[0].y);
-    x[2] = __uint_as_float(w[0].z);
-    x[3] = __uint_as_float(w[0].w);
-    x[4] = __uint_as_float(w[1].x);
-    x[5] = __uint_as_float(w[1].y);
-    x[6] = __uint_as_float(w[1].z);
-    x[7] = __uint_as_float(w[1].w);
-  }
-}
-
-template <bool BF16>
 __device__ __forceinline__ void merge_row_hw(const TcArgs& a, int bh, int h, int b, int grow, int hl, float sl2) {
   const unsigned full = 0xffffffffu;
   const size_t base = static_cast<size_t>(bh) * a.splits * a.rows_pad + max(grow, 0);
   const size_t sstride = a.rows_pad;
-  constexpr int NB = BF16 ? kMergeBatch : kMergeBatch / 2;  // fp32 rows take two words per lane
-  uint4 v[NB][2];
+  float4 v[kMergeBatch][2];
 #pragma unroll
-  for (int u = 0; u < NB; ++u) load_part8(a, base + min(u, a.splits - 1) * sstride, hl, BF16, v[u]);
+  for (int u = 0; u < kMergeBatch; ++u) load_part8(a, base + min(u, a.splits - 1) * sstride, hl, v[u]);
   float2 ml[4];
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
@@ -228,26 +217,34 @@ __device__ __forceinline__ void merge_row_hw(const TcArgs& a, int bh, int h, int
   float acc[8];
 #pragma unroll
   for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+  auto add8 = [&](float ws, const float4 (&x)[2]) {
+    acc[0] = fmaf(ws, x[0].x, acc[0]);
+    acc[1] = fmaf(ws, x[0].y, acc[1]);
+    acc[2] = fmaf(ws, x[0].z, acc[2]);
+    acc[3] = fmaf(ws, x[0].w, acc[3]);
+    acc[4] = fmaf(ws, x[1].x, acc[4]);
+    acc[5] = fmaf(ws, x[1].y, acc[5]);
+    acc[6] = fmaf(ws, x[1].z, acc[6]);
+    acc[7] = fmaf(ws, x[1].w, acc[7]);
+  };
 #pragma unroll
-  for (int u = 0; u < NB; ++u) {
+  for (int u = 0; u < kMergeBatch; ++u) {
     const float ws = __shfl_sync(full, w4[0], u, 16);  // 0 for u >= splits
-    float x[8];
-    part8_f32(v[u], BF16, x);
-#pragma unroll
-    for (int e = 0; e < 8; ++e) acc[e] = fmaf(ws, x[e], acc[e]);
+    if (u < a.splits) add8(ws, v[u]);
   }
-  for (int sp = NB; sp < a.splits; ++sp) {  // more splits than one batch
-    const int k = sp >> 4;
-    const float ws = __shfl_sync(full, k == 0 ? w4[0] : (k == 1 ? w4[1] : (k == 2 ? w4[2] : w4[3])), sp & 15, 16);
-    uint4 t[2];
-    load_part8(a, base + sp * sstride, hl, BF16, t);
-    float x[8];
-    part8_f32(t, BF16, x);
+  for (int sp0 = kMergeBatch; sp0 < a.splits; sp0 += kMergeBatch) {  // further batches of splits
 #pragma unroll
-    for (int e = 0; e < 8; ++e) acc[e] = fmaf(ws, x[e], acc[e]);
+    for (int u = 0; u < kMergeBatch; ++u) load_part8(a, base + min(sp0 + u, a.splits - 1) * sstride, hl, v[u]);
+#pragma unroll
+    for (int u = 0; u < kMergeBatch; ++u) {
+      const int sp = sp0 + u;
+      const int k = (sp >> 4) & 3;
+      const float ws = __shfl_sync(full, k == 0 ? w4[0] : (k == 1 ? w4[1] : (k == 2 ? w4[2] : w4[3])), sp & 15, 16);
+      if (sp < a.splits) add8(ws, v[u]);
+    }
   }
   if (grow < 0) return;
-  const float inv = 1.f / L;
+  const float inv = L > 0.f ? 1.f / L : 0.f;
   const int node = grow / a.G, hq = h * a.G + grow % a.G;
   const size_t orow = (static_cast<size_t>(b * a.R + node) * a.Hq + hq) * 128 + 8 * hl;
   if (a.out_f32) {
@@ -266,16 +263,16 @@ __device__ __forceinline__ void merge_row_hw(const TcArgs& a, int bh, int h, int
   if (a.lse && hl == 0) a.lse[static_cast<size_t>(b * a.R + node) * a.Hq + hq] = a.scale * M + logf(L);
 }
 
-// Counts this split into its group and waits (at most 2 s, then ERR_GROUP) until all
+// Counts this split into its group and waits (at most limit_ns, then ERR_GROUP) until
 // `n` splits of the group have counted.  Only valid when the whole grid is resident
 // (cooperative launch).
-__device__ __forceinline__ bool group_arrive_wait(int* cnt, int n, int* err) {
+__device__ __forceinline__ bool group_arrive_wait(int* cnt, int n, int* err, unsigned long long limit_ns) {
   __threadfence();
   atomicAdd(cnt, 1);
   if (ld_acquire_gpu(cnt) >= n) return true;
   const uint64_t t0 = global_ns();
   while (ld_acquire_gpu(cnt) < n) {
-    if (global_ns() - t0 > 2000000000ull) {
+    if (global_ns() - t0 > limit_ns) {
       atomicOr(err, ERR_GROUP);
       return false;
     }
@@ -323,18 +320,57 @@ __device__ __forceinline__ void issue_qk(uint32_t tb, const uint8_t* sQ, const u
   }
 }
 
-// O += P V over the 8 K-steps of 16 keys; the P of keys 64 h + 16 k .. sits in columns
-// scol + 64 h + 8 k .. (the precise low parts 32 columns further on).
+// O (TMEM columns ocol) += P V over the 8 K-steps of 16 keys; the P of keys
+// 64 h + 16 k .. sits in columns scol + 64 h + 8 k .. (the precise low parts 32 columns
+// further on).
 template <bool PRECISE>
-__device__ __forceinline__ void issue_pv(uint32_t tb, const uint8_t* sV, uint32_t scol, bool first) {
+__device__ __forceinline__ void issue_pv(uint32_t tb, const uint8_t* sV, uint32_t scol, uint32_t ocol, bool first) {
   constexpr uint32_t idesc = idesc_bf16_f32(128, 128, 0, 1);
 #pragma unroll
   for (int ks = 0; ks < 8; ++ks) {
     const uint64_t bd = smem_desc_sw128(smem_u32(sV) + ks * 2048, HALF, 1024);
     const uint32_t acol = scol + (ks >> 2) * 64 + (ks & 3) * 8;
-    mma_ts(tb + COL_O, tb + acol, bd, idesc, (first && ks == 0) ? 0u : 1u);
-    if constexpr (PRECISE) mma_ts(tb + COL_O, tb + acol + 32, bd, idesc, 1u);
+    mma_ts(tb + ocol, tb + acol, bd, idesc, (first && ks == 0) ? 0u : 1u);
+    if constexpr (PRECISE) mma_ts(tb + ocol, tb + acol + 32, bd, idesc, 1u);
   }
+}
+
+// P of 32 keys held in registers (raw scores, masked keys -inf) -> TMEM columns
+// `col` .. (bf16 pairs; the precise low parts 32 columns further on), 16 keys per
+// store.  Returns the row sum of exactly what the PV product multiplies.
+template <bool PRECISE>
+__device__ __forceinline__ float emit_p32(const uint32_t (&r)[32], uint32_t col, uint64_t sl2x2, uint64_t nmux2) {
+  float sum = 0.f;
+#pragma unroll
+  for (int g = 0; g < 2; ++g) {
+    uint32_t hi[8], lo[8];
+    uint64_t acc2 = 0ull;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int k = 16 * g + 2 * j;
+      float x0, x1;
+      f32x2_split(fma_f32x2(f32x2(r[k], r[k + 1]), sl2x2, nmux2), x0, x1);
+      const float p0 = ex2(x0), p1 = ex2(x1);
+      __nv_bfloat162 u = __floats2bfloat162_rn(p0, p1);
+      hi[j] = *reinterpret_cast<uint32_t*>(&u);
+      if constexpr (PRECISE) {
+        const float h0 = __uint_as_float(hi[j] << 16), h1 = __uint_as_float(hi[j] & 0xffff0000u);
+        __nv_bfloat162 w = __floats2bfloat162_rn(p0 - h0, p1 - h1);
+        lo[j] = *reinterpret_cast<uint32_t*>(&w);
+        // the row sum adds hi + lo, the value the two MMAs multiply
+        acc2 = add_f32x2(acc2, f32x2(__float_as_uint(h0 + __uint_as_float(lo[j] << 16)),
+                                     __float_as_uint(h1 + __uint_as_float(lo[j] & 0xffff0000u))));
+      } else {
+        acc2 = add_f32x2(acc2, f32x2(__float_as_uint(p0), __float_as_uint(p1)));
+      }
+    }
+    tmem_st8(col + 8 * g, hi);
+    if constexpr (PRECISE) tmem_st8(col + 32 + 8 * g, lo);
+    float a0, a1;
+    f32x2_split(acc2, a0, a1);
+    sum += a0 + a1;
+  }
+  return sum;
 }
 
 template <bool PRECISE>
@@ -342,12 +378,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     tree_attn_tc_kernel(const __grid_constant__ Tmaps tm, const TcArgs a) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  __shared__ uint64_t bar_q, k_full[KST], k_empty[KST], v_full[VST], v_empty[VST], s_full[2], p_full[2], o_done, o_full;
+  __shared__ uint64_t bar_q, k_full[KST], k_empty[KST], v_full[VST], v_empty[VST], s_full[2], p_full[2], o_full;
   __shared__ uint32_t tmem_base;
-  __shared__ int s_abort;
-  __shared__ float s_red[2][2][2][128];  // [tile parity][M-tile][key half][row] half-row maxima
-  __shared__ float s_l[2][2][128];        // [M-tile][key half][row] half-row sums
-  __shared__ int s_go;                    // group merge: every split published in time
+  __shared__ float s_m[2][128], s_l[2][128];  // [tile parity][row] running max and sum
+  __shared__ int s_go;                        // group merge: every split published in time
 
   // grid: cooperative (splits, B Hkv, row blocks); otherwise (row blocks, splits, B Hkv),
   // so that the row blocks of one key range, which read the same K/V tiles, are
@@ -357,7 +391,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   const int ybh = a.coop ? blockIdx.y : blockIdx.z;
   const int h = ybh % a.Hkv;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int n_mt = a.n_mt;
 
   // prologue: nothing read from global memory before griddep_wait below
   if (warp == 8 && lane == 0) {
@@ -377,11 +410,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&s_full[s], 1);
-      mbar_init(&p_full[s], 256);
+      mbar_init(&p_full[s], 128);
     }
-    mbar_init(&o_done, 1);
     mbar_init(&o_full, 1);
-    s_abort = 0;
     fence_barrier_init();
   }
   if (warp == 9) {
@@ -400,12 +431,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   const int bh = b * a.Hkv + h;
   uint8_t* sQ = smem + SM_Q;
   auto load_q = [&]() {
-    mbar_arrive_expect_tx(&bar_q, n_mt * TILE);
-    for (int i = 0; i < n_mt; ++i) {
-      const int node0 = (rb * a.rows_per_cta + i * 128) / a.G;
-      for (int hh = 0; hh < 2; ++hh)
-        tma_load_3d(sQ + i * TILE + hh * HALF, &tm.q, 64 * hh, h * a.G, b * a.R + node0, &bar_q);
-    }
+    mbar_arrive_expect_tx(&bar_q, TILE);
+    const int node0 = (rb * 128) / a.G;
+    for (int hh = 0; hh < 2; ++hh) tma_load_3d(sQ + hh * HALF, &tm.q, 64 * hh, h * a.G, b * a.R + node0, &bar_q);
   };
   // Q does not depend on the sequence length: with even splits its load goes out before
   // seq_len is read; with fixed-size splits only a CTA that has tiles loads it.  The MMA
@@ -438,8 +466,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     }
   } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
-    // S of tile t goes to TMEM buffer t & 1: QK(0) QK(1) | PV(0) QK(2) | PV(1) QK(3) | ...
-    // so the tensor cores compute the next-but-one S while the softmax works on this one.
+    // S of tile t goes to TMEM buffer t & 1 and its PV into O(t & 1):
+    // QK(0) QK(1) | PV(0) QK(2) | PV(1) QK(3) | ...
     bool ok = true;
     if (lane == 0 && q_loaded) ok = wait_parity(&bar_q, 0, a.err, ERR_Q);
     ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0 && ti.n_tiles > 0;
@@ -455,12 +483,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     if (ok && lane == 0) ok = qk(0) && (ti.n_tiles < 2 || qk(1));
     ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
     for (int t = 0; t < ti.n_tiles && ok; ++t) {
-      const int s = t & 1, sv = t % VST;
+      const int j = t & 1, sv = t % VST;
       // V of tile t: wait, then zero the rows past the last valid key
       ok = wait_parity(&v_full[sv], (t / VST) & 1, a.err, ERR_VFULL);
       ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
       if (!ok) break;
-      const int nv = tile_valid(a, ti, t);
+      const int nv = tile_valid(ti, t);
       if (nv < KT) {
         uint8_t* vt = smem + SM_V + sv * TILE;
         for (int idx = lane; idx < (KT - nv) * 16; idx += 32) {
@@ -471,12 +499,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       }
       __syncwarp();
       if (lane == 0) {
-        ok = wait_parity(&p_full[s], (t >> 1) & 1, a.err, ERR_P);
+        ok = wait_parity(&p_full[j], (t >> 1) & 1, a.err, ERR_P);
         if (ok) {
           tc_fence_after();
-          issue_pv<PRECISE>(tb, smem + SM_V + sv * TILE, col_s(s), t == 0);
+          issue_pv<PRECISE>(tb, smem + SM_V + sv * TILE, col_s(j), col_o(j), t < 2);
           mma_commit(&v_empty[sv]);
-          mma_commit(&o_done);
           if (t + 2 < ti.n_tiles) ok = qk(t + 2);
         }
       }
@@ -485,324 +512,217 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     if (lane == 0 && ti.n_tiles > 0) mma_commit(&o_full);
   } else {
     // ------------------------------------------------------------ softmax, warps 0-7
-    // All eight warps work on one M-tile at a time: warp w reads TMEM lane quarter
-    // w & 3 (32 rows) and key half w >> 2 (keys / S columns [64 hf, 64 hf + 64)).  The
-    // two halves of a row agree on its max through shared memory; each half reads its
-    // S once, keeps it in registers across the exchange and writes its P into its own
-    // S columns.
+    // Warpgroup j = warp >> 2 takes the tiles t with t & 1 == j; thread = TMEM lane =
+    // row r_local of the M-tile, all 128 keys of the tile.
+    const int wg = warp >> 2;
     const int qd = warp & 3;
-    const int hf = warp >> 2;
-    const int r_local = qd * 32 + lane;      // row within an M-tile = TMEM lane
+    const int r_local = qd * 32 + lane;
     const uint32_t lb = tb + (static_cast<uint32_t>(qd * 32) << 16);
     const float sl2 = a.scale_log2;
-    bool vrow[2];
-    int node[2], hq[2];
-    uint32_t tw[2][2];                       // this half's ancestor words (keys >= R cleared)
-    float m_ref[2], l[2];
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {
-      const int row = rb * a.rows_per_cta + i * 128 + r_local;
-      vrow[i] = i < n_mt && row < a.R * a.G;
-      node[i] = vrow[i] ? row / a.G : 0;
-      hq[i] = h * a.G + (vrow[i] ? row % a.G : 0);
-      tw[i][0] = tw[i][1] = 0u;
-      if (vrow[i]) {
-        const uint64_t* mrow = a.anc_mask + (static_cast<size_t>(b) * a.R + node[i]) * a.W;
-        const uint64_t mw = (hf == 0) ? mrow[0] : (a.W > 1 ? mrow[1] : 0ull);
-        tw[i][0] = static_cast<uint32_t>(mw) & low_bits(a.R - 64 * hf);
-        tw[i][1] = static_cast<uint32_t>(mw >> 32) & low_bits(a.R - 64 * hf - 32);
-      }
-      m_ref[i] = -INFINITY;
-      l[i] = 0.f;
+    const int row = rb * 128 + r_local;
+    const bool vrow = row < ti.Rb * a.G;
+    const int node = vrow ? row / a.G : 0;
+    const int hq = h * a.G + (vrow ? row % a.G : 0);
+    uint32_t tw[4] = {0u, 0u, 0u, 0u};  // the row's ancestor words over the tree keys
+    if (vrow) {
+      const uint64_t* mrow = a.anc_mask + (static_cast<size_t>(b) * a.R + node) * a.W;
+      const uint64_t w0 = mrow[0], w1 = a.W > 1 ? mrow[1] : 0ull;
+      tw[0] = static_cast<uint32_t>(w0) & low_bits(ti.Rb);
+      tw[1] = static_cast<uint32_t>(w0 >> 32) & low_bits(ti.Rb - 32);
+      tw[2] = static_cast<uint32_t>(w1) & low_bits(ti.Rb - 64);
+      tw[3] = static_cast<uint32_t>(w1 >> 32) & low_bits(ti.Rb - 96);
     }
+    float m_ref = -INFINITY, l = 0.f;
     bool ok = true;
-    for (int t = 0; t < ti.n_tiles && ok; ++t) {
+    const uint64_t sl2x2 = f32x2(__float_as_uint(sl2), __float_as_uint(sl2));
+    for (int t = wg; t < ti.n_tiles && ok; t += 2) {
+      if (!__all_sync(0xffffffffu, wait_parity(&s_full[wg], (t >> 1) & 1, a.err, ERR_S))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
       const bool tree = t >= ti.n_pt;
-      const int nv = tile_valid(a, ti, t);
+      const int nv = tile_valid(ti, t);
+      uint32_t km[4];
 #pragma unroll
-      for (int i = 0; i < 2; ++i) {
-        if (i >= n_mt) break;
-        const bool got = __all_sync(0xffffffffu, wait_parity(&s_full[t & 1], (t >> 1) & 1, a.err, ERR_S));
-        tc_fence_after();
-        // the max of this half's 64 scores over the kept keys
-        const uint32_t k0 = !vrow[i] ? 0u : (tree ? tw[i][0] : low_bits(nv - 64 * hf));
-        const uint32_t k1 = !vrow[i] ? 0u : (tree ? tw[i][1] : low_bits(nv - 64 * hf - 32));
-        const bool full = __all_sync(0xffffffffu, (k0 & k1) == 0xffffffffu);
-        // S of this half-row stays in registers from the max to the exponentials
-        float mx = -INFINITY;
-        uint32_t s0[32], s1[32];
-        if (got) {
-          tmem_ld32(lb + col_s(t & 1) + 64 * hf, s0);
-          tmem_ld32(lb + col_s(t & 1) + 64 * hf + 32, s1);
+      for (int i = 0; i < 4; ++i) km[i] = !vrow ? 0u : (tree ? tw[i] : low_bits(nv - 32 * i));
+      const bool full = __all_sync(0xffffffffu, (km[0] & km[1] & km[2] & km[3]) == 0xffffffffu);
+      const uint32_t sc = lb + col_s(wg);
+      // keys 64..127 stay in registers from the max to the exponentials; keys 0..63
+      // are read again after their max is known
+      uint32_t s0[32], s1[32], s2[32], s3[32];
+      tmem_ld32(sc, s0);
+      tmem_ld32(sc + 32, s1);
+      tmem_ld32(sc + 64, s2);
+      tmem_ld32(sc + 96, s3);
+      tmem_ld_wait();
+      if (!full) {
+        mask_keys(s0, km[0]);
+        mask_keys(s1, km[1]);
+        mask_keys(s2, km[2]);
+        mask_keys(s3, km[3]);
+      }
+      const float mx = fmaxf(max64(s0, s1), max64(s2, s3));
+      const float m_new = fmaxf(m_ref, mx);
+      // lazy rescale: move the row's reference max only when it grew by > 2^8.  O(wg)
+      // holds this warpgroup's earlier tiles; their PV finished before S of this tile
+      // did (in-order tensor pipe, one commit covers every earlier MMA).  tcgen05.ld/st
+      // are warp-collective, so the whole warp touches O when any of its rows must.
+      const bool move = m_new != -INFINITY && (m_ref == -INFINITY || (m_new - m_ref) * sl2 > kRescaleLog2);
+      const bool scale_o = move && m_ref != -INFINITY;
+      const float alpha = scale_o ? ex2((m_ref - m_new) * sl2) : 1.f;
+      if (__any_sync(0xffffffffu, scale_o)) {
+        l *= alpha;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t o[32];
+          tmem_ld32(lb + col_o(wg) + 32 * c, o);
           tmem_ld_wait();
-          if (!full) {
-            mask_keys(s0, k0);
-            mask_keys(s1, k1);
-          }
-          mx = max64(s0, s1);
-        }
-        s_red[t & 1][i][hf][r_local] = mx;
-        if (!bar_and(1, 256, got)) {  // every softmax warp leaves together on a timeout
-          ok = false;
-          break;
-        }
-        const float m_new = fmaxf(m_ref[i], fmaxf(mx, s_red[t & 1][i][hf ^ 1][r_local]));
-        // lazy rescale: move the row's reference max only when it grew by > 2^8; O
-        // holds earlier tiles only when m_ref is already finite.  Both halves of a row
-        // decide alike; each rescales its own 64 O columns.  tcgen05.ld/st are
-        // warp-collective, so the whole warp touches O when any of its rows must.
-        const bool move = m_new != -INFINITY && (m_ref[i] == -INFINITY || (m_new - m_ref[i]) * sl2 > kRescaleLog2);
-        const bool scale_o = move && m_ref[i] != -INFINITY;
-        const float alpha = scale_o ? ex2((m_ref[i] - m_new) * sl2) : 1.f;
-        if (__any_sync(0xffffffffu, scale_o)) {
-          // O must hold every earlier tile: wait for PV(t - 1) (PV(t - 2) finished
-          // before S of tile t did).  A timeout only records ERR_O: leaving the loop here
-          // would desert the named barriers the other softmax warps wait on.
-          __syncwarp();
-          (void)wait_parity(&o_done, (t - 1) & 1, a.err, ERR_O);
-          __syncwarp();
-          tc_fence_after();
-          l[i] *= alpha;
 #pragma unroll
-          for (int c = 0; c < 2; ++c) {
-            uint32_t o[32];
-            tmem_ld32(lb + COL_O + 64 * hf + 32 * c, o);
-            tmem_ld_wait();
-#pragma unroll
-            for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha);
-            tmem_st32(lb + COL_O + 64 * hf + 32 * c, o);
-          }
-          tmem_st_wait();
-        }
-        if (move) m_ref[i] = m_new;
-        const float mu = (m_ref[i] == -INFINITY) ? 0.f : m_ref[i] * sl2;
-        // P = 2^(s c - m c) from the S held in registers, as bf16 pairs (masked keys hold
-        // -inf and give exactly 0): keys 64 hf + 32 c .. + 31 go to columns
-        // 64 hf + 16 c .. + 15; the precise path puts the low parts 32 columns further
-        // on.  l sums the fp32 p (the precise path: hi + lo).
-        float ls[4] = {0.f, 0.f, 0.f, 0.f};
-        uint64_t ls2[2] = {0ull, 0ull};  // standard path: packed row-sum accumulators
-        const uint64_t sl2x2 = f32x2(__float_as_uint(sl2), __float_as_uint(sl2));
-        const uint64_t nmux2 = f32x2(__float_as_uint(-mu), __float_as_uint(-mu));
-        auto emit = [&](const uint32_t (&r)[32], int c) {
-          uint32_t hi[16];
-          if constexpr (!PRECISE) {
-            // two keys per packed instruction: x = s c - m c, then 2^x on the MUFU
-#pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              float x0, x1;
-              f32x2_split(fma_f32x2(f32x2(r[2 * j], r[2 * j + 1]), sl2x2, nmux2), x0, x1);
-              const float p0 = ex2(x0), p1 = ex2(x1);
-              __nv_bfloat162 u = __floats2bfloat162_rn(p0, p1);
-              hi[j] = *reinterpret_cast<uint32_t*>(&u);
-              ls2[j & 1] = add_f32x2(ls2[j & 1], f32x2(__float_as_uint(p0), __float_as_uint(p1)));
-            }
-            tmem_st16(lb + col_s(t & 1) + 64 * hf + 16 * c, hi);
-          } else {
-            // P = hi + lo, both bf16; the low parts go 32 columns after the high ones
-            uint32_t lo[16];
-#pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              const float p0 = ex2(fmaf(__uint_as_float(r[2 * j]), sl2, -mu));
-              const float p1 = ex2(fmaf(__uint_as_float(r[2 * j + 1]), sl2, -mu));
-              __nv_bfloat162 u = __floats2bfloat162_rn(p0, p1);
-              hi[j] = *reinterpret_cast<uint32_t*>(&u);
-              const float h0 = __uint_as_float(hi[j] << 16), h1 = __uint_as_float(hi[j] & 0xffff0000u);
-              __nv_bfloat162 w = __floats2bfloat162_rn(p0 - h0, p1 - h1);
-              lo[j] = *reinterpret_cast<uint32_t*>(&w);
-              ls[j & 3] += (h0 + __uint_as_float(lo[j] << 16)) + (h1 + __uint_as_float(lo[j] & 0xffff0000u));
-            }
-            tmem_st16(lb + col_s(t & 1) + 64 * hf + 16 * c, hi);
-            tmem_st16(lb + col_s(t & 1) + 64 * hf + 32 + 16 * c, lo);
-          }
-        };
-        emit(s0, 0);
-        emit(s1, 1);
-        if constexpr (!PRECISE) {
-          float a0, a1, b0, b1;
-          f32x2_split(ls2[0], a0, a1);
-          f32x2_split(ls2[1], b0, b1);
-          l[i] += (a0 + a1) + (b0 + b1);
-        } else {
-          l[i] += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+          for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
+          tmem_st32(lb + col_o(wg) + 32 * c, o);
         }
         tmem_st_wait();
-        tc_fence_before();
-        mbar_arrive(&p_full[t & 1]);
       }
+      if (move) m_ref = m_new;
+      const float mu = (m_ref == -INFINITY) ? 0.f : m_ref * sl2;
+      const uint64_t nmux2 = f32x2(__float_as_uint(-mu), __float_as_uint(-mu));
+      // P of keys 64 h + 32 c .. + 31 goes to columns 64 h + 16 c .. + 15 (low parts
+      // 32 columns further on); keys 64..127 first, whose S columns are already read
+      float ls = emit_p32<PRECISE>(s2, sc + 64, sl2x2, nmux2);
+      ls += emit_p32<PRECISE>(s3, sc + 80, sl2x2, nmux2);
+      tmem_ld32(sc, s0);
+      tmem_ld32(sc + 32, s1);
+      tmem_ld_wait();
+      if (!full) {
+        mask_keys(s0, km[0]);
+        mask_keys(s1, km[1]);
+      }
+      ls += emit_p32<PRECISE>(s0, sc, sl2x2, nmux2);
+      ls += emit_p32<PRECISE>(s1, sc + 16, sl2x2, nmux2);
+      l += ls;
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(&p_full[wg]);
     }
-    // ---- epilogue: O from TMEM to the output (one split) or the partials
-    const bool have = ok && ti.n_tiles > 0;
-    const bool done = have ? __all_sync(0xffffffffu, wait_parity(&o_full, 0, a.err, ERR_O)) : false;
+    // ---- epilogue: the two warpgroups' states merge; warpgroup j writes dims
+    // [64 j, 64 j + 64) of its row to the output (one split) or the partials
+    const bool have = ti.n_tiles > 0;
+    const bool done = have && ok ? __all_sync(0xffffffffu, wait_parity(&o_full, 0, a.err, ERR_O)) : false;
     tc_fence_after();
+    s_m[wg][r_local] = m_ref;
+    s_l[wg][r_local] = l;
+    const bool all_done = bar_and(1, 256, done) && have;
+    const float mA = s_m[0][r_local], mB = s_m[1][r_local];
+    const float M = fmaxf(mA, mB);
+    const float aA = mA == -INFINITY ? 0.f : ex2((mA - M) * sl2);
+    const float aB = mB == -INFINITY ? 0.f : ex2((mB - M) * sl2);
+    const float L = aA * s_l[0][r_local] + aB * s_l[1][r_local];
+    const bool two = ti.n_tiles > 1;  // O(1) holds tiles only when there are two or more
+    float o[64];
+    if (all_done) {
+      uint32_t x[32], y[32];
 #pragma unroll
-    for (int i = 0; i < 2; ++i) s_l[i][hf][r_local] = l[i];
-    const bool all_done = bar_and(2, 256, done);
-    float l_tot[2];
+      for (int c = 0; c < 2; ++c) {
+        tmem_ld32(lb + col_o(0) + 64 * wg + 32 * c, x);
+        if (two) tmem_ld32(lb + col_o(1) + 64 * wg + 32 * c, y);
+        tmem_ld_wait();
 #pragma unroll
-    for (int i = 0; i < 2; ++i) l_tot[i] = l[i] + s_l[i][hf ^ 1][r_local];
-    if (a.splits > 1 && all_done) {
-      // partial O of each M-tile (128 rows, contiguous in the workspace) is staged in
-      // the free K/V stages as 128-byte-swizzled column slices (fp32: four slices of
-      // 32 columns; bf16: two of 64), then stored with one TMA store per slice.  Row
-      // r's 16-byte chunk j sits at chunk j ^ (r & 7), so each quarter-warp store
-      // covers all 32 banks.
+        for (int k = 0; k < 32; ++k)
+          o[32 * c + k] = two ? fmaf(aA, __uint_as_float(x[k]), aB * __uint_as_float(y[k])) : aA * __uint_as_float(x[k]);
+      }
+    } else {
 #pragma unroll
-      for (int i = 0; i < 2; ++i) {
-        if (i >= n_mt) break;
-        uint8_t* so = smem + SM_K + i * 4 * HALF;
-        if (a.part_bf16) {
-          uint32_t o0[32], o1[32];
-          tmem_ld32(lb + COL_O + 64 * hf, o0);
-          tmem_ld32(lb + COL_O + 64 * hf + 32, o1);
-          tmem_ld_wait();
-          uint8_t* dst = so + hf * HALF + r_local * 128;
+      for (int k = 0; k < 64; ++k) o[k] = 0.f;
+    }
+    const size_t prow = (static_cast<size_t>(bh) * a.splits + split) * a.rows_pad + rb * 128 + r_local;
+    if (a.splits == 1) {
+      if (vrow && all_done) {
+        const float inv = L > 0.f ? 1.f / L : 0.f;
+        const size_t orow = (static_cast<size_t>(b * a.R + node) * a.Hq + hq) * 128 + 64 * wg;
+        if (a.out_f32) {
+          float4* dst = reinterpret_cast<float4*>(static_cast<float*>(a.out) + orow);
 #pragma unroll
-          for (int j = 0; j < 8; ++j) {
+          for (int k = 0; k < 16; ++k)
+            dst[k] = make_float4(o[4 * k] * inv, o[4 * k + 1] * inv, o[4 * k + 2] * inv, o[4 * k + 3] * inv);
+        } else {
+          uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.out) + orow);
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
             uint32_t w[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-              const uint32_t* src = (j < 4) ? o0 : o1;
-              const int k = 8 * (j & 3) + 2 * e;
-              __nv_bfloat162 u = __floats2bfloat162_rn(__uint_as_float(src[k]), __uint_as_float(src[k + 1]));
+              __nv_bfloat162 u = __floats2bfloat162_rn(o[8 * k + 2 * e] * inv, o[8 * k + 2 * e + 1] * inv);
               w[e] = *reinterpret_cast<uint32_t*>(&u);
             }
-            *reinterpret_cast<uint4*>(dst + ((j ^ (r_local & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
-          }
-        } else {
-#pragma unroll
-          for (int cc = 0; cc < 2; ++cc) {
-            const int c = 2 * hf + cc;
-            uint32_t o[32];
-            tmem_ld32(lb + COL_O + 32 * c, o);
-            tmem_ld_wait();
-            uint8_t* dst = so + c * HALF + r_local * 128;
-#pragma unroll
-            for (int j = 0; j < 8; ++j)
-              *reinterpret_cast<uint4*>(dst + ((j ^ (r_local & 7)) << 4)) =
-                  make_uint4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
+            dst[k] = make_uint4(w[0], w[1], w[2], w[3]);
           }
         }
+        if (a.lse && wg == 0) a.lse[static_cast<size_t>(b * a.R + node) * a.Hq + hq] = a.scale * M + logf(L);
+      }
+    } else if (all_done) {
+      // partial O of the M-tile (128 rows, contiguous in the workspace) staged in the
+      // free K stages as four 128-byte-swizzled slices of 32 fp32 columns, then stored
+      // with one TMA store per slice.  Row r's 16-byte chunk q sits at chunk q ^ (r & 7),
+      // so each quarter-warp store covers all 32 banks.
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        uint8_t* dst = smem + SM_K + (2 * wg + c) * HALF + r_local * 128;
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          *reinterpret_cast<float4*>(dst + ((q ^ (r_local & 7)) << 4)) =
+              make_float4(o[32 * c + 4 * q], o[32 * c + 4 * q + 1], o[32 * c + 4 * q + 2], o[32 * c + 4 * q + 3]);
       }
       fence_proxy_async_smem();
-      bar_sync(2, 256);
+      bar_sync(1, 256);
       if (threadIdx.x == 0) {
-        for (int i = 0; i < n_mt; ++i) {
-          const int y = (bh * a.splits + split) * a.rows_pad + rb * a.rows_per_cta + i * 128;
-          const int slices = a.part_bf16 ? 2 : 4;
-          for (int c = 0; c < slices; ++c)
-            tma_store_2d(&tm.po, smem + SM_K + i * 4 * HALF + c * HALF, (a.part_bf16 ? 64 : 32) * c, y);
-        }
+        const int y = (bh * a.splits + split) * a.rows_pad + rb * 128;
+        for (int c = 0; c < 4; ++c) tma_store_2d(&tm.po, smem + SM_K + c * HALF, 32 * c, y);
         bulk_commit();
         if (a.coop)
           bulk_wait0();  // other CTAs read these rows
         else
           bulk_wait_read0();
       }
-      if (hf == 0) {
+      if (wg == 0 && vrow) *reinterpret_cast<float2*>(a.part_ml + prow * 2) = make_float2(M, L);
+    } else if (!(a.tps > 0 && ti.n_tiles == 0) && vrow) {
+      // a split with no tiles (or one that timed out): zeros and weight 0; a split past
+      // its request's last unit (fixed-size splits) writes nothing
+      float4* dst = reinterpret_cast<float4*>(a.part_o + prow * 128 + 64 * wg);
 #pragma unroll
-        for (int i = 0; i < 2; ++i) {
-          if (!vrow[i]) continue;
-          const size_t prow = (static_cast<size_t>(bh) * a.splits + split) * a.rows_pad + rb * a.rows_per_cta + i * 128 + r_local;
-          *reinterpret_cast<float2*>(a.part_ml + prow * 2) = make_float2(m_ref[i], l_tot[i]);
-        }
-      }
-    } else if (!(a.tps > 0 && ti.n_tiles == 0)) {  // a split past its request's last unit writes nothing
-#pragma unroll
-      for (int i = 0; i < 2; ++i) {
-        if (i >= n_mt) break;
-        const float inv = (a.splits == 1 && l_tot[i] > 0.f) ? 1.f / l_tot[i] : 1.f;
-        const size_t prow = (static_cast<size_t>(bh) * a.splits + split) * a.rows_pad + rb * a.rows_per_cta + i * 128 + r_local;
-#pragma unroll
-        for (int cc = 0; cc < 2; ++cc) {
-          const int c = 2 * hf + cc;
-          uint32_t o[32];
-          if (all_done) {
-            tmem_ld32(lb + COL_O + 32 * c, o);
-            tmem_ld_wait();
-          } else {
-#pragma unroll
-            for (int j = 0; j < 32; ++j) o[j] = 0u;
-          }
-          if (!vrow[i]) continue;
-          if (a.splits == 1) {
-            const size_t orow = (static_cast<size_t>(b * a.R + node[i]) * a.Hq + hq[i]) * 128 + 32 * c;
-            if (a.out_f32) {
-              float4* dst = reinterpret_cast<float4*>(static_cast<float*>(a.out) + orow);
-#pragma unroll
-              for (int j = 0; j < 8; ++j)
-                dst[j] = make_float4(__uint_as_float(o[4 * j]) * inv, __uint_as_float(o[4 * j + 1]) * inv,
-                                     __uint_as_float(o[4 * j + 2]) * inv, __uint_as_float(o[4 * j + 3]) * inv);
-            } else {
-              uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.out) + orow);
-#pragma unroll
-              for (int j = 0; j < 4; ++j) {
-                uint32_t w[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                  __nv_bfloat162 u = __floats2bfloat162_rn(__uint_as_float(o[8 * j + 2 * e]) * inv,
-                                                           __uint_as_float(o[8 * j + 2 * e + 1]) * inv);
-                  w[e] = *reinterpret_cast<uint32_t*>(&u);
-                }
-                dst[j] = make_uint4(w[0], w[1], w[2], w[3]);
-              }
-            }
-          } else if (a.part_bf16) {  // a timed-out split: zeros (its weight is 0 too)
-            uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.part_o) + prow * 128 + 32 * c);
-#pragma unroll
-            for (int j = 0; j < 4; ++j) dst[j] = make_uint4(0u, 0u, 0u, 0u);
-          } else {
-            float4* dst = reinterpret_cast<float4*>(static_cast<float*>(a.part_o) + prow * 128 + 32 * c);
-#pragma unroll
-            for (int j = 0; j < 8; ++j)
-              dst[j] = make_float4(__uint_as_float(o[4 * j]), __uint_as_float(o[4 * j + 1]),
-                                   __uint_as_float(o[4 * j + 2]), __uint_as_float(o[4 * j + 3]));
-          }
-        }
-        if (vrow[i] && hf == 0) {
-          if (a.splits == 1) {
-            if (a.lse) a.lse[static_cast<size_t>(b * a.R + node[i]) * a.Hq + hq[i]] = a.scale * m_ref[i] + logf(l_tot[i]);
-          } else {
-            *reinterpret_cast<float2*>(a.part_ml + prow * 2) =
-                make_float2(all_done ? m_ref[i] : -INFINITY, all_done ? l_tot[i] : 0.f);
-          }
-        }
-      }
+      for (int k = 0; k < 16; ++k) dst[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (wg == 0) *reinterpret_cast<float2*>(a.part_ml + prow * 2) = make_float2(-INFINITY, 0.f);
     }
     if (a.coop) {
       // the group's merge: publish this split's partials (all writes fenced, then one
       // release-ordered count), wait until every split of this (request, KV head, row
       // block) has counted, then merge rows [split n / S, (split + 1) n / S) of the
-      // block from the partials in L2, a warp per row: M = max m_s,
-      // w_s = 2^((m_s - M) c), O = sum w_s O_s / sum w_s l_s
+      // block from the partials in L2, a half-warp per row
       fence_proxy_async_global();
       __threadfence();
-      bar_sync(2, 256);
+      bar_sync(1, 256);
       const int grp = bh * gridDim.z + rb;
       if (threadIdx.x == 0) {
-        s_go = group_arrive_wait(a.cnt + grp, a.splits, a.err) ? 1 : 0;
+        s_go = group_arrive_wait(a.cnt + grp, a.group_need, a.err, a.group_limit_ns) ? 1 : 0;
         // past the wait: the last split of the group to get here returns both counters
         // to zero for the next call
-        int* done = a.cnt + a.n_groups + grp;
-        if (atomicAdd(done, 1) == a.splits - 1) {
+        int* fin = a.cnt + a.n_groups + grp;
+        if (atomicAdd(fin, 1) == a.splits - 1) {
           atomicExch(a.cnt + grp, 0);
-          atomicExch(done, 0);
+          atomicExch(fin, 0);
         }
       }
-      bar_sync(2, 256);
+      bar_sync(1, 256);
       if (s_go) {
-        const int n = min(a.rows_per_cta, a.R * a.G - rb * a.rows_per_cta);
+        const int n = min(128, ti.Rb * a.G - rb * 128);
+        const int lo = split * n / a.splits;
         const int hi = (split + 1) * n / a.splits;
         // a half-warp per row; both halves of a warp loop together (shuffles are
         // warp-collective), the spare half on a row of its own block with no output
-        const int lo = split * n / a.splits;
         for (int s0 = lo + 2 * warp; s0 < hi; s0 += 16) {
           const int lr = s0 + (lane >> 4);
-          const int grow = lr < hi ? rb * a.rows_per_cta + lr : -1;
-          if (a.part_bf16)
-            merge_row_hw<true>(a, bh, h, b, grow < 0 ? -1 : grow, lane & 15, sl2);
-          else
-            merge_row_hw<false>(a, bh, h, b, grow < 0 ? -1 : grow, lane & 15, sl2);
+          const int grow = lr < hi ? rb * 128 + lr : -1;
+          merge_row_hw(a, bh, h, b, grow, lane & 15, sl2);
         }
       }
     }
@@ -885,7 +805,8 @@ cudaError_t launch_tc(const Tmaps& tm, const TcArgs& a, dim3 grid, cudaStream_t 
 
 cudaError_t launch_tree_attn_tc(const AttnPlan& p, const void* q, const void* k_cache, const void* v_cache,
                                 const void* tree_k, const void* tree_v, const int32_t* seq_len,
-                                const uint64_t* anc_mask, void* out, float* lse, void* ws, cudaStream_t s) {
+                                const int32_t* n_nodes, const uint64_t* anc_mask, void* out, float* lse, void* ws,
+                                cudaStream_t s) {
   Tmaps tm;
   const cuuint64_t D = 128;
   {
@@ -912,20 +833,19 @@ cudaError_t launch_tree_attn_tc(const AttnPlan& p, const void* q, const void* k_
   memset(&tm.po, 0, sizeof(tm.po));
   if (p.splits > 1) {
     const cuuint64_t dims[2] = {D, static_cast<cuuint64_t>(p.B) * p.Hkv * p.splits * p.rows_pad};
-    const cuuint64_t strides[1] = {D * (p.part_bf16 ? 2 : 4)};
-    const cuuint32_t box[2] = {p.part_bf16 ? 64u : 32u, 128};
-    if (!make_tmap(&tm.po, p.part_bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, w + p.off_o,
-                   2, dims, strides, box))
+    const cuuint64_t strides[1] = {D * 4};
+    const cuuint32_t box[2] = {32u, 128};
+    if (!make_tmap(&tm.po, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, w + p.off_o, 2, dims, strides, box))
       return cudaErrorInvalidValue;
   }
   TcArgs a;
   a.seq_len = seq_len;
+  a.n_nodes = n_nodes;
   a.anc_mask = anc_mask;
   a.out = out;
   a.lse = lse;
   const bool partials = p.splits > 1;
-  a.part_o = partials ? static_cast<void*>(w + p.off_o) : nullptr;
-  a.part_bf16 = p.part_bf16 ? 1 : 0;
+  a.part_o = partials ? reinterpret_cast<float*>(w + p.off_o) : nullptr;
   a.part_ml = partials ? reinterpret_cast<float*>(w + p.off_ml) : nullptr;
   a.err = reinterpret_cast<int*>(w + p.off_err);
   a.B = p.B;
@@ -937,13 +857,15 @@ cudaError_t launch_tree_attn_tc(const AttnPlan& p, const void* q, const void* k_
   a.W = p.W;
   a.splits = p.splits;
   a.rows_pad = p.rows_pad;
-  a.rows_per_cta = p.rows_per_cta;
-  a.n_mt = p.rows_per_cta / 128;
   a.coop = p.coop ? 1 : 0;
   a.tps = p.tps;
   a.lpt = p.lpt ? 1 : 0;
   a.cnt = p.coop ? reinterpret_cast<int*>(w + p.off_cnt) : nullptr;
   a.n_groups = p.B * p.Hkv * p.row_blocks;
+  // the failure test hook: the group waits for one split that does not exist and gives
+  // up after 1 ms
+  a.group_need = p.splits + (p.fault_test ? 1 : 0);
+  a.group_limit_ns = p.fault_test ? 1000000ull : 2000000000ull;
   a.out_f32 = p.out_dtype == EAGLE_F32;
   a.scale = p.scale;
   a.scale_log2 = p.scale * kLog2e;
@@ -951,7 +873,7 @@ cudaError_t launch_tree_attn_tc(const AttnPlan& p, const void* q, const void* k_
   const dim3 grid = p.coop ? dim3(p.splits, p.B * p.Hkv, p.row_blocks) : dim3(p.row_blocks, p.splits, p.B * p.Hkv);
   e = p.precise ? launch_tc<true>(tm, a, grid, s) : launch_tc<false>(tm, a, grid, s);
   if (e != cudaSuccess || !partials || p.coop) return e;
-  return launch_tree_attn_combine(p, seq_len, out, lse, static_cast<const float*>(a.part_o), a.part_ml, s);
+  return launch_tree_attn_combine(p, seq_len, n_nodes, out, lse, static_cast<const float*>(a.part_o), a.part_ml, s);
 }
 
 }  // namespace eagle

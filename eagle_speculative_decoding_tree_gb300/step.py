@@ -129,7 +129,7 @@ class VerifyStep:
 
     def __init__(self, w: synth.Workload, batch: Optional[int] = None, layers: Optional[int] = None,
                  device="cuda", q_scale: float = 1.0, num_splits: int = 0, tree: Optional[dict] = None,
-                 keep_host: bool = False, precision: int = B.EAGLE_ATTN_STANDARD):
+                 keep_host: bool = False, precision: int = B.EAGLE_ATTN_PRECISE):
         self.w = w
         self.B = batch if batch is not None else w.batch
         self.L = layers if layers is not None else w.layers

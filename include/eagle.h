@@ -96,9 +96,13 @@ enum {
 
 /* Precision of the attention PV product (bf16 path) */
 enum {
-  EAGLE_ATTN_STANDARD = 0, /* P rounded to bf16 (8 significant bits), as flash attention does */
-  EAGLE_ATTN_PRECISE = 1   /* P split into two bf16 terms (hi + lo, ~16 bits): one extra MMA per PV
-                              step; for sharply peaked rows where bf16 rounding of P shows */
+  EAGLE_ATTN_PRECISE = 0, /* default: P enters the PV product as two bf16 terms (hi + lo, about 16
+                             significant bits; one extra MMA per PV step) and split partials stay
+                             fp32, so the only bf16 rounding after the inputs is that of a bf16
+                             output: max abs error 2e-3 + 2^-8 |O| against exact arithmetic */
+  EAGLE_ATTN_FAST = 1     /* P rounded to bf16 once (8 significant bits), as flash attention does:
+                             cheaper, but on sharply peaked rows the rounding of P moves O by up to
+                             2^-8 max|v| */
 };
 
 /* Attention kernel selection.  The tcgen05 kernel covers bf16 inputs with head_dim 128
@@ -175,18 +179,28 @@ typedef struct {
                           when the grid fits on the SMs at once, else key pieces of a fixed
                           number of tiles per request */
   int32_t out_dtype;   /* element type of out: EAGLE_F32, or EAGLE_BF16 when dtype is EAGLE_BF16 */
-  int32_t precision;   /* EAGLE_ATTN_STANDARD or EAGLE_ATTN_PRECISE (ignored for fp32 inputs) */
+  int32_t precision;   /* EAGLE_ATTN_PRECISE (0, default) or EAGLE_ATTN_FAST (ignored for fp32 inputs) */
   int32_t engine;      /* EAGLE_ENGINE_AUTO (tensor-core tcgen05 kernel where supported) or
                           EAGLE_ENGINE_MMA_SYNC (the legacy warp-level MMA kernel) */
+  int32_t fault_test;  /* 0 in normal use.  1 is a test hook for the failure path of the
+                          tcgen05 kernel's in-kernel split merge: each split group waits for
+                          one split more than exist and gives up after 1 ms, so the call
+                          returns with bit 0x100 set in the workspace error word and the
+                          outputs unwritten (re-zero the workspace afterwards).  No effect
+                          when the splits do not merge in the kernel. */
 } eagle_attn_desc;
 
 /* One layer of tree attention.  Row i of request b, query head hq attends to the
- * prefix keys j < seq_len[b] of KV head hq / G and to the tree keys a whose bit is
- * set in anc_mask[b][i]:
+ * prefix keys j < seq_len[b] of KV head hq / G and to the tree keys a < n_nodes[b]
+ * whose bit is set in anc_mask[b][i]:
  *     out = softmax(scale * q k^T) v,   lse = ln sum exp(scale * q k^T)  (natural log)
  *   q [B][R][Hq][D]; k_cache, v_cache [B][Hkv][P][D]; tree_k, tree_v [B][Hkv][R][D];
  *   seq_len [B] int32 (0 <= seq_len <= P); anc_mask [B][R][W]; out [B][R][Hq][D];
  *   lse [B][R][Hq] fp32, may be NULL.
+ *   n_nodes [B] int32, may be NULL (every request has R rows): request b's tree has
+ *   n_nodes[b] rows (clamped to [0, R]), so requests with trees of different sizes
+ *   share one call; rows i >= n_nodes[b] of out and lse are left untouched and the
+ *   tree keys >= n_nodes[b] are ignored whatever their mask bits say.
  * ws: eagle_workspace_size(EAGLE_WS_TREE_ATTN, d) bytes (split partials and, for the
  * tcgen05 kernel, an error word and split-group counters), zero-filled by the caller
  * before its first use; every call leaves the counters at zero again.  The tcgen05
@@ -200,7 +214,7 @@ typedef struct {
  * Unsupported: head_dim not 64/128, R > 128, Hq % Hkv != 0, B * Hkv > 65535, bf16 out
  * with fp32 inputs. */
 int eagle_tree_attn(const eagle_attn_desc* d, const void* q, const void* k_cache, const void* v_cache,
-                    const void* tree_k, const void* tree_v, const int32_t* seq_len,
+                    const void* tree_k, const void* tree_v, const int32_t* seq_len, const int32_t* n_nodes,
                     const uint64_t* anc_mask, void* out, float* lse, void* ws, size_t ws_bytes,
                     void* stream);
 

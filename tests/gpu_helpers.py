@@ -34,22 +34,27 @@ def random_tree(rows: int, seed: int, chain: bool = False):
 
 def run_attn(w: synth.Workload, batch: int, seq_len: np.ndarray, rows: int, parent: np.ndarray,
              mask: np.ndarray, layer: int = 0, q_scale: float = 1.0, num_splits: int = 0, out_f32: bool = False,
-             precision: int = B.EAGLE_ATTN_STANDARD, engine: int = B.EAGLE_ENGINE_AUTO):
-    """Generate one layer's inputs and run eagle_tree_attn; returns host inputs and outputs."""
+             precision: int = B.EAGLE_ATTN_PRECISE, engine: int = B.EAGLE_ENGINE_AUTO, n_nodes=None,
+             fault_test: int = 0, ws=None):
+    """Generate one layer's inputs and run eagle_tree_attn; returns host inputs and outputs
+    (n_nodes: per-request tree sizes; ws: a workspace to reuse, else a zeroed one)."""
     q, kc, vc, tk, tv = synth.attn_tensors(w, layer, batch, seq_len, rows, q_scale)
     dt = B.EAGLE_F32 if w.dtype == "f32" else B.EAGLE_BF16
     odt = B.EAGLE_F32 if (out_f32 or w.dtype == "f32") else B.EAGLE_BF16
     desc = B.AttnDesc(batch, rows, w.n_q_heads, w.n_kv_heads, w.head_dim, w.max_seq, 1.0 / math.sqrt(w.head_dim),
-                      dt, num_splits, odt, precision, engine)
-    ws = torch.zeros(B.workspace_size(B.EAGLE_WS_TREE_ATTN, desc), dtype=torch.uint8, device="cuda")
+                      dt, num_splits, odt, precision, engine, fault_test)
+    if ws is None:
+        ws = torch.zeros(B.workspace_size(B.EAGLE_WS_TREE_ATTN, desc), dtype=torch.uint8, device="cuda")
     tq = dev(q, w.dtype)
-    out = torch.empty(tq.shape, dtype=torch.float32 if odt == B.EAGLE_F32 else torch.bfloat16, device="cuda")
+    out = torch.full(tq.shape, float("nan"), dtype=torch.float32 if odt == B.EAGLE_F32 else torch.bfloat16,
+                     device="cuda")
     lse = torch.empty(batch, rows, w.n_q_heads, dtype=torch.float32, device="cuda")
     am = torch.from_numpy(np.broadcast_to(mask, (batch,) + mask.shape[-2:]).copy().view(np.int64)).cuda()
     B.eagle_tree_attn(desc, tq, dev(kc, w.dtype), dev(vc, w.dtype), dev(tk, w.dtype), dev(tv, w.dtype),
-                      torch.from_numpy(np.asarray(seq_len, np.int32)).cuda(), am, out, lse, ws)
+                      torch.from_numpy(np.asarray(seq_len, np.int32)).cuda(), am, out, lse, ws,
+                      n_nodes=None if n_nodes is None else torch.from_numpy(np.asarray(n_nodes, np.int32)).cuda())
     torch.cuda.synchronize()
-    if ws.numel() >= 4:  # the tensor-core kernel's error word (bounded waits that gave up)
+    if ws.numel() >= 4 and not fault_test:  # the tensor-core kernel's error word (bounded waits that gave up)
         assert int(ws[:4].view(torch.int32).item()) == 0 or not is_tc(desc), "tcgen05 kernel wait timed out"
     return (q, kc, vc, tk, tv), out.float().cpu().numpy(), lse.cpu().numpy()
 

@@ -58,7 +58,7 @@ def _attn(**kw):
 
 
 def _call_attn(lib, desc, q=A, ws=A, ws_bytes=0, lse=None):
-    return lib.eagle_tree_attn(ctypes.byref(desc), q, A, A, A, A, A, A, A, lse, ws, ws_bytes, None)
+    return lib.eagle_tree_attn(ctypes.byref(desc), q, A, A, A, A, A, None, A, A, lse, ws, ws_bytes, None)
 
 
 @pytest.mark.parametrize("kw,code", [
@@ -71,6 +71,7 @@ def _call_attn(lib, desc, q=A, ws=A, ws_bytes=0, lse=None):
     (dict(num_splits=-1), B.EAGLE_ERR_INVALID_ARG),
     (dict(dtype=0, out_dtype=1), B.EAGLE_ERR_UNSUPPORTED),
     (dict(precision=2), B.EAGLE_ERR_INVALID_ARG),
+    (dict(fault_test=2), B.EAGLE_ERR_INVALID_ARG),
 ])
 def test_attn_rejects_bad_descriptors(lib, kw, code):
     assert _call_attn(lib, _attn(**kw)) == code
