@@ -58,8 +58,10 @@ int report_cuda_error(cudaError_t e);
 
 void plan_tree_attn(const eagle_attn_desc* d, int num_sms, AttnPlan* p);
 // Merge split partials into out / lse (shared by the mma.sync and tcgen05 kernels).
+// pdl: programmatic launch (waits for the preceding kernel inside, lets the next start early)
 cudaError_t launch_tree_attn_combine(const AttnPlan& p, const int32_t* seq_len, const int32_t* n_nodes, void* out,
-                                     float* lse, const float* part_o, const float* part_ml, cudaStream_t s);
+                                     float* lse, const float* part_o, const float* part_ml, cudaStream_t s,
+                                     bool pdl = false);
 // The tcgen05 kernel (plan.tc); ws holds the error word and the partials.
 cudaError_t launch_tree_attn_tc(const AttnPlan& p, const void* q, const void* k_cache, const void* v_cache,
                                 const void* tree_k, const void* tree_v, const int32_t* seq_len,

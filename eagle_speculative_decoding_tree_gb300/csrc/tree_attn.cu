@@ -362,7 +362,10 @@ __global__ void __launch_bounds__(NW * 32, (NW == 4) ? 2 : 1) tree_attn_mma_kern
 template <int D>
 __global__ void __launch_bounds__(128) tree_attn_combine_kernel(const AttnArgs a) {
   constexpr int PER = D / 32;
-  constexpr int BATCH = 32;
+  constexpr int BATCH = 16;
+  // a programmatic launch: the partials belong to the preceding kernel until it ends
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int r = blockIdx.x * 4 + warp;
   const int bh = blockIdx.y;
@@ -423,12 +426,15 @@ __global__ void __launch_bounds__(128) tree_attn_combine_kernel(const AttnArgs a
 #pragma unroll
     for (int e = 0; e < PER; ++e) acc[e] = fmaf(w, v[u][e], acc[e]);
   }
-  for (int s0 = BATCH; s0 < n_act; s0 += 8) {  // splits beyond 32: eight at a time
+  for (int s0 = BATCH; s0 < n_act; s0 += 8) {  // splits beyond the first batch: eight at a time
     float x[8][PER], wv[8];
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
       const int s = s0 + u;
-      wv[u] = __shfl_sync(0xffffffffu, w2[1], s & 31);
+      // split s's weight sits in lane s & 31 of w2[s >> 5]
+      const float w_lo = __shfl_sync(0xffffffffu, w2[0], s & 31);
+      const float w_hi = __shfl_sync(0xffffffffu, w2[1], s & 31);
+      wv[u] = (s >> 5) ? w_hi : w_lo;
       const bool in = s < n_act;
       const float* po = po0 + static_cast<size_t>(in ? s : 0) * sstride;
 #pragma unroll
@@ -615,7 +621,7 @@ void plan_tree_attn(const eagle_attn_desc* d, int num_sms, AttnPlan* p) {
 }
 
 cudaError_t launch_tree_attn_combine(const AttnPlan& p, const int32_t* seq_len, const int32_t* n_nodes, void* out,
-                                     float* lse, const float* part_o, const float* part_ml, cudaStream_t s) {
+                                     float* lse, const float* part_o, const float* part_ml, cudaStream_t s, bool pdl) {
   AttnArgs a{};
   a.seq_len = seq_len;
   a.n_nodes = n_nodes;
@@ -636,11 +642,18 @@ cudaError_t launch_tree_attn_combine(const AttnPlan& p, const int32_t* seq_len, 
   a.out_f32 = p.out_dtype == EAGLE_F32;
   a.scale = p.scale;
   a.scale_log2 = p.scale * kLog2e;
-  dim3 cgrid((p.R * p.G + 3) / 4, p.B * p.Hkv);
-  if (p.D == 64)
-    tree_attn_combine_kernel<64><<<cgrid, 128, 0, s>>>(a);
-  else
-    tree_attn_combine_kernel<128><<<cgrid, 128, 0, s>>>(a);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((p.R * p.G + 3) / 4, p.B * p.Hkv);
+  cfg.blockDim = dim3(128, 1, 1);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  cudaError_t e = p.D == 64 ? cudaLaunchKernelEx(&cfg, tree_attn_combine_kernel<64>, a)
+                            : cudaLaunchKernelEx(&cfg, tree_attn_combine_kernel<128>, a);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

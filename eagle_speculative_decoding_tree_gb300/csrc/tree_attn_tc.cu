@@ -64,7 +64,7 @@ constexpr int HALF = 16384;               // one 64-dim half of a 128-row tile (
 constexpr int TILE = 2 * HALF;            // one K or V tile
 constexpr int NTHREADS = 320;
 constexpr int SM_Q = 0;                   // the 128-row M-tile, 32 KB
-constexpr int KST = 2;                    // K ring stages
+constexpr int KST = 3;                    // K ring stages
 constexpr int VST = 3;                    // V ring stages
 constexpr int SM_K = TILE;
 constexpr int SM_V = SM_K + KST * TILE;
@@ -168,6 +168,14 @@ __device__ int request_of_rank(const TcArgs& a, int r) {
   return res;
 }
 
+// One 128-key K or V tile (rows y .. y + 127 of the tensor map, both 64-dim halves)
+// into a ring stage, completing on `bar`.
+__device__ __forceinline__ void load_kv_tile(const CUtensorMap& m, uint8_t* dst, int y, uint64_t* bar,
+                                             uint64_t policy) {
+  tma_load_2d_hint(dst, &m, 0, y, bar, policy);
+  tma_load_2d_hint(dst + HALF, &m, 64, y, bar, policy);
+}
+
 // Valid keys of tile t (prefix keys before L; tree rows before the request's row count).
 __device__ __forceinline__ int tile_valid(const TileInfo& ti, int t) {
   if (t < ti.n_pt) return min(KT, ti.L - (ti.t_begin + t) * KT);
@@ -181,7 +189,7 @@ __device__ __forceinline__ int tile_valid(const TileInfo& ti, int t) {
 // 8 hl .. 8 hl + 7.  The partial rows of up to kMergeBatch splits are requested before
 // any is used (split indices past the last are clamped; their weight is 0), so a row
 // costs about one L2 round trip.  grow < 0: nothing to write (the loads stay in bounds).
-constexpr int kMergeBatch = 8;
+constexpr int kMergeBatch = 10;
 
 __device__ __forceinline__ void load_part8(const TcArgs& a, size_t prow, int hl, float4 (&w)[2]) {
   const float4* src = reinterpret_cast<const float4*>(a.part_o + prow * 128) + 2 * hl;
@@ -337,7 +345,7 @@ __device__ __forceinline__ void issue_pv(uint32_t tb, const uint8_t* sV, uint32_
 
 // P of 32 keys held in registers (raw scores, masked keys -inf) -> TMEM columns
 // `col` .. (bf16 pairs; the precise low parts 32 columns further on), 16 keys per
-// store.  Returns the row sum of exactly what the PV product multiplies.
+// store.  Returns the fp32 row sum of the 32 values.
 template <bool PRECISE>
 __device__ __forceinline__ float emit_p32(const uint32_t (&r)[32], uint32_t col, uint64_t sl2x2, uint64_t nmux2) {
   float sum = 0.f;
@@ -357,12 +365,9 @@ __device__ __forceinline__ float emit_p32(const uint32_t (&r)[32], uint32_t col,
         const float h0 = __uint_as_float(hi[j] << 16), h1 = __uint_as_float(hi[j] & 0xffff0000u);
         __nv_bfloat162 w = __floats2bfloat162_rn(p0 - h0, p1 - h1);
         lo[j] = *reinterpret_cast<uint32_t*>(&w);
-        // the row sum adds hi + lo, the value the two MMAs multiply
-        acc2 = add_f32x2(acc2, f32x2(__float_as_uint(h0 + __uint_as_float(lo[j] << 16)),
-                                     __float_as_uint(h1 + __uint_as_float(lo[j] & 0xffff0000u))));
-      } else {
-        acc2 = add_f32x2(acc2, f32x2(__float_as_uint(p0), __float_as_uint(p1)));
       }
+      // the row sum adds the fp32 p: hi + lo differs from p by at most 2^-17 p
+      acc2 = add_f32x2(acc2, f32x2(__float_as_uint(p0), __float_as_uint(p1)));
     }
     tmem_st8(col + 8 * g, hi);
     if constexpr (PRECISE) tmem_st8(col + 32 + 8 * g, lo);
@@ -380,8 +385,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   __shared__ uint64_t bar_q, k_full[KST], k_empty[KST], v_full[VST], v_empty[VST], s_full[2], p_full[2], o_full;
   __shared__ uint32_t tmem_base;
-  __shared__ float s_m[2][128], s_l[2][128];  // [tile parity][row] running max and sum
   __shared__ int s_go;                        // group merge: every split published in time
+  // [tile parity][row] running max and sum, exchanged in the epilogue (the Q area: every
+  // QK has completed by then)
+  float (*s_m)[128] = reinterpret_cast<float (*)[128]>(smem + SM_Q);
+  float (*s_l)[128] = reinterpret_cast<float (*)[128]>(smem + SM_Q + 1024);
 
   // grid: cooperative (splits, B Hkv, row blocks); otherwise (row blocks, splits, B Hkv),
   // so that the row blocks of one key range, which read the same K/V tiles, are
@@ -421,6 +429,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   }
   __syncthreads();
   tc_fence_after();
+  int issued_k[KST], issued_v[VST];  // producer: loads issued into each stage
+  for (int s = 0; s < KST; ++s) issued_k[s] = 0;
+  for (int s = 0; s < VST; ++s) issued_v[s] = 0;
   // the inputs (and the workspace counters) belong to the preceding kernel in the
   // stream until it completes
   griddep_wait();
@@ -451,17 +462,15 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       for (int t = 0; t < ti.n_tiles; ++t) {
         const int s = t % KST, use = t / KST, sv = t % VST, usev = t / VST;
         const bool tree = t >= ti.n_pt;
-        const CUtensorMap* mk = tree ? &tm.tk : &tm.kc;
-        const CUtensorMap* mv = tree ? &tm.tv : &tm.vc;
         const int y = tree ? bh * a.R : bh * a.P + (ti.t_begin + t) * KT;
         if (use > 0 && !wait_parity(&k_empty[s], (use - 1) & 1, a.err, ERR_KEMPTY)) break;
         mbar_arrive_expect_tx(&k_full[s], TILE);
-        tma_load_2d_hint(smem + SM_K + s * TILE, mk, 0, y, &k_full[s], policy);
-        tma_load_2d_hint(smem + SM_K + s * TILE + HALF, mk, 64, y, &k_full[s], policy);
+        load_kv_tile(tree ? tm.tk : tm.kc, smem + SM_K + s * TILE, y, &k_full[s], policy);
+        ++issued_k[s];
         if (usev > 0 && !wait_parity(&v_empty[sv], (usev - 1) & 1, a.err, ERR_VEMPTY)) break;
         mbar_arrive_expect_tx(&v_full[sv], TILE);
-        tma_load_2d_hint(smem + SM_V + sv * TILE, mv, 0, y, &v_full[sv], policy);
-        tma_load_2d_hint(smem + SM_V + sv * TILE + HALF, mv, 64, y, &v_full[sv], policy);
+        load_kv_tile(tree ? tm.tv : tm.vc, smem + SM_V + sv * TILE, y, &v_full[sv], policy);
+        ++issued_v[sv];
       }
     }
   } else if (warp == 9) {
@@ -680,9 +689,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         for (int c = 0; c < 4; ++c) tma_store_2d(&tm.po, smem + SM_K + c * HALF, 32 * c, y);
         bulk_commit();
         if (a.coop)
-          bulk_wait0();  // other CTAs read these rows
+          bulk_wait0();  // other CTAs of this launch read these rows
         else
-          bulk_wait_read0();
+          bulk_wait_read0();  // the combine kernel reads them once this grid has completed
       }
       if (wg == 0 && vrow) *reinterpret_cast<float2*>(a.part_ml + prow * 2) = make_float2(M, L);
     } else if (!(a.tps > 0 && ti.n_tiles == 0) && vrow) {
@@ -693,39 +702,48 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       for (int k = 0; k < 16; ++k) dst[k] = make_float4(0.f, 0.f, 0.f, 0.f);
       if (wg == 0) *reinterpret_cast<float2*>(a.part_ml + prow * 2) = make_float2(-INFINITY, 0.f);
     }
-    if (a.coop) {
-      // the group's merge: publish this split's partials (all writes fenced, then one
-      // release-ordered count), wait until every split of this (request, KV head, row
-      // block) has counted, then merge rows [split n / S, (split + 1) n / S) of the
-      // block from the partials in L2, a half-warp per row
-      fence_proxy_async_global();
-      __threadfence();
-      bar_sync(1, 256);
-      const int grp = bh * gridDim.z + rb;
-      if (threadIdx.x == 0) {
-        s_go = group_arrive_wait(a.cnt + grp, a.group_need, a.err, a.group_limit_ns) ? 1 : 0;
-        // past the wait: the last split of the group to get here returns both counters
-        // to zero for the next call
-        int* fin = a.cnt + a.n_groups + grp;
-        if (atomicAdd(fin, 1) == a.splits - 1) {
-          atomicExch(a.cnt + grp, 0);
-          atomicExch(fin, 0);
-        }
-      }
-      bar_sync(1, 256);
-      if (s_go) {
-        const int n = min(128, ti.Rb * a.G - rb * 128);
-        const int lo = split * n / a.splits;
-        const int hi = (split + 1) * n / a.splits;
-        // a half-warp per row; both halves of a warp loop together (shuffles are
-        // warp-collective), the spare half on a row of its own block with no output
-        for (int s0 = lo + 2 * warp; s0 < hi; s0 += 16) {
-          const int lr = s0 + (lane >> 4);
-          const int grow = lr < hi ? rb * 128 + lr : -1;
-          merge_row_hw(a, bh, h, b, grow, lane & 15, sl2);
-        }
+  }
+  if (a.coop) {
+    // the group's merge: publish this split's partials (every thread's writes fenced,
+    // then one count), wait until every split of this (request, KV head, row block)
+    // has counted, then merge rows [split n / S, (split + 1) n / S) of the block from
+    // the partials in L2, a half-warp per row over all ten warps
+    fence_proxy_async_global();
+    __threadfence();
+    __syncthreads();
+    const int grp = bh * gridDim.z + rb;
+    if (threadIdx.x == 0) {
+      s_go = group_arrive_wait(a.cnt + grp, a.group_need, a.err, a.group_limit_ns) ? 1 : 0;
+      // past the wait: the last split of the group to get here returns both counters
+      // to zero for the next call
+      int* fin = a.cnt + a.n_groups + grp;
+      if (atomicAdd(fin, 1) == a.splits - 1) {
+        atomicExch(a.cnt + grp, 0);
+        atomicExch(fin, 0);
       }
     }
+    __syncthreads();
+    if (s_go) {
+      const int n = max(0, min(128, ti.Rb * a.G - rb * 128));
+      const int lo = split * n / a.splits;
+      const int hi = (split + 1) * n / a.splits;
+      // both halves of a warp loop together (shuffles are warp-collective), the spare
+      // half on a row of its own block with no output
+      for (int s0 = lo + 2 * warp; s0 < hi; s0 += 2 * (NTHREADS / 32)) {
+        const int lr = s0 + (lane >> 4);
+        const int grow = lr < hi ? rb * 128 + lr : -1;
+        merge_row_hw(a, bh, h, b, grow, lane & 15, a.scale_log2);
+      }
+    }
+  }
+  // no copy of this CTA's may still be landing when it exits: the producer waits (at
+  // most 2 s each) for the last load it issued into every stage; on the normal path
+  // the MMA warp has already consumed them all
+  if (warp == 8 && lane == 0) {
+    for (int s = 0; s < KST; ++s)
+      if (issued_k[s] > 0) (void)wait_parity(&k_full[s], (issued_k[s] - 1) & 1, a.err, ERR_KFULL);
+    for (int s = 0; s < VST; ++s)
+      if (issued_v[s] > 0) (void)wait_parity(&v_full[s], (issued_v[s] - 1) & 1, a.err, ERR_VFULL);
   }
   tc_fence_before();
   __syncthreads();
@@ -873,7 +891,8 @@ cudaError_t launch_tree_attn_tc(const AttnPlan& p, const void* q, const void* k_
   const dim3 grid = p.coop ? dim3(p.splits, p.B * p.Hkv, p.row_blocks) : dim3(p.row_blocks, p.splits, p.B * p.Hkv);
   e = p.precise ? launch_tc<true>(tm, a, grid, s) : launch_tc<false>(tm, a, grid, s);
   if (e != cudaSuccess || !partials || p.coop) return e;
-  return launch_tree_attn_combine(p, seq_len, n_nodes, out, lse, static_cast<const float*>(a.part_o), a.part_ml, s);
+  return launch_tree_attn_combine(p, seq_len, n_nodes, out, lse, static_cast<const float*>(a.part_o), a.part_ml, s,
+                                  true);
 }
 
 }  // namespace eagle
