@@ -31,7 +31,8 @@ EAGLE_STATUS_BAD_TREE, EAGLE_STATUS_PATH_OVERFLOW, EAGLE_STATUS_CACHE_FULL, EAGL
 EXPORTED_SYMBOLS = ("eagle_tree_build", "eagle_tree_attn", "eagle_accept", "eagle_kv_commit",
                     "eagle_workspace_size", "eagle_status_string", "eagle_version",
                     "eagle_tree_frontier_rows", "eagle_tree_max_frontier", "eagle_last_cuda_error",
-                    "eagle_last_cuda_error_string", "eagle_tree_attn_plan", "eagle_accept_noalloc")
+                    "eagle_last_cuda_error_string", "eagle_tree_attn_plan", "eagle_accept_noalloc",
+                    "eagle_selftest_ff_log")
 
 
 class TreeDesc(ctypes.Structure):
@@ -93,6 +94,7 @@ def load() -> ctypes.CDLL:
         L.eagle_accept_noalloc.argtypes = [ctypes.POINTER(AcceptDesc), vp, vp, vp, vp, vp, vp,
                                            ctypes.POINTER(AcceptOut), vp]
         L.eagle_kv_commit.argtypes = [ctypes.POINTER(CommitDesc), vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
+        L.eagle_selftest_ff_log.argtypes = [vp, vp, vp, vp, i32, vp]
         L.eagle_workspace_size.argtypes = [i32, vp]
         L.eagle_workspace_size.restype = sz
         L.eagle_status_string.argtypes = [i32]
@@ -311,3 +313,13 @@ def eagle_kv_commit(desc: CommitDesc, layers: LayerPointers, n_acc, path, seq_le
 
 def version() -> str:
     return load().eagle_version().decode()
+
+
+def selftest_ff_log(z_hi: torch.Tensor, z_lo: torch.Tensor):
+    """The tree build's float-float logarithm on device values (see eagle.h:
+    eagle_selftest_ff_log); returns (hi, lo) device tensors."""
+    out_hi, out_lo = torch.empty_like(z_hi), torch.empty_like(z_lo)
+    _check("eagle_selftest_ff_log", load().eagle_selftest_ff_log(
+        _ptr(z_hi, torch.float32, "z_hi"), _ptr(z_lo, torch.float32, "z_lo"), _ptr(out_hi, torch.float32, "out_hi"),
+        _ptr(out_lo, torch.float32, "out_lo"), z_hi.numel(), _stream(None)))
+    return out_hi, out_lo

@@ -270,4 +270,10 @@ int eagle_kv_commit(const eagle_commit_desc* d, void* const* k_cache_layers, voi
                           static_cast<cudaStream_t>(stream)));
 }
 
+int eagle_selftest_ff_log(const float* z_hi, const float* z_lo, float* out_hi, float* out_lo, int32_t n,
+                          void* stream) {
+  if (n < 0 || (n > 0 && (!z_hi || !z_lo || !out_hi || !out_lo))) return EAGLE_ERR_INVALID_ARG;
+  return cuda_status(launch_ff_log_selftest(z_hi, z_lo, out_hi, out_lo, n, static_cast<cudaStream_t>(stream)));
+}
+
 }  // extern "C"

@@ -36,6 +36,10 @@ cudaError_t launch_tree_build(const TreeBuildPlan& p, int level, const void* log
                               const int32_t* root_tok, const int32_t* seq_len, void* ws, const eagle_tree& out,
                               cudaStream_t s);
 
+// The tree build's float-float natural logarithm on n values (self-test entry).
+cudaError_t launch_ff_log_selftest(const float* z_hi, const float* z_lo, float* out_hi, float* out_lo, int n,
+                                   cudaStream_t s);
+
 // ------------------------------------------------------------------ tree attention
 struct AttnPlan {
   int B, R, Hq, Hkv, G, D, P, dtype, W, out_dtype;

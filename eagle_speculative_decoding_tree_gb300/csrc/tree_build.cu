@@ -1014,4 +1014,22 @@ cudaError_t launch_tree_build(const TreeBuildPlan& p, int level, const void* log
   return cudaGetLastError();
 }
 
+namespace {
+// Evaluates the float-float logarithm on n inputs (one thread each).
+__global__ void ff_log_selftest_kernel(const float* z_hi, const float* z_lo, float* out_hi, float* out_lo, int n) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n) return;
+  const ff r = ff_log(ff{z_hi[i], z_lo[i]});
+  out_hi[i] = r.hi;
+  out_lo[i] = r.lo;
+}
+}  // namespace
+
+cudaError_t launch_ff_log_selftest(const float* z_hi, const float* z_lo, float* out_hi, float* out_lo, int n,
+                                   cudaStream_t s) {
+  if (n <= 0) return cudaSuccess;
+  ff_log_selftest_kernel<<<(n + 255) / 256, 256, 0, s>>>(z_hi, z_lo, out_hi, out_lo, n);
+  return cudaGetLastError();
+}
+
 }  // namespace eagle

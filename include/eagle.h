@@ -27,7 +27,13 @@
  *   - All buffer pointers are DEVICE pointers unless the comment says HOST.
  *     The caller owns every buffer; the library allocates nothing, keeps no
  *     state between calls and is reentrant.  Scratch memory comes from the
- *     caller's `ws` buffer, sized by eagle_workspace_size().
+ *     caller's `ws` buffer, sized by eagle_workspace_size().  The one exception
+ *     is eagle_accept_noalloc, which takes its scratch from a fixed device array
+ *     inside the library instead (see there: one array per device, shared by
+ *     every call, so its calls on a device must not overlap).
+ *   - A workspace belongs to one descriptor: calls whose descriptors differ may
+ *     lay their scratch out differently, so give each its own workspace (or
+ *     re-zero it between them).
  *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Every call
  *     only enqueues work on it and returns; nothing synchronises.  Outputs are
  *     valid once the stream has reached the call's work.  No call does a
@@ -137,7 +143,10 @@ typedef struct {             /* all DEVICE pointers, caller-allocated */
   float* score;              /* [B][R]   cumulative ln draft confidence (root 0) */
   int32_t* frontier_tok;     /* [B][F_max] tokens of the nodes whose draft rows feed the next level */
   int32_t* frontier_slot;    /* [B][F_max] each such node's parent row in this level's input */
-  int32_t* near_tie;         /* [B]      selection or draw decisions within 1e-5 of a boundary */
+  int32_t* near_tie;         /* [B]      1 if a selection boundary fell between two scores less
+                                           than 1e-5 apart (siblings with equal logits excepted: both
+                                           sides break those by index), or a draw landed within 1e-7 of
+                                           the row's mass from a bin edge */
 } eagle_tree;
 
 /* Rows the frontier_logits of `level` must have: 1 at level 1; then top_k (dynamic)
@@ -240,8 +249,8 @@ typedef struct {       /* all DEVICE pointers, caller-allocated */
   int32_t* n_acc;      /* [B] accepted drafts */
   int32_t* path;       /* [B][max_depth+1] accepted node rows, root first, -1 padded */
   int32_t* out_tok;    /* [B][max_depth+1] accepted tokens then the emitted token, -1 padded */
-  int32_t* near_tie;   /* [B] 1 if a decision had |u - p/q| < 1e-5 or a draw landed within
-                          1e-5 of a bin edge */
+  int32_t* near_tie;   /* [B] 1 if an accept decision had |u - p/q| < 1e-5, or the final draw
+                          landed within 1e-7 of the distribution's mass from a bin edge */
   uint32_t* status;    /* [1] EAGLE_STATUS_* bits (ORed) */
 } eagle_accept_out;
 
@@ -276,7 +285,10 @@ int eagle_accept(const eagle_accept_desc* d, const void* target_logits, const vo
  *     logits as a second source.
  *   - The first call on each device looks the buffer's address up (a CUDA runtime
  *     query, done once per device with that device current); make that first call
- *     outside any stream capture.
+ *     outside any stream capture.  The address is kept for the life of the process:
+ *     a device reset (cudaDeviceReset, or anything else that destroys the primary
+ *     context) after the first call is not supported, since later calls would
+ *     launch with the old address.
  *   - The buffer needs no clearing: every entry is written before it is read.
  *   - One buffer per device: calls on the same device must not overlap in time
  *     (concurrent streams or host threads would race on it). */
@@ -325,6 +337,15 @@ const char* eagle_status_string(int status);
 
 /* Library version string. */
 const char* eagle_version(void);
+
+/* Self-test of an internal routine (no counterpart in the method's description):
+ * evaluates the float-float natural logarithm that eagle_tree_build uses for the
+ * log-normaliser ln Z of a draft row, on n values z = z_hi[i] + z_lo[i] (DEVICE
+ * arrays of n floats, z > 0, |z_lo| <= ulp(z_hi) / 2), writing ln z as
+ * out_hi[i] + out_lo[i].  Asynchronous on `stream`.  EAGLE_ERR_INVALID_ARG for n < 0
+ * or a NULL array. */
+int eagle_selftest_ff_log(const float* z_hi, const float* z_lo, float* out_hi, float* out_lo, int32_t n,
+                          void* stream);
 
 /* The CUDA error behind the calling thread's most recent EAGLE_ERR_CUDA (a
  * cudaError_t value, 0 if none), and its name.  Thread-local, like cudaGetLastError. */

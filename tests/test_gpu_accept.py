@@ -4,7 +4,9 @@ Trees come from the oracle's builder on the synthetic path-keyed LM; target (and
 draft) rows are that LM's rows at the tree's nodes; uniforms are seeded.  The GPU
 must reproduce the oracle's accepted lengths, paths and emitted tokens bit for
 bit, except for requests where either side reports a near-tie (|u - p/q| < 1e-5,
-or a draw within 1e-7 of the mass of a bin edge), which are counted.  A GPU-side chi-square
+or a draw within 1e-7 of the mass of a bin edge), which are counted, reported in
+the test summary and capped near their expected rate (about 2e-5 per accept
+decision, and up to a few percent per draw at 128K tokens).  A GPU-side chi-square
 check repeats the losslessness test on the kernels themselves.
 """
 import numpy as np
@@ -15,6 +17,7 @@ from scipy.special import softmax
 import oracle
 from eagle_speculative_decoding_tree_gb300 import binding as B
 from eagle_speculative_decoding_tree_gb300 import synth
+from conftest import draw_rate, draw_rate_of, near_tie_cap, record_near_ties
 from gpu_helpers import dev
 from spec_helpers import OracleDynamicBuilder, OracleStaticBuilder, build_tree_bigram, chisquare_pvalue, \
     drive_tree_build, node_hashes
@@ -37,8 +40,21 @@ def gpu_accept(w, tree, target, draft, ua, uf, proposal, T, max_depth):
     return {k: getattr(out, k).cpu().numpy() for k in ("n_acc", "path", "out_tok", "near_tie", "status")}
 
 
-def compare(g, r, max_near):
+def accept_cap(n, V, target=None, dtype="bf16", T=1.0):
+    """Near-tie cap for n requests over V tokens: one final draw each (its rate taken
+    from the target rows when given, else the bound for V tokens) and up to eight
+    accept decisions at 2e-5."""
+    rate = draw_rate(V)
+    if target is not None and T > 0:
+        vals = synth.bf16_value(target[:16]) if dtype == "bf16" else np.asarray(target[:16], np.float32)
+        rate = draw_rate_of(vals, T)
+    return near_tie_cap(n, rate + 8 * 2e-5)
+
+
+def compare(g, r, max_near, label="accept"):
     near = (g["near_tie"] > 0) | (r["near_tie"] > 0)
+    record_near_ties(label, near.sum(), len(near))
+    assert near.sum() < len(near), "no request was compared"
     ok = ~near
     for key in ("n_acc", "path", "out_tok"):
         bad = np.nonzero(ok & np.any(np.atleast_2d(g[key].reshape(len(near), -1) != r[key].reshape(len(near), -1)),
@@ -74,6 +90,7 @@ def case(w, batch, seed, T=None, proposal=None):
     max_depth = int(tree["depth"].max())
     r = oracle.accept(target, tree["tokens"], tree["parent"], ua, uf, T, proposal, max_depth + 1, draft=draft)
     g = gpu_accept(w, tree, target, draft, ua, uf, proposal, T, max_depth)
+    g["_target"] = target
     return g, r
 
 
@@ -82,25 +99,27 @@ def case(w, batch, seed, T=None, proposal=None):
 ])
 def test_accept_workloads(name, batch, T):
     g, r = case(W[name], batch, seed=1, T=T)
-    compare(g, r, max_near=max(2, batch // 4))
+    compare(g, r, max_near=accept_cap(batch, W[name].vocab, g["_target"], W[name].dtype, T),
+            label=f"accept {name} T={T} B={batch}")
 
 
 def test_accept_concurrency_batch32():
-    w = W["concurrency"].with_(batch=32, vocab=32768)
+    """The concurrency workload's full shape: 32 requests, vocab 128256, 61-row trees."""
+    w = W["concurrency"].with_(batch=32)
     g, r = case(w, 32, seed=2)
-    compare(g, r, max_near=4)
+    compare(g, r, max_near=accept_cap(32, w.vocab, g["_target"], w.dtype, w.temperature), label="accept concurrency B=32")
 
 
 def test_accept_temperature_07_delta():
     w = W["vicuna7b"].with_(vocab=5000, temperature=0.7)
     g, r = case(w, 32, seed=3)
-    compare(g, r, max_near=4)
+    compare(g, r, max_near=accept_cap(32, w.vocab, g["_target"], w.dtype, 0.7), label="accept T=0.7 delta B=32")
 
 
 def test_accept_sampled_static_multi_sibling_residuals():
     w = W["tiny"].with_(vocab=5000, dtype="bf16", temperature=0.8, draft_sigma=2.0)
     g, r = case(w, 64, seed=4)
-    compare(g, r, max_near=8)
+    compare(g, r, max_near=accept_cap(64, w.vocab), label="accept sampled multi-sibling B=64")
     assert (r["n_acc"] < 3).sum() > 10  # rejections (and residual passes) happened
 
 
@@ -109,7 +128,7 @@ def test_accept_delta_with_duplicate_siblings():
     # rejected token has zero residual mass and must be rejected too
     w = W["tiny"].with_(vocab=40, dtype="f32", temperature=1.0, sigma=1.0)
     g, r = case(w, 128, seed=5, proposal=oracle.DELTA)
-    compare(g, r, max_near=8)
+    compare(g, r, max_near=accept_cap(128, w.vocab), label="accept duplicate siblings B=128")
 
 
 def test_accept_gpu_chisquare_first_token():
@@ -145,7 +164,8 @@ def test_accept_gpu_chisquare_sampled_static():
     assert chisquare_pvalue(c1, p) > 1e-3
     r = oracle.accept(target[:2000], tree["tokens"][:2000], tree["parent"][:2000], ua[:2000], uf[:2000], 1.0,
                       oracle.SAMPLED, 4, draft=draft[:2000])
-    compare({k: v[:2000] if k != "status" else v for k, v in out.items()}, r, max_near=4)
+    compare({k: v[:2000] if k != "status" else v for k, v in out.items()}, r, max_near=accept_cap(2000, V),
+            label="accept sampled static (chi-square run) B=2000")
 
 
 def test_accept_bad_token_is_flagged_and_rejected():
@@ -183,6 +203,9 @@ def test_accept_agreement_many_requests_128k(proposal):
     w = W["llama8b"]
     r = oracle.accept(target, tokens, parent, ua, uf, 1.0, proposal, max_depth + 1, draft=draft)
     out = gpu_accept(w, tree, target, draft, ua, uf, proposal, 1.0, max_depth)
-    near = compare(out, r, max_near=Bn // 8)
+    # each draw lands within 1e-7 of the mass of a bin edge with probability about
+    # sum min(p, 2e-7) = 2.6% over a Zipf(1.1) row of 128256 tokens: ~3 of 128 expected
+    near = compare(out, r, max_near=accept_cap(Bn, V, target, "bf16", 1.0),
+                   label=f"accept 128K agreement proposal={proposal} B={Bn}")
     assert (r["n_acc"] > 0).sum() > Bn // 10
     print(f"near-ties: {near} of {Bn}")

@@ -179,3 +179,32 @@ def test_static_topk_tree_children_are_ranked_tokens():
             row = lm.draft_row(hs[par[i]]).astype(np.float64)
             order = np.lexsort((np.arange(V), -row))
             assert tree["tokens"][b, i] == order[choices[i][-1]]
+
+
+@pytest.mark.parametrize("choices", [synth.TINY_STATIC_CHOICES,
+                                     tuple((0,) * d for d in range(1, 8)),
+                                     tuple((i,) for i in range(70)) + ((0, 0), (69, 3))])
+def test_static_finalize_from_the_choice_paths(choices):
+    """StaticTree.finalize against the static tree written as child-rank paths (EAGLE
+    review appendix A.1, a fixed tree shape): node j is an ancestor of node i exactly
+    when j's path is a prefix of i's (the root's empty path is a prefix of every path),
+    a node's depth is its path length and its position is seq_len + depth.  Covers the
+    tiny tree, the 8-row chain and a 73-row tree that needs two mask words."""
+    paths = ((),) + tuple(tuple(c) for c in choices)
+    R = len(paths)
+    W = -(-R // 64)
+    par = synth.static_parents(choices)
+    t = oracle.StaticTree(2, 50, par, False, 0.0)
+    seq_len = np.array([5, 1234], np.int32)
+    out = t.finalize(np.array([11, 22], np.int32), seq_len)
+    for i, pi in enumerate(paths):
+        want = np.zeros(W, np.uint64)
+        for j, pj in enumerate(paths):
+            if pi[:len(pj)] == pj:
+                want[j // 64] |= np.uint64(1) << np.uint64(j % 64)
+        for b in range(2):
+            assert np.array_equal(out["anc_mask"][b, i], want), (i, pi)
+            assert out["depth"][b, i] == len(pi)
+            assert out["pos_id"][b, i] == seq_len[b] + len(pi)
+            assert out["parent"][b, i] == (-1 if i == 0 else paths.index(pi[:-1]))
+    assert out["tokens"][:, 0].tolist() == [11, 22]
