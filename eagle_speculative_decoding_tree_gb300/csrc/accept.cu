@@ -11,14 +11,24 @@
 // ones.
 //
 // Kernels
-//   accept_rowstats_kernel  one CTA per (tree row, 4096-token chunk, source): chunk
-//                           max, sum exp((x - m) / T) and argmax -- a single
-//                           streaming pass over every target (and draft) row.
-//   accept_walk_kernel      one CTA per request: merges the chunk statistics of the
-//                           rows it visits, applies the rule, and draws the emitted
-//                           token by inverse CDF.  Point-mass residuals only zero a
-//                           few tokens, so the draw skips to the chunk that holds
-//                           the crossing; drawn-proposal residuals take full passes.
+//   accept_coop_kernel      the walk as one cooperative launch: a group of CTAs per
+//                           request, each owning a slice of the vocabulary (whole
+//                           4096-token chunks).  At each node the walk reaches, every
+//                           CTA reads its slice of that node's row once (chunk max,
+//                           sum exp((x - m) / T), argmax), the group exchanges the
+//                           chunk records through a bounded per-request barrier, and
+//                           every CTA merges them and takes the same decision; a
+//                           rejected drawn proposal adds one more slice pass (the
+//                           residual's mass).  The emitted token is drawn by the CTA
+//                           whose chunk holds the crossing.  Only the rows the walk
+//                           visits are read.
+//   accept_rowstats_kernel  (when a cooperative grid of the requests does not fit)
+//   + accept_walk_kernel    one CTA per (tree row, chunk, source) for every row's
+//                           statistics, then one CTA per request walks, merging the
+//                           chunk statistics of the rows it visits.  Point-mass
+//                           residuals only zero a few tokens, so a draw skips to the
+//                           chunk that holds the crossing; drawn-proposal residuals
+//                           take full passes.
 //
 // Precision: weights are expf((x - m) / T) in fp32; per-thread sums are compensated
 // (Neumaier) and every sum across threads, chunks or tiles is float-float (about 48
@@ -30,6 +40,7 @@
 
 #include "common.cuh"
 #include "launch.h"
+#include "sm100.cuh"
 
 namespace eagle {
 namespace {
@@ -112,17 +123,19 @@ __device__ __forceinline__ void load_chunk(const void* base, size_t off, int lo,
   }
 }
 
-__global__ void __launch_bounds__(kThreads, 4) accept_rowstats_kernel(const AcceptPlan p, const void* target,
-                                                                   const void* draft, RowPart* part) {
-  const int row = blockIdx.x, c = blockIdx.y, src = blockIdx.z;
-  const int rows = gridDim.x, n_chunks = gridDim.y;
-  const void* base = src == 0 ? target : draft;
-  const size_t off = static_cast<size_t>(row) * p.V;
+// Block-wide statistics of chunk c of one row (elements [c 4096, min(V, (c + 1) 4096))):
+// max, argmax (lowest index on ties) and sum exp((x - m) / T) as float-float.  Every
+// thread of the block calls it; the returned record is valid in thread 0.
+__device__ RowPart chunk_rowpart(const AcceptPlan& p, const void* base, size_t off, int c, float invT,
+                                float* keep = nullptr) {
   const int lo = c * kVocabChunk, hi = min(p.V, lo + kVocabChunk);
-  const float invT = 1.f / (p.temperature > 0.f ? p.temperature : 1.f);
   float x[kPer];
   int xi[kPer];
   load_chunk(base, off, lo, hi, p.dtype, p.V, x, xi);
+  if (keep) {  // the chunk's values, by position in the chunk, for a later draw
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) keep[xi[k] - lo] = x[k];
+  }
   // this thread's max and argmax (lowest index on ties), then its sum of
   // exp((x - m) / T), compensated
   float m = -INFINITY, av = -INFINITY;
@@ -159,10 +172,11 @@ __global__ void __launch_bounds__(kThreads, 4) accept_rowstats_kernel(const Acce
   s = warp_sum_ff(s);
   __shared__ RowPart wp[kThreads / 32];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  __syncthreads();  // earlier readers of wp are done
   if (lane == 0) wp[warp] = RowPart{M, av, ai, 0, s};
   __syncthreads();
+  RowPart r = wp[0];
   if (threadIdx.x == 0) {
-    RowPart r = wp[0];
     for (int w = 1; w < kThreads / 32; ++w) r.m = fmaxf(r.m, wp[w].m);
     ff t = ff_make(0.f);
     for (int w = 0; w < kThreads / 32; ++w) {
@@ -173,8 +187,18 @@ __global__ void __launch_bounds__(kThreads, 4) accept_rowstats_kernel(const Acce
       }
     }
     r.s = t;
-    part[(static_cast<size_t>(src) * rows + row) * n_chunks + c] = r;
   }
+  return r;
+}
+
+__global__ void __launch_bounds__(kThreads, 4) accept_rowstats_kernel(const AcceptPlan p, const void* target,
+                                                                   const void* draft, RowPart* part) {
+  const int row = blockIdx.x, c = blockIdx.y, src = blockIdx.z;
+  const int rows = gridDim.x, n_chunks = gridDim.y;
+  const void* base = src == 0 ? target : draft;
+  const float invT = 1.f / (p.temperature > 0.f ? p.temperature : 1.f);
+  const RowPart r = chunk_rowpart(p, base, static_cast<size_t>(row) * p.V, c, invT);
+  if (threadIdx.x == 0) part[(static_cast<size_t>(src) * rows + row) * n_chunks + c] = r;
 }
 
 // ------------------------------------------------------------------ block helpers
@@ -291,13 +315,28 @@ struct RowStats {
   ff Z;
 };
 
+// A chunk record read from L2 (.cg): records are rewritten between the barrier phases of
+// one launch by other CTAs, so this SM's L1 may hold an older copy.
+__device__ __forceinline__ RowPart load_rowpart(const RowPart* rp) {
+  RowPart r;
+  r.m = __ldcg(&rp->m);
+  r.av = __ldcg(&rp->av);
+  r.ai = __ldcg(&rp->ai);
+  r.pad = 0;
+  r.s = ff{__ldcg(&rp->s.hi), __ldcg(&rp->s.lo)};
+  return r;
+}
+
 __device__ RowStats merge_row_stats(const RowPart* rp, int C, float invT, ff* tile_mass, float* rf, int* ri,
                                     ff* rd) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   float m = -INFINITY, av = -INFINITY;
   int ai = INT_MAX;
+  // this thread's first record stays in registers for the mass pass below (C <= 256
+  // needs no second read)
+  const RowPart r0 = threadIdx.x < C ? load_rowpart(rp + threadIdx.x) : RowPart{-INFINITY, -INFINITY, INT_MAX, 0, {0.f, 0.f}};
   for (int c = threadIdx.x; c < C; c += kThreads) {
-    const RowPart r = rp[c];
+    const RowPart r = c == threadIdx.x ? r0 : load_rowpart(rp + c);
     m = fmaxf(m, r.m);
     if (before(r.av, r.ai, av, ai)) {
       av = r.av;
@@ -335,7 +374,7 @@ __device__ RowStats merge_row_stats(const RowPart* rp, int C, float invT, ff* ti
   st.amax = ai;
   ff z = ff_make(0.f);
   for (int c = threadIdx.x; c < C; c += kThreads) {
-    const RowPart r = rp[c];
+    const RowPart r = c == threadIdx.x ? r0 : load_rowpart(rp + c);
     const ff wc = (r.m == -INFINITY) ? ff_make(0.f) : ff_mul(r.s, expf((r.m - st.M) * invT));
     if (tile_mass) tile_mass[c] = wc;
     z = ff_add(z, wc);
@@ -673,6 +712,469 @@ __global__ void __launch_bounds__(kThreads, 1) accept_walk_kernel(const AcceptPl
   }
 }
 
+// ------------------------------------------------------------------ cooperative walk
+struct CoopArgs {
+  WalkArgs w;  // w.part: chunk records [B][2 slots][2 sources][C]
+  int* cnt;    // [B] arrivals at the per-request barrier, zeroed before each launch
+  int cpr;     // CTAs per request
+};
+
+// Per-request barrier: thread 0 counts this CTA in and waits (at most 2 s) until the
+// request has `target` arrivals; then the block syncs.  False on a timeout.
+__device__ bool req_barrier(int* cnt, int target) {
+  __shared__ int s_ok;
+  __syncthreads();  // this CTA's record writes come before its count
+  if (threadIdx.x == 0) {
+    __threadfence();
+    atomicAdd(cnt, 1);
+    int ok = 1;
+    if (sm100::ld_acquire_gpu(cnt) < target) {
+      const uint64_t t0 = sm100::global_ns();
+      while (sm100::ld_acquire_gpu(cnt) < target) {
+        if (sm100::global_ns() - t0 > 2000000000ull) {
+          ok = 0;
+          break;
+        }
+        __nanosleep(64);
+      }
+    }
+    s_ok = ok;
+  }
+  __syncthreads();
+  return s_ok != 0;
+}
+
+// Float-float sum of the s fields of C chunk records (every thread returns it).
+__device__ ff sum_records(const RowPart* rp, int C, ff* red) {
+  ff z = ff_make(0.f);
+  for (int c = threadIdx.x; c < C; c += kThreads) z = ff_add(z, ff{__ldcg(&rp[c].s.hi), __ldcg(&rp[c].s.lo)});
+  z = warp_sum_ff(z);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  __syncthreads();
+  if (lane == 0) red[warp] = z;
+  __syncthreads();
+  ff t = ff_make(0.f);
+  for (int i = 0; i < kThreads / 32; ++i) t = ff_add(t, red[i]);
+  __syncthreads();
+  return t;
+}
+
+__global__ void __launch_bounds__(kThreads, 2) accept_coop_kernel(const AcceptPlan p, const CoopArgs ca) {
+  const WalkArgs& a = ca.w;
+  const int b = blockIdx.y, cta = blockIdx.x, cpr = ca.cpr;
+  const int R = p.R, V = p.V, C = p.n_chunks;
+  const bool greedy = !(p.temperature > 0.f);
+  const bool sampled = !greedy && p.proposal == EAGLE_PROPOSAL_SAMPLED;
+  const float invT = 1.f / (greedy ? 1.f : p.temperature);
+  const int maxp = p.max_depth + 1;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  int* cnt = ca.cnt + b;
+  // chunk records of slot s (alternating between barrier phases) and source (0 target, 1 draft)
+  auto rec = [&](int slot, int src) { return const_cast<RowPart*>(a.part) + ((static_cast<size_t>(b) * 2 + slot) * 2 + src) * C; };
+  int phase = 0;  // barrier phases this request has passed
+
+  __shared__ int s_path[kMaxRows + 1];
+  __shared__ int s_par[kMaxRows], s_tokr[kMaxRows];
+  __shared__ uint32_t s_kidmask[kMaxRows / 32];
+  __shared__ int s_kids[kMaxRows];
+  __shared__ float s_wk[kMaxRows];
+  __shared__ float s_uk[kMaxRows];
+  __shared__ int s_nk, s_len, s_cur, s_next, s_emit, s_done, s_near, s_flag, s_abort, s_write;
+  __shared__ unsigned s_status;
+  __shared__ int s_rej[kMaxRows];
+  __shared__ float s_rejw[kMaxRows];
+  __shared__ int s_nrej;
+  __shared__ float s_Z[kMaxRows];
+  __shared__ int s_nz;
+  __shared__ float s_M, s_Mq;
+  __shared__ ff s_Zt, s_Zq;
+  __shared__ int s_amax;
+  __shared__ ff red[kThreads / 32];
+  __shared__ float s_rf[kThreads / 16];
+  __shared__ int s_ri[kThreads / 32];
+  __shared__ DrawScratch ds;
+  __shared__ int s_chunk, s_fallback;
+  __shared__ ff s_base, s_W;
+  __shared__ ff s_tile[kMaxVocabTiles];
+  __shared__ float s_xk[kMaxRows];  // the target logits of the children's tokens
+  // one chunk per CTA: the target (and draft) values of that chunk of the current row,
+  // kept from the statistics pass for the residual passes and the draw in this CTA
+  __shared__ float s_vals[kVocabChunk];
+  __shared__ float s_dvals[kVocabChunk];
+  const bool keep = cpr == C;
+  const int own_lo = cta * kVocabChunk;
+
+  for (int c = threadIdx.x; c < R; c += kThreads) {
+    s_par[c] = a.parent[static_cast<size_t>(b) * R + c];
+    s_tokr[c] = a.tokens[static_cast<size_t>(b) * R + c];
+  }
+  if (threadIdx.x == 0) {
+    s_len = 1;
+    s_path[0] = 0;
+    s_cur = 0;
+    s_done = 0;
+    s_near = 0;
+    s_status = 0;
+    s_emit = -1;
+    s_abort = 0;
+    s_write = cta == 0;  // the writer of the outputs unless a draw names another CTA
+  }
+  __syncthreads();
+  {
+    bool bad = false;
+    for (int c = 1 + threadIdx.x; c < R; c += kThreads) bad |= (s_par[c] >= c || s_par[c] < 0);
+    if (__syncthreads_or(bad) && threadIdx.x == 0) s_status |= EAGLE_STATUS_BAD_TREE;
+  }
+
+  const size_t row_base = static_cast<size_t>(b) * R;
+  const int32_t* tok = s_tokr;
+  for (int iter = 0; iter <= R && !s_done && !s_abort; ++iter) {
+    const int cur = s_cur;
+    const size_t xrow = (row_base + cur) * V;
+    if (warp < kMaxRows / 32) {
+      const int c = warp * 32 + lane;
+      const uint32_t mk = __ballot_sync(0xffffffffu, c > cur && c < R && s_par[c] == cur);
+      if (lane == 0) s_kidmask[warp] = mk;
+    }
+    __syncthreads();
+    // the children of cur, their uniforms and their tokens' target logits, fetched
+    // while the row's statistics load
+    if (threadIdx.x == 0) {
+      int nk = 0;
+      for (int w = 0; w < kMaxRows / 32; ++w) {
+        uint32_t mk = s_kidmask[w];
+        while (mk) {
+          s_kids[nk++] = w * 32 + __ffs(mk) - 1;
+          mk &= mk - 1;
+        }
+      }
+      s_nk = nk;
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < s_nk; i += kThreads) {
+      const int c = s_kids[i];
+      const int d = tok[c];
+      s_uk[i] = a.u_accept[row_base + c];
+      s_xk[i] = (!greedy && !sampled && d >= 0 && d < V) ? load_elem(a.target, xrow + d, p.dtype) : 0.f;
+    }
+    // this CTA's slice of the node's target (and draft) row, exchanged with the group
+    const int slot = phase & 1;
+    for (int c = cta; c < C; c += cpr) {
+      const RowPart r = chunk_rowpart(p, a.target, xrow, c, invT, keep ? s_vals : nullptr);
+      if (threadIdx.x == 0) rec(slot, 0)[c] = r;
+      if (sampled) {
+        const RowPart q = chunk_rowpart(p, a.draft, xrow, c, invT, keep ? s_dvals : nullptr);
+        if (threadIdx.x == 0) rec(slot, 1)[c] = q;
+      }
+    }
+    if (!req_barrier(cnt, ++phase * cpr)) {
+      if (threadIdx.x == 0) s_abort = 1;
+      __syncthreads();
+      break;
+    }
+    const RowStats ts = merge_row_stats(rec(slot, 0), C, invT, s_tile, s_rf, s_ri, red);
+    RowStats qs{};
+    if (sampled) qs = merge_row_stats(rec(slot, 1), C, invT, nullptr, s_rf, s_ri, red);
+    if (threadIdx.x == 0) {
+      s_M = ts.M;
+      s_Zt = ts.Z;
+      s_amax = ts.amax;
+      s_Mq = qs.M;
+      s_Zq = qs.Z;
+      s_next = -1;
+      s_nrej = 0;
+      s_nz = 0;
+    }
+    __syncthreads();
+    const float M = s_M, Mq = s_Mq;
+    const float invZt = 1.f / ff_float(s_Zt);
+    const float invZq = sampled ? 1.f / ff_float(s_Zq) : 0.f;
+    auto w_target = [&](int v) { return expf((load_elem(a.target, xrow + v, p.dtype) - M) * invT); };
+    auto p_of = [&](int v) { return w_target(v) * invZt; };
+    auto q_of = [&](int v) { return expf((load_elem(a.draft, xrow + v, p.dtype) - Mq) * invT) * invZq; };
+    auto pres_of = [&](int v, int nz) {
+      float pv = p_of(v);
+      if (nz == 0) return pv;
+      const float qv = q_of(v);
+      for (int i = 0; i < nz; ++i) pv = fmaxf(pv - qv, 0.f) / s_Z[i];
+      return pv;
+    };
+    // the same for a token of this CTA's own chunk, from the kept values
+    auto pres_own = [&](int v, int nz) {
+      if (!keep) return pres_of(v, nz);
+      float pv = expf((s_vals[v - own_lo] - M) * invT) * invZt;
+      if (nz == 0) return pv;
+      const float qv = expf((s_dvals[v - own_lo] - Mq) * invT) * invZq;
+      for (int i = 0; i < nz; ++i) pv = fmaxf(pv - qv, 0.f) / s_Z[i];
+      return pv;
+    };
+    auto q_own = [&](int v) { return keep ? expf((s_dvals[v - own_lo] - Mq) * invT) * invZq : q_of(v); };
+    for (int i = threadIdx.x; i < s_nk; i += kThreads) {
+      const int d = tok[s_kids[i]];
+      s_wk[i] = (!greedy && !sampled && d >= 0 && d < V) ? expf((s_xk[i] - M) * invT) : 0.f;
+    }
+    __syncthreads();
+
+    if (greedy) {
+      if (threadIdx.x == 0) {
+        const int am = s_amax;
+        for (int i = 0; i < s_nk; ++i)
+          if (tok[s_kids[i]] == am) {
+            s_next = s_kids[i];
+            break;
+          }
+        if (s_next < 0) {
+          s_emit = am;
+          s_done = 1;
+        }
+      }
+      __syncthreads();
+    } else if (!sampled) {
+      // point-mass proposals: p_res(d) = p(d) / (1 - mass of the rejected tokens)
+      if (threadIdx.x == 0) {
+        const float invZ = 1.f / ff_float(s_Zt);
+        ff rejmass = ff_make(0.f);
+        for (int i = 0; i < s_nk; ++i) {
+          const int c = s_kids[i];
+          const int d = tok[c];
+          if (d < 0 || d >= V) {
+            s_status |= EAGLE_STATUS_BAD_TOKEN;
+            continue;
+          }
+          bool dup = false;
+          for (int r = 0; r < s_nrej; ++r) dup |= (s_rej[r] == d);
+          const float pd = dup ? 0.f : s_wk[i] * invZ;
+          const float denom = ff_float(ff_sub(ff_make(1.f), rejmass));
+          const float ratio = denom > 0.f ? __fdividef(pd, denom) : 0.f;
+          const float u = s_uk[i];
+          if (fabsf(u - ratio) < kNearTieEps) s_near = 1;
+          if (u < ratio) {
+            s_next = c;
+            break;
+          }
+          if (!dup) {
+            s_rejw[s_nrej] = s_wk[i];
+            s_rej[s_nrej++] = d;
+            rejmass = ff_add(rejmass, pd);
+          }
+        }
+      }
+      __syncthreads();
+    } else {
+      // drawn proposals (SpecInfer multi-round): q fixed across siblings; a rejection
+      // needs the residual's normaliser, one more slice pass of the group
+      for (int i = 0; i < s_nk; ++i) {
+        const int c = s_kids[i];
+        const int nz = s_nz;
+        if (threadIdx.x == 0) {
+          const int d = tok[c];
+          s_flag = 0;
+          if (d < 0 || d >= V) {
+            s_status |= EAGLE_STATUS_BAD_TOKEN;
+          } else {
+            const float qd = q_of(d);
+            const float pd = pres_of(d, nz);
+            const float ratio = qd > 0.f ? pd / qd : INFINITY;
+            const float u = s_uk[i];
+            if (qd > 0.f && fabsf(u - ratio) < kNearTieEps) s_near = 1;
+            if (!(qd > 0.f) || u < ratio)
+              s_next = c;
+            else
+              s_flag = 1;
+          }
+        }
+        __syncthreads();
+        if (s_next >= 0) break;
+        if (s_flag) {
+          const int slot2 = phase & 1;
+          for (int cc = cta; cc < C; cc += cpr) {
+            const int lo = cc * kVocabChunk, hi = min(V, lo + kVocabChunk);
+            const ff z = block_sum(lo, hi, [&](int v) { return fmaxf(pres_own(v, nz) - q_own(v), 0.f); }, red);
+            if (threadIdx.x == 0) rec(slot2, 0)[cc] = RowPart{0.f, 0.f, 0, 0, z};
+          }
+          if (!req_barrier(cnt, ++phase * cpr)) {
+            if (threadIdx.x == 0) s_abort = 1;
+            __syncthreads();
+            break;
+          }
+          const ff z = sum_records(rec(slot2, 0), C, red);
+          if (threadIdx.x == 0 && z.hi > 0.f) s_Z[s_nz++] = ff_float(z);
+        }
+        __syncthreads();
+      }
+      if (s_abort) break;
+    }
+
+    if (s_next >= 0) {
+      if (threadIdx.x == 0) {
+        if (s_len >= maxp) {  // deeper than the path arrays: emit the accepted token and stop
+          s_status |= EAGLE_STATUS_PATH_OVERFLOW;
+          s_emit = tok[s_next];
+          s_done = 1;
+        } else {
+          s_path[s_len++] = s_next;
+          s_cur = s_next;
+        }
+      }
+      __syncthreads();
+      continue;
+    }
+    if (s_done) break;
+
+    // ---- draw the emitted token from the (residual) target distribution: the chunk
+    // masses (the group's slice passes for a drawn-proposal residual), the chunk holding
+    // the crossing, then that chunk element by element in the CTA that owns it
+    const float u = a.u_final[b];
+    const bool residual = sampled && s_nz > 0;
+    const int nz = s_nz, nrej = s_nrej;
+    if (residual) {
+      const int slot2 = phase & 1;
+      for (int cc = cta; cc < C; cc += cpr) {
+        const int lo = cc * kVocabChunk, hi = min(V, lo + kVocabChunk);
+        const ff m = block_sum(lo, hi, [&](int v) { return pres_own(v, nz); }, red);
+        if (threadIdx.x == 0) rec(slot2, 0)[cc] = RowPart{0.f, 0.f, 0, 0, m};
+      }
+      if (!req_barrier(cnt, ++phase * cpr)) {
+        if (threadIdx.x == 0) s_abort = 1;
+        __syncthreads();
+        break;
+      }
+      for (int c = threadIdx.x; c < C; c += kThreads) s_tile[c] = ff{__ldcg(&rec(slot2, 0)[c].s.hi), __ldcg(&rec(slot2, 0)[c].s.lo)};
+    } else {
+      for (int c = threadIdx.x; c < C; c += kThreads) {
+        ff wc = s_tile[c];
+        for (int r = 0; r < nrej; ++r)
+          if (s_rej[r] / kVocabChunk == c) wc = ff_sub(wc, ff_make(s_rejw[r]));
+        s_tile[c] = wc;
+      }
+    }
+    __syncthreads();
+    if (warp == 0) {
+      ff W = ff_make(0.f);
+      if (residual) {
+        for (int c = lane; c < C; c += 32) W = ff_add(W, s_tile[c]);
+        W = warp_sum_ff(W);
+      } else {
+        W = s_Zt;
+        for (int r = 0; r < nrej; ++r) W = ff_sub(W, ff_make(s_rejw[r]));
+      }
+      const ff target = ff_mul(W, u);
+      ff carry = ff_make(0.f), bs = ff_make(0.f);
+      int cs = -1, lastc = -1;
+      for (int c0 = 0; c0 < C; c0 += 32) {
+        const int c = c0 + lane;
+        const ff wc = c < C ? s_tile[c] : ff_make(0.f);
+        ff incl = wc;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const ff t = ff_shfl_up(incl, o);
+          if (lane >= o) incl = ff_add(incl, t);
+        }
+        const ff cum = ff_add(carry, incl);
+        const unsigned pos = __ballot_sync(0xffffffffu, c < C && wc.hi > 0.f);
+        if (pos) lastc = c0 + 31 - __clz(pos);
+        const unsigned cross = __ballot_sync(0xffffffffu, c < C && ff_gt(cum, target));
+        const ff excl = ff_sub(cum, wc);
+        if (cs < 0 && cross) {
+          const int l = __ffs(cross) - 1;
+          cs = c0 + l;
+          bs = ff{__shfl_sync(0xffffffffu, excl.hi, l), __shfl_sync(0xffffffffu, excl.lo, l)};
+        }
+        carry = ff_add(carry, ff{__shfl_sync(0xffffffffu, incl.hi, 31), __shfl_sync(0xffffffffu, incl.lo, 31)});
+      }
+      if (lane == 0) {
+        s_fallback = cs < 0;
+        s_chunk = cs < 0 ? (lastc < 0 ? 0 : lastc) : cs;
+        s_base = bs;
+        s_W = W;
+        s_write = (s_chunk % cpr) == cta;  // the chunk's owner draws and writes the outputs
+      }
+    }
+    __syncthreads();
+    if (!s_write) break;
+    const int lo = s_chunk * kVocabChunk;
+    const ff W = s_W;
+    const ff target = s_fallback ? ff{INFINITY, 0.f} : ff_mul(W, u);
+    if (residual) {
+      block_draw_tile(
+          lo, min(V, lo + kVocabChunk), s_base, target,
+          [&](int v) {
+            return keep ? make_float2(s_vals[v - lo], s_dvals[v - lo])
+                        : make_float2(load_elem(a.target, xrow + v, p.dtype), load_elem(a.draft, xrow + v, p.dtype));
+          },
+          [&](int v, float2 x) {
+            float pv = expf((x.x - M) * invT) * invZt;
+            const float qv = expf((x.y - Mq) * invT) * invZq;
+            for (int i = 0; i < nz; ++i) pv = fmaxf(pv - qv, 0.f) / s_Z[i];
+            return pv;
+          },
+          s_rej, 0, ds);
+    } else {
+      block_draw_tile(
+          lo, min(V, lo + kVocabChunk), s_base, target,
+          [&](int v) { return make_float2(keep ? s_vals[v - lo] : load_elem(a.target, xrow + v, p.dtype), 0.f); },
+          [&](int, float2 x) { return expf((x.x - M) * invT); }, s_rej, nrej, ds);
+    }
+    if (threadIdx.x == 0) {
+      int emit = ds.found;
+      const float win = kIcdfNearEps * ff_float(W);
+      if (emit == INT_MAX) {
+        emit = ds.last < 0 ? lo : ds.last;
+        s_near = 1;
+      } else if (ff_float(ff_sub(target, ds.prev_edge)) < win || ff_float(ff_sub(ds.next_edge, target)) < win) {
+        s_near = 1;
+      }
+      s_emit = emit;
+    }
+    __syncthreads();
+    break;
+  }
+
+  // ---- outputs, from one CTA of the request
+  if (threadIdx.x == 0) {
+    if (s_abort) {
+      atomicOr(a.out.status, EAGLE_STATUS_TIMEOUT | s_status);
+    } else if (s_write) {
+      const int len = s_len;
+      const int na = len - 1;
+      int32_t* pb = a.out.path + static_cast<size_t>(b) * maxp;
+      int32_t* ob = a.out.out_tok + static_cast<size_t>(b) * maxp;
+      for (int j = 0; j < maxp; ++j) {
+        pb[j] = j < len ? s_path[j] : -1;
+        ob[j] = j < na ? s_tokr[s_path[j + 1]] : (j == na ? s_emit : -1);
+      }
+      a.out.n_acc[b] = na;
+      a.out.near_tie[b] = s_near;
+      if (s_status) atomicOr(a.out.status, s_status);
+    }
+  }
+}
+
+// Co-resident CTAs of the cooperative walk on the current device (0 when unknown);
+// cached per device.
+int coop_capacity() {
+  static int cached[64];
+  static unsigned long long known = 0;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return 0;
+  }
+  if (dev < 64 && (__atomic_load_n(&known, __ATOMIC_ACQUIRE) & (1ull << dev))) return cached[dev];
+  int per_sm = 0, sms = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, accept_coop_kernel, kThreads, 0) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+    per_sm = sms = 0;
+  }
+  (void)cudaGetLastError();
+  const int n = per_sm * sms;
+  if (dev < 64) {
+    cached[dev] = n;
+    __atomic_fetch_or(&known, 1ull << dev, __ATOMIC_RELEASE);
+  }
+  return n;
+}
+
 }  // namespace
 
 void plan_accept(const eagle_accept_desc* d, AcceptPlan* p) {
@@ -685,14 +1187,50 @@ void plan_accept(const eagle_accept_desc* d, AcceptPlan* p) {
   p->temperature = d->temperature;
   p->n_chunks = (d->vocab + kVocabChunk - 1) / kVocabChunk;
   p->n_sources = (d->temperature > 0.f && d->proposal == EAGLE_PROPOSAL_SAMPLED) ? 2 : 1;
-  p->off_part = 0;
-  p->total = static_cast<size_t>(p->n_sources) * p->B * p->R * p->n_chunks * sizeof(RowPart);
+  // the workspace holds either launch form: the cooperative walk's barrier counters and
+  // chunk records [B][2][2][C], or every row's chunk statistics for the two-kernel form
+  p->off_cnt = 0;
+  p->off_part = (static_cast<size_t>(p->B) * sizeof(int) + 255) / 256 * 256;
+  const size_t coop = static_cast<size_t>(p->B) * 4 * p->n_chunks * sizeof(RowPart);
+  const size_t rows = static_cast<size_t>(p->n_sources) * p->B * p->R * p->n_chunks * sizeof(RowPart);
+  p->total = p->off_part + (coop > rows ? coop : rows);
 }
 
 cudaError_t launch_accept(const AcceptPlan& p, const void* target, const void* draft, const int32_t* tokens,
                           const int32_t* parent, const float* u_accept, const float* u_final,
                           const eagle_accept_out& out, void* ws, cudaStream_t s) {
   RowPart* part = reinterpret_cast<RowPart*>(static_cast<uint8_t*>(ws) + p.off_part);
+  // the cooperative walk when a group of CTAs per request fits on the device at once
+  const int cap = coop_capacity();
+  const int cpr = cap / p.B < p.n_chunks ? cap / p.B : p.n_chunks;
+  if (cpr >= 1) {
+    int* cnt = reinterpret_cast<int*>(static_cast<uint8_t*>(ws) + p.off_cnt);
+    cudaError_t e = cudaMemsetAsync(cnt, 0, static_cast<size_t>(p.B) * sizeof(int), s);
+    if (e != cudaSuccess) return e;
+    CoopArgs ca;
+    ca.w.target = target;
+    ca.w.draft = draft;
+    ca.w.tokens = tokens;
+    ca.w.parent = parent;
+    ca.w.u_accept = u_accept;
+    ca.w.u_final = u_final;
+    ca.w.out = out;
+    ca.w.part = part;
+    ca.cnt = cnt;
+    ca.cpr = cpr;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(cpr, p.B, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, accept_coop_kernel, p, ca);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+  }
   dim3 grid(p.B * p.R, p.n_chunks, p.n_sources);
   accept_rowstats_kernel<<<grid, kThreads, 0, s>>>(p, target, draft, part);
   cudaError_t e = cudaGetLastError();

@@ -10,10 +10,10 @@
 // in a file-scope device array of EAGLE_ACCEPT_NOALLOC_SCRATCH_BYTES instead and
 // makes no allocation itself.  It runs the very same kernels as eagle_accept.
 //
-// The scratch needs no clearing: the row-statistics kernel writes every entry the
-// walk kernel later reads.  There is one buffer per device, so calls on the same
-// device must not overlap in time (two streams, or two host threads, running it at
-// once would race on the buffer).
+// The scratch needs no clearing: each call zeroes the barrier counters it uses and
+// writes every chunk record before reading it.  There is one buffer per device, so
+// calls on the same device must not overlap in time (two streams, or two host
+// threads, running it at once would race on the buffer).
 #include <mutex>
 
 #include "launch.h"

@@ -81,7 +81,7 @@ struct AcceptPlan {
   float temperature;
   int n_chunks;
   int n_sources;  // 1 (target) or 2 (target + draft)
-  size_t off_part, total;
+  size_t off_cnt, off_part, total;
 };
 void plan_accept(const eagle_accept_desc* d, AcceptPlan* p);
 cudaError_t launch_accept(const AcceptPlan& p, const void* target, const void* draft, const int32_t* tokens,

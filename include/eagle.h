@@ -83,6 +83,8 @@ enum {
 #define EAGLE_STATUS_PATH_OVERFLOW 0x2u /* accepted path deeper than max_depth: truncated */
 #define EAGLE_STATUS_CACHE_FULL 0x4u    /* seq_len + n_acc + 1 > max_seq: that request was not committed */
 #define EAGLE_STATUS_BAD_TOKEN 0x8u     /* a draft token outside [0, V): treated as rejected */
+#define EAGLE_STATUS_TIMEOUT 0x10u      /* eagle_accept: a bounded wait between the CTAs of a request
+                                           gave up (2 s); that request's outputs were not written */
 
 /* Element types */
 enum { EAGLE_F32 = 0, EAGLE_BF16 = 1 };
@@ -289,7 +291,8 @@ int eagle_accept(const eagle_accept_desc* d, const void* target_logits, const vo
  *     a device reset (cudaDeviceReset, or anything else that destroys the primary
  *     context) after the first call is not supported, since later calls would
  *     launch with the old address.
- *   - The buffer needs no clearing: every entry is written before it is read.
+ *   - The buffer needs no clearing: each call zeroes the counters it uses and
+ *     writes every other entry before reading it.
  *   - One buffer per device: calls on the same device must not overlap in time
  *     (concurrent streams or host threads would race on it). */
 #define EAGLE_ACCEPT_NOALLOC_SCRATCH_BYTES (4u << 20)
