@@ -107,7 +107,9 @@ def test_accept_validation(lib):
     assert _call_acc(lib, _acc(), out_ok=False) == B.EAGLE_ERR_INVALID_ARG
     d = _acc()
     need = B.workspace_size(B.EAGLE_WS_ACCEPT, d)
-    assert need == 61 * 32 * 24  # one 24-byte record per (row, 4096-token chunk)
+    # 256 bytes of per-request barrier counters, then one 24-byte record per (row,
+    # 4096-token chunk): the larger of the two launch forms' record areas
+    assert need == 256 + 61 * 32 * 24
     assert _call_acc(lib, d, ws_bytes=need - 1) == B.EAGLE_ERR_WORKSPACE
     ds = _acc(proposal=1)
     assert B.workspace_size(B.EAGLE_WS_ACCEPT, ds) == 2 * need
