@@ -112,7 +112,7 @@ def test_accept_validation(lib):
     assert need == 256 + 61 * 32 * 24
     assert _call_acc(lib, d, ws_bytes=need - 1) == B.EAGLE_ERR_WORKSPACE
     ds = _acc(proposal=1)
-    assert B.workspace_size(B.EAGLE_WS_ACCEPT, ds) == 2 * need
+    assert B.workspace_size(B.EAGLE_WS_ACCEPT, ds) == 256 + 2 * 61 * 32 * 24  # target and draft records
 
 
 def _call_build(lib, desc, level=1, ws_bytes=0, u=None):
