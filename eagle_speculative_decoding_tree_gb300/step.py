@@ -147,7 +147,8 @@ class VerifyStep:
         self.tree = tree
         R = tree["tokens"].shape[1]
         self.R = R
-        self.max_depth = int(tree["depth"].max())
+        # path arrays sized for the deepest tree the workload builds (step variants included)
+        self.max_depth = max(int(tree["depth"].max()), w.depth if w.tree_mode == "dynamic" else 0)
         dev = torch.device(device)
         i32 = lambda a: torch.from_numpy(np.ascontiguousarray(a, np.int32)).to(dev)
         self.tokens, self.parent = i32(tree["tokens"]), i32(tree["parent"])
@@ -196,6 +197,46 @@ class VerifyStep:
         self.commit_desc = B.CommitDesc(L, Bn, w.n_kv_heads, w.head_dim, R, w.max_seq, self.max_depth, dt, 0, dt)
         self.layers = B.LayerPointers(self.kc, self.vc, self.tk, self.tv)
         self.commit_pos = torch.zeros(Bn, self.max_depth + 1, dtype=torch.int32, device=dev)
+        self.variants = [dict(tokens=self.tokens, parent=self.parent, anc_mask=self.anc_mask, target=self.target,
+                              draft=self.draft, u_accept=self.u_accept, u_final=self.u_final)]
+
+    # ------------------------------------------------------------------ step variants
+    def add_variants(self, n: int):
+        """n more verify steps of the same workload over the same caches and queries: each
+        has its own root token, draft tree (built on the GPU from the synthetic LM's rows),
+        logits at its nodes and uniforms (seeded by the step index), so replaying them in
+        turn accepts drafts at the workload's own rate.  Variant 0 is the step built in
+        the constructor."""
+        w, Bn, dev = self.w, self.B, torch.device(self.device)
+        i32 = lambda a: torch.from_numpy(np.ascontiguousarray(a, np.int32)).to(dev)
+        lm = synth.hash_lm(w)
+        for k in range(1, n + 1):
+            g = synth.rng(w.config_id, 9100, k, Bn)
+            root_tok = g.integers(0, w.vocab, size=Bn).astype(np.int32)
+            root_h = [synth.root_hash(w.config_id, b, 1000 + k) for b in range(Bn)]
+            ua, uf, ud = synth.step_uniforms(w, Bn, w.rows, step=1000 + k)
+            tree, _ = build_tree(w, Bn, root_tok, root_h, self.seq_len0,
+                                 ud if w.tree_mode == "static_sampled" else None, self.device)
+            if tree["tokens"].shape[1] != self.R or int(tree["depth"].max()) > self.max_depth:
+                continue  # a variant must fit the step's shapes (rows, path length)
+            hs = node_hashes(tree["tokens"], tree["parent"], root_h)
+            tgt = synth.as_dtype_bytes(np.stack([lm.rows(hs[b], "target") for b in range(Bn)]), w.dtype)
+            v = dict(tokens=i32(tree["tokens"]), parent=i32(tree["parent"]),
+                     anc_mask=torch.from_numpy(np.ascontiguousarray(tree["anc_mask"]).view(np.int64)).to(dev),
+                     target=_to_dev(tgt, w.dtype, dev), draft=None, u_accept=torch.from_numpy(ua).to(dev),
+                     u_final=torch.from_numpy(uf).to(dev))
+            if self.draft is not None:
+                dft = synth.as_dtype_bytes(np.stack([lm.rows(hs[b], "draft") for b in range(Bn)]), w.dtype)
+                v["draft"] = _to_dev(dft, w.dtype, dev)
+            self.variants.append(v)
+        return len(self.variants)
+
+    def use_variant(self, k: int):
+        """Point the step's calls at variant k's tree, logits and uniforms."""
+        v = self.variants[k]
+        self.tokens, self.parent, self.anc_mask = v["tokens"], v["parent"], v["anc_mask"]
+        self.target, self.draft = v["target"], v["draft"]
+        self.u_accept, self.u_final = v["u_accept"], v["u_final"]
 
     # ------------------------------------------------------------------ calls
     def attn_layer(self, l: int, stream=None, lse: bool = False):
