@@ -282,3 +282,57 @@ def kv_commit(k_cache, v_cache, tree_k, tree_v, n_acc, path, seq_len, feat_cache
             pos[b, m] = slot
         new_len[b] = int(seq_len[b]) + int(n_acc[b]) + 1
     return new_len, pos
+
+
+# ---------------------------------------------------------------------------- LM-head statistics
+def lmhead_logits(hidden, weight):
+    """The target model's logits at the tree's nodes: hidden [M][h] times the LM head
+    W [V][h] transposed, in float64 (inputs float32 or bf16 bits).  EAGLE review, data
+    path steps 3 and 6 (the frozen LM head gives the distribution at every node)."""
+    def f64(a):
+        a = np.asarray(a)
+        if a.dtype == np.uint16:
+            return (a.astype(np.uint32) << np.uint32(16)).view(np.float32).astype(np.float64)
+        return a.astype(np.float64)
+    return f64(hidden) @ f64(weight).T
+
+
+def lmhead_stats(hidden, weight, temperature: float, tile: int, tokens=None, parent=None):
+    """What acceptance needs from each node's distribution, from the logits
+    x = hidden W^T (EAGLE review, section 3.3 / Algorithm 1: the accept test reads the
+    target probability of each child's token, the bonus draw reads the distribution):
+    per row and per tile of `tile` vocabulary entries, the max logit, its index (lowest
+    on ties) and sum exp((x - max) / T) (T <= 0 counts as 1); and, given the tree
+    (tokens, parent [B][R] with rows ordered b * R + node), each node's own token's
+    logit under its parent's row (NaN at the roots).  Returns a dict of float64 /
+    int64 arrays: max, argmax [M][C], sum [M][C], child [B][R]."""
+    x = lmhead_logits(hidden, weight)
+    M, V = x.shape
+    T = temperature if temperature > 0 else 1.0
+    C = -(-V // tile)
+    mx = np.full((M, C), -np.inf)
+    am = np.zeros((M, C), np.int64)
+    sm = np.zeros((M, C))
+    for c in range(C):
+        blk = x[:, c * tile:(c + 1) * tile]
+        mx[:, c] = blk.max(axis=1)
+        am[:, c] = c * tile + np.argmax(blk, axis=1)  # first maximum: the lowest index
+        sm[:, c] = np.exp((blk - mx[:, c:c + 1]) / T).sum(axis=1)
+    out = dict(max=mx, argmax=am, sum=sm, logits=x)
+    if tokens is not None:
+        Bn, R = np.asarray(tokens).shape
+        child = np.full((Bn, R), np.nan)
+        for b in range(Bn):
+            for i in range(1, R):
+                child[b, i] = x[b * R + int(parent[b][i]), int(tokens[b][i])]
+        out["child"] = child
+    return out
+
+
+def lmhead_accept(hidden, weight, tokens, parent, u_accept, u_final, temperature: float, proposal: int,
+                  max_path: int):
+    """Acceptance with the target rows given as hidden states and the LM head: the
+    logits at every node (lmhead_logits), then the multi-round rule (accept)."""
+    Bn, R = np.asarray(tokens).shape
+    x = lmhead_logits(hidden, weight).astype(np.float32).reshape(Bn, R, -1)
+    return accept(x, tokens, parent, u_accept, u_final, temperature, proposal, max_path)
