@@ -32,7 +32,7 @@ EXPORTED_SYMBOLS = ("eagle_tree_build", "eagle_tree_attn", "eagle_accept", "eagl
                     "eagle_workspace_size", "eagle_status_string", "eagle_version",
                     "eagle_tree_frontier_rows", "eagle_tree_max_frontier", "eagle_last_cuda_error",
                     "eagle_last_cuda_error_string", "eagle_tree_attn_plan", "eagle_accept_noalloc",
-                    "eagle_selftest_ff_log")
+                    "eagle_selftest_ff_log", "eagle_lmhead_stats")
 
 
 class TreeDesc(ctypes.Structure):
@@ -65,6 +65,15 @@ class AcceptOut(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in ("n_acc", "path", "out_tok", "near_tie", "status")]
 
 
+class LmHeadDesc(ctypes.Structure):
+    _fields_ = [("rows", ctypes.c_int32), ("tree_rows", ctypes.c_int32), ("hidden", ctypes.c_int32),
+                ("vocab", ctypes.c_int32), ("temperature", ctypes.c_float)]
+
+
+EAGLE_LMHEAD_TILE = 128
+EAGLE_STATUS_TIMEOUT = 0x10
+
+
 class CommitDesc(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in ("layers", "batch", "n_kv_heads", "head_dim", "rows", "max_seq",
                                               "max_depth", "dtype", "feat_dim", "feat_dtype")]
@@ -95,6 +104,7 @@ def load() -> ctypes.CDLL:
                                            ctypes.POINTER(AcceptOut), vp]
         L.eagle_kv_commit.argtypes = [ctypes.POINTER(CommitDesc), vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
         L.eagle_selftest_ff_log.argtypes = [vp, vp, vp, vp, i32, vp]
+        L.eagle_lmhead_stats.argtypes = [ctypes.POINTER(LmHeadDesc), vp, vp, vp, vp, vp, vp, vp, vp]
         L.eagle_workspace_size.argtypes = [i32, vp]
         L.eagle_workspace_size.restype = sz
         L.eagle_status_string.argtypes = [i32]
@@ -323,3 +333,15 @@ def selftest_ff_log(z_hi: torch.Tensor, z_lo: torch.Tensor):
         _ptr(z_hi, torch.float32, "z_hi"), _ptr(z_lo, torch.float32, "z_lo"), _ptr(out_hi, torch.float32, "out_hi"),
         _ptr(out_lo, torch.float32, "out_lo"), z_hi.numel(), _stream(None)))
     return out_hi, out_lo
+
+
+def eagle_lmhead_stats(desc: LmHeadDesc, hidden, weight, tree_tokens, tree_parent, records, child_logit, status,
+                       stream=None) -> None:
+    """Vocabulary statistics at every tree node from hidden states and the LM head (see
+    eagle.h: eagle_lmhead_stats).  records: an int32 tensor [M][tiles][4] (max, argmax,
+    sum_hi, sum_lo as 32-bit words)."""
+    _check("eagle_lmhead_stats", load().eagle_lmhead_stats(
+        ctypes.byref(desc), _ptr(hidden, torch.bfloat16, "hidden"), _ptr(weight, torch.bfloat16, "weight"),
+        _ptr(tree_tokens, torch.int32, "tree_tokens"), _ptr(tree_parent, torch.int32, "tree_parent"),
+        _ptr(records, torch.int32, "records"), _ptr(child_logit, torch.float32, "child_logit"),
+        _ptr(status, torch.int32, "status"), _stream(stream)))

@@ -270,6 +270,22 @@ int eagle_kv_commit(const eagle_commit_desc* d, void* const* k_cache_layers, voi
                           static_cast<cudaStream_t>(stream)));
 }
 
+int eagle_lmhead_stats(const eagle_lmhead_desc* d, const void* hidden, const void* weight,
+                       const int32_t* tree_tokens, const int32_t* tree_parent, eagle_vocab_record* records,
+                       float* child_logit, uint32_t* status, void* stream) {
+  if (!d || !hidden || !weight || !records || !status) return EAGLE_ERR_INVALID_ARG;
+  if (d->rows < 1 || d->tree_rows < 1 || d->hidden < 1 || d->vocab < 1 || d->rows % d->tree_rows)
+    return EAGLE_ERR_INVALID_ARG;
+  if (!isfinite(d->temperature)) return EAGLE_ERR_INVALID_ARG;
+  if ((tree_tokens == nullptr) != (tree_parent == nullptr) || (tree_tokens && !child_logit))
+    return EAGLE_ERR_INVALID_ARG;
+  if (d->rows > 128 || d->hidden % 64) return EAGLE_ERR_UNSUPPORTED;
+  if (!aligned(hidden, 16) || !aligned(weight, 16) || !aligned(records, 16)) return EAGLE_ERR_ALIGNMENT;
+  return cuda_status(launch_lmhead_stats(d->rows, d->hidden, d->vocab, d->tree_rows, d->temperature, hidden, weight,
+                                         tree_tokens, tree_parent, records, tree_tokens ? child_logit : nullptr,
+                                         status, num_sms(), static_cast<cudaStream_t>(stream)));
+}
+
 int eagle_selftest_ff_log(const float* z_hi, const float* z_lo, float* out_hi, float* out_lo, int32_t n,
                           void* stream) {
   if (n < 0 || (n > 0 && (!z_hi || !z_lo || !out_hi || !out_lo))) return EAGLE_ERR_INVALID_ARG;

@@ -88,6 +88,12 @@ cudaError_t launch_accept(const AcceptPlan& p, const void* target, const void* d
                           const int32_t* parent, const float* u_accept, const float* u_final,
                           const eagle_accept_out& out, void* ws, cudaStream_t s);
 
+// ------------------------------------------------------------------ LM-head statistics
+int lmhead_tiles(int vocab);
+cudaError_t launch_lmhead_stats(int M, int h, int V, int R, float temperature, const void* hidden, const void* weight,
+                                const int32_t* tokens, const int32_t* parent, eagle_vocab_record* rec, float* child,
+                                uint32_t* status, int num_sms, cudaStream_t s);
+
 // ------------------------------------------------------------------ commit
 constexpr int kMaxLayers = 128;
 struct CommitArgs {

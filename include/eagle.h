@@ -300,6 +300,41 @@ int eagle_accept_noalloc(const eagle_accept_desc* d, const void* target_logits, 
                          const int32_t* tree_tokens, const int32_t* tree_parent, const float* u_accept,
                          const float* u_final, const eagle_accept_out* out, void* stream);
 
+/* ---------------------------------------------------------------- LM-head statistics */
+/* What acceptance needs from the target model's distribution at every tree node,
+ * computed from the verify pass's hidden states and the frozen LM head without
+ * writing the [rows][V] logits (EAGLE review, "GPU / system data path" steps 3 and 6:
+ * the LM head gives the distribution at each node; section 3.3 / Algorithm 1: the
+ * multi-round test reads each child's token probability under its parent, the bonus
+ * draw reads the distribution).  logits x = hidden W^T, fp32 accumulation. */
+#define EAGLE_LMHEAD_TILE 128 /* vocabulary entries per record */
+
+typedef struct {
+  int32_t rows;        /* M = B * R hidden rows, 1..128: row b * R + i is node i of request b */
+  int32_t tree_rows;   /* R, rows per request (M a multiple of R) */
+  int32_t hidden;      /* h, a multiple of 64 */
+  int32_t vocab;       /* V */
+  float temperature;   /* T of the sums (T <= 0 counts as 1) */
+} eagle_lmhead_desc;
+
+typedef struct {       /* one row's statistics over one tile of EAGLE_LMHEAD_TILE tokens */
+  float max;           /* max logit */
+  int32_t argmax;      /* its token (lowest id on ties) */
+  float sum_hi, sum_lo; /* sum exp((x - max) / T) over the tile, as the float pair hi + lo */
+} eagle_vocab_record;
+
+/* hidden [M][h] bf16, weight [V][h] bf16 (row v = token v's output embedding), both
+ * 16-byte aligned with h * 2 a multiple of 16.  records [M][ceil(V / 128)] (DEVICE).
+ * tree_tokens, tree_parent [B][R] int32 (may both be NULL): then child_logit [M] gets,
+ * for every node i >= 1 of request b, the logit of its token under its parent's row
+ * (entry b * R + i; roots and nodes whose token is out of range are left untouched).
+ * status [1] (DEVICE): EAGLE_STATUS_TIMEOUT is ORed in when a bounded wait inside the
+ * kernel gives up (2 s); the outputs are then incomplete.  Allocates nothing.
+ * Unsupported: rows > 128, h not a multiple of 64. */
+int eagle_lmhead_stats(const eagle_lmhead_desc* d, const void* hidden, const void* weight,
+                       const int32_t* tree_tokens, const int32_t* tree_parent, eagle_vocab_record* records,
+                       float* child_logit, uint32_t* status, void* stream);
+
 /* ---------------------------------------------------------------- KV commit */
 typedef struct {
   int32_t layers;      /* L, 1..128 */
