@@ -381,6 +381,7 @@ def run_ours(args):
                 else "fallback 6.8 TB/s", "traffic": traffic, "algorithmic_bytes_per_launch": bytes_layer,
                 "us_per_launch": round(attn_ms * 1e3, 2)}
     tree_build = time_tree_build(st, stream, max(20, args.steps // 2))
+    lmhead = time_lmhead(st, stream, max(10, args.steps // 4), peak)
     step_bytes = kv_total + float(np.mean([st.logit_bytes_visited(a) for a in n_acc_all]))
     step_frac = step_bytes / (ms_per_step / 1e3) / 1e9 / peak
 
@@ -395,7 +396,7 @@ def run_ours(args):
                        "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU"},
             "step_roofline_frac": round(step_frac, 4), "step_algorithmic_bytes": int(step_bytes),
             "mean_accept_length": round(float(np.mean(n_acc_all + 1)), 4), "step_variants": int(n_var),
-            "roofline": roofline, "tree_build": tree_build,
+            "roofline": roofline, "tree_build": tree_build, "lmhead_stats": lmhead,
             "e2e": e2e,
             "gpu_launches": int(launches_per_step * args.steps), "clocks": clocks,
             "setup_s": round(t_setup, 1)}
@@ -443,6 +444,48 @@ def time_tree_build(st, stream, reps: int):
     return {"us_per_tree": round(us, 2), "levels": len(bld.levels), "launches_per_tree": 2 * len(bld.levels),
             "logit_bytes_per_tree": int(logit_bytes), "gbs": round(logit_bytes / (us / 1e6) / 1e9, 1),
             "note": "timed apart from the verify step (not in value); inputs resident, L2 warm"}
+
+
+def time_lmhead(st, stream, reps: int, peak: float):
+    """The LM-head statistics at the step's tree nodes (eagle_lmhead_stats), timed apart
+    from the verify step: hidden rows of the tree's nodes (4096 wide, N(0, 1)) times a
+    random bf16 head of the workload's vocabulary (N(0, 1/4096)); the kernel reads the
+    head once, so its roofline is the head's bytes over the time."""
+    import torch
+    from eagle_speculative_decoding_tree_gb300 import binding as B
+    w = st.w
+    M, R, h, V = st.B * st.R, st.R, 4096, w.vocab
+    if M > 128 or w.dtype != "bf16":
+        return {"skipped": f"{M} rows (the kernel takes up to 128) or fp32 workload"}
+    g = torch.Generator(device="cuda").manual_seed(0xEA61E000 + w.config_id)
+    hid = torch.randn(M, h, device="cuda", generator=g).to(torch.bfloat16)
+    head = (torch.randn(V, h, device="cuda", generator=g) / 64.0).to(torch.bfloat16)
+    desc = B.LmHeadDesc(M, R, h, V, float(w.temperature))
+    rec = torch.zeros(M, -(-V // B.EAGLE_LMHEAD_TILE), 4, dtype=torch.int32, device="cuda")
+    child = torch.zeros(M, dtype=torch.float32, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    gr = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        B.eagle_lmhead_stats(desc, hid, head, st.tokens, st.parent, rec, child, status, stream)
+        stream.synchronize()
+        with torch.cuda.graph(gr, stream=stream):
+            B.eagle_lmhead_stats(desc, hid, head, st.tokens, st.parent, rec, child, status, stream)
+        for _ in range(3):
+            gr.replay()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(reps):
+            gr.replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    us = e0.elapsed_time(e1) * 1e3 / reps
+    byt = V * h * 2 + M * h * 2
+    out = {"us_per_call": round(us, 2), "rows": M, "hidden": h, "vocab": V, "algorithmic_bytes": int(byt),
+           "gbs": round(byt / us / 1e3, 1), "frac": round(byt / us / 1e3 / peak, 4), "status": int(status.item()),
+           "note": "timed apart from the verify step (not in value): head bytes read once per call"}
+    del head
+    torch.cuda.empty_cache()
+    return out
 
 
 def e2e_run(st, stream, args, ws):
