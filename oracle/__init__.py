@@ -336,3 +336,45 @@ def lmhead_accept(hidden, weight, tokens, parent, u_accept, u_final, temperature
     Bn, R = np.asarray(tokens).shape
     x = lmhead_logits(hidden, weight).astype(np.float32).reshape(Bn, R, -1)
     return accept(x, tokens, parent, u_accept, u_final, temperature, proposal, max_path)
+
+
+# ---------------------------------------------------------------------------- TTT attention
+def ttt_attn(q, k_trunk, v_trunk, k_branch, v_branch, scale: float):
+    """Attention of EAGLE-3's training-time test (EAGLE-3 visual reading, "训练时的
+    Attention Mask 设计"; Didi article sections 5.2-5.3).  TTT step j's prediction at
+    position t attends causally to the original sequence (trunk keys t' <= t) and,
+    through the diagonal mask, only to its own predecessors in the earlier TTT steps
+    at the same position (branch keys (i, t), 1 <= i <= j); the two parts share one
+    softmax (the streaming-softmax / LSE fusion of trunk and branch).
+    Shapes: q [k][S][Hq][D]; k/v_trunk [Hkv][S][D]; k/v_branch [k][Hkv][S][D] (step 0
+    unused); float32 or bf16 bits.  Returns (out [k][S][Hq][D], lse [k][S][Hq]) in
+    float64, lse the natural log of the softmax normaliser of the scaled scores."""
+    def f64(a):
+        a = np.asarray(a)
+        if a.dtype == np.uint16:
+            return (a.astype(np.uint32) << np.uint32(16)).view(np.float32).astype(np.float64)
+        return a.astype(np.float64)
+    q, kt, vt, kb, vb = (f64(x) for x in (q, k_trunk, v_trunk, k_branch, v_branch))
+    K, S, Hq, D = q.shape
+    Hkv = kt.shape[0]
+    G = Hq // Hkv
+    out = np.zeros((K, S, Hq, D))
+    lse = np.zeros((K, S, Hq))
+    causal = np.tril(np.ones((S, S), bool))
+    for j in range(K):
+        for hq in range(Hq):
+            h = hq // G
+            s_trunk = (q[j, :, hq] @ kt[h].T) * scale                       # [S][S]
+            s_trunk = np.where(causal, s_trunk, -np.inf)
+            s_br = np.stack([np.einsum("td,td->t", q[j, :, hq], kb[i, h]) * scale for i in range(1, j + 1)],
+                            axis=1) if j > 0 else np.zeros((S, 0))          # [S][j]
+            s = np.concatenate([s_trunk, s_br], axis=1)
+            m = s.max(axis=1, keepdims=True)
+            p = np.exp(s - m)
+            l = p.sum(axis=1, keepdims=True)
+            o = p[:, :S] @ vt[h]
+            for i in range(1, j + 1):
+                o += p[:, S + i - 1:S + i] * vb[i, h]
+            out[j, :, hq] = o / l
+            lse[j, :, hq] = (m + np.log(l))[:, 0]
+    return out, lse
