@@ -32,7 +32,7 @@ EXPORTED_SYMBOLS = ("eagle_tree_build", "eagle_tree_attn", "eagle_accept", "eagl
                     "eagle_workspace_size", "eagle_status_string", "eagle_version",
                     "eagle_tree_frontier_rows", "eagle_tree_max_frontier", "eagle_last_cuda_error",
                     "eagle_last_cuda_error_string", "eagle_tree_attn_plan", "eagle_accept_noalloc",
-                    "eagle_selftest_ff_log", "eagle_lmhead_stats")
+                    "eagle_selftest_ff_log", "eagle_lmhead_stats", "eagle_ttt_attn")
 
 
 class TreeDesc(ctypes.Structure):
@@ -71,6 +71,13 @@ class LmHeadDesc(ctypes.Structure):
 
 
 EAGLE_LMHEAD_TILE = 128
+EAGLE_WS_TTT_ATTN = 4
+
+
+class TttDesc(ctypes.Structure):
+    _fields_ = [("steps", ctypes.c_int32), ("seq", ctypes.c_int32), ("n_q_heads", ctypes.c_int32),
+                ("n_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32), ("scale", ctypes.c_float),
+                ("out_dtype", ctypes.c_int32)]
 EAGLE_STATUS_TIMEOUT = 0x10
 
 
@@ -105,6 +112,7 @@ def load() -> ctypes.CDLL:
         L.eagle_kv_commit.argtypes = [ctypes.POINTER(CommitDesc), vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
         L.eagle_selftest_ff_log.argtypes = [vp, vp, vp, vp, i32, vp]
         L.eagle_lmhead_stats.argtypes = [ctypes.POINTER(LmHeadDesc), vp, vp, vp, vp, vp, vp, vp, vp]
+        L.eagle_ttt_attn.argtypes = [ctypes.POINTER(TttDesc), vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
         L.eagle_workspace_size.argtypes = [i32, vp]
         L.eagle_workspace_size.restype = sz
         L.eagle_status_string.argtypes = [i32]
@@ -345,3 +353,13 @@ def eagle_lmhead_stats(desc: LmHeadDesc, hidden, weight, tree_tokens, tree_paren
         _ptr(tree_tokens, torch.int32, "tree_tokens"), _ptr(tree_parent, torch.int32, "tree_parent"),
         _ptr(records, torch.int32, "records"), _ptr(child_logit, torch.float32, "child_logit"),
         _ptr(status, torch.int32, "status"), _stream(stream)))
+
+
+def eagle_ttt_attn(desc: TttDesc, q, k_trunk, v_trunk, k_branch, v_branch, out, lse: Optional[torch.Tensor],
+                   ws: torch.Tensor, stream=None) -> None:
+    """Training-time-test attention (see eagle.h: eagle_ttt_attn)."""
+    _check("eagle_ttt_attn", load().eagle_ttt_attn(
+        ctypes.byref(desc), _ptr(q, torch.bfloat16, "q"), _ptr(k_trunk, torch.bfloat16, "k_trunk"),
+        _ptr(v_trunk, torch.bfloat16, "v_trunk"), _ptr(k_branch, torch.bfloat16, "k_branch"),
+        _ptr(v_branch, torch.bfloat16, "v_branch"), _ptr(out, FLOATS, "out"), _ptr(lse, torch.float32, "lse"),
+        _ptr(ws, name="ws"), ws.numel() * ws.element_size(), _stream(stream)))

@@ -84,6 +84,18 @@ int check_attn_desc(const eagle_attn_desc* d) {
   return EAGLE_OK;
 }
 
+int check_ttt_desc(const eagle_ttt_desc* d) {
+  if (!d) return EAGLE_ERR_INVALID_ARG;
+  if (d->steps < 1 || d->seq < 1 || d->n_q_heads < 1 || d->n_kv_heads < 1 || !(d->scale > 0.f) ||
+      !isfinite(d->scale))
+    return EAGLE_ERR_INVALID_ARG;
+  if (d->head_dim != 128 || d->n_q_heads % d->n_kv_heads || 128 % (d->n_q_heads / d->n_kv_heads))
+    return EAGLE_ERR_UNSUPPORTED;
+  if (d->out_dtype != EAGLE_BF16 && d->out_dtype != EAGLE_F32) return EAGLE_ERR_UNSUPPORTED;
+  if (static_cast<long long>(d->steps) * d->n_kv_heads > 65535) return EAGLE_ERR_UNSUPPORTED;  // grid z
+  return EAGLE_OK;
+}
+
 int check_accept_desc(const eagle_accept_desc* d) {
   if (!d) return EAGLE_ERR_INVALID_ARG;
   if (d->batch < 1 || d->rows < 1 || d->vocab < 1 || d->max_depth < 0) return EAGLE_ERR_INVALID_ARG;
@@ -144,6 +156,8 @@ size_t eagle_workspace_size(int which, const void* desc) {
       plan_accept(d, &p);
       return p.total;
     }
+    case EAGLE_WS_TTT_ATTN:
+      return check_ttt_desc(static_cast<const eagle_ttt_desc*>(desc)) == EAGLE_OK ? 256 : 0;
     default: return 0;
   }
 }
@@ -268,6 +282,23 @@ int eagle_kv_commit(const eagle_commit_desc* d, void* const* k_cache_layers, voi
   }
   return cuda_status(launch_kv_commit(d, a, n_acc, path, seq_len, commit_pos, feat_cache, tree_feat, status,
                           static_cast<cudaStream_t>(stream)));
+}
+
+
+int eagle_ttt_attn(const eagle_ttt_desc* d, const void* q, const void* k_trunk, const void* v_trunk,
+                   const void* k_branch, const void* v_branch, void* out, float* lse, void* ws, size_t ws_bytes,
+                   void* stream) {
+  const int rc = check_ttt_desc(d);
+  if (rc != EAGLE_OK) return rc;
+  if (!q || !k_trunk || !v_trunk || !out || (d->steps > 1 && (!k_branch || !v_branch))) return EAGLE_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k_trunk, 16) || !aligned(v_trunk, 16) || !aligned(out, 16) ||
+      (k_branch && !aligned(k_branch, 16)) || (v_branch && !aligned(v_branch, 16)) || (lse && !aligned(lse, 4)) ||
+      (ws && !aligned(ws, 16)))
+    return EAGLE_ERR_ALIGNMENT;
+  if (!ws || ws_bytes < 256) return EAGLE_ERR_WORKSPACE;
+  return cuda_status(launch_ttt_attn_tc(d->steps, d->seq, d->n_q_heads, d->n_kv_heads, d->scale,
+                                        d->out_dtype == EAGLE_F32, q, k_trunk, v_trunk, k_branch, v_branch, out, lse,
+                                        ws, static_cast<cudaStream_t>(stream)));
 }
 
 int eagle_lmhead_stats(const eagle_lmhead_desc* d, const void* hidden, const void* weight,

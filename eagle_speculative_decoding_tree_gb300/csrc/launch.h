@@ -75,6 +75,11 @@ cudaError_t launch_tree_attn(const AttnPlan& p, const void* q, const void* k_cac
                              const void* tree_k, const void* tree_v, const int32_t* seq_len, const int32_t* n_nodes,
                              const uint64_t* anc_mask, void* out, float* lse, void* ws, cudaStream_t s);
 
+// Training-time-test attention on the tcgen05 kernel (see eagle.h: eagle_ttt_attn).
+cudaError_t launch_ttt_attn_tc(int steps, int S, int Hq, int Hkv, float scale, bool out_f32, const void* q,
+                               const void* k_trunk, const void* v_trunk, const void* k_branch, const void* v_branch,
+                               void* out, float* lse, void* ws, cudaStream_t s);
+
 // ------------------------------------------------------------------ accept
 struct AcceptPlan {
   int B, R, V, dtype, proposal, max_depth;

@@ -92,6 +92,15 @@ struct TcArgs {
   int tps;         // > 0: split s takes tile units [s tps, (s + 1) tps) of its request
                    //      (splits past a request's last unit do nothing); 0: even splits
   int lpt;         // 1: the request index of the grid is a rank in decreasing sequence length
+  // Training-time-test attention (causal = 1): "request" b is TTT step j, "node" t is
+  // sequence position t (R = P = S); the keys are the trunk K/V [Hkv][S][128] shared by
+  // every step, row t sees keys t' <= t, and step j's rows then take j more keys, their
+  // own predecessors (i, t), 1 <= i <= j, from the branch K/V [k][Hkv][S][128], folded
+  // into the same softmax in the epilogue (one split, no partials).
+  int causal;
+  const uint16_t* qg;  // Q [k][S][Hq][128] (the branch dot products)
+  const uint16_t* kb;
+  const uint16_t* vb;
   int* cnt;        // coop: [2][n_groups] published / finished splits per (request, KV head, row block)
   int n_groups;
   int group_need;  // splits a group waits for (splits; one more under the failure test hook)
@@ -121,8 +130,17 @@ __device__ __forceinline__ int rows_of(const TcArgs& a, int b) {
   return n < 0 ? 0 : (n > a.R ? a.R : n);
 }
 
-__device__ __forceinline__ TileInfo tile_info(const TcArgs& a, int b, int split) {
+__device__ __forceinline__ TileInfo tile_info(const TcArgs& a, int b, int split, int rb) {
   TileInfo ti;
+  if (a.causal) {  // keys 0 .. (last position of this CTA's rows), one split, no tree tile
+    const int per = 128 / a.G;
+    const int L = min(a.R, (rb + 1) * per);
+    ti.t_begin = 0;
+    ti.n_pt = ti.n_tiles = (L + KT - 1) / KT;
+    ti.L = L;
+    ti.Rb = a.R;
+    return ti;
+  }
   const int L = clamp_len(a, a.seq_len[b]);
   // units of work: the prefix tiles, then the tree tile; split s takes units
   // [U s / S, U (s + 1) / S) (or [s tps, (s + 1) tps) when tps > 0), so only the last
@@ -378,7 +396,7 @@ __device__ __forceinline__ float emit_p32(const uint32_t (&r)[32], uint32_t col,
   return sum;
 }
 
-template <bool PRECISE>
+template <bool PRECISE, bool CAUSAL>
 __global__ void __launch_bounds__(NTHREADS, 1)
     tree_attn_tc_kernel(const __grid_constant__ Tmaps tm, const TcArgs a) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -450,7 +468,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   // seq_len is read; with fixed-size splits only a CTA that has tiles loads it.  The MMA
   // warp waits for every Q load, so no copy is in flight at exit.
   if (a.tps == 0 && warp == 8 && lane == 0) load_q();
-  const TileInfo ti = tile_info(a, b, split);
+  const TileInfo ti = tile_info(a, b, split, rb);
   const bool q_loaded = a.tps == 0 || ti.n_tiles > 0;
   if (a.tps > 0 && q_loaded && warp == 8 && lane == 0) load_q();
   const uint32_t tb = tmem_base;
@@ -462,7 +480,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       for (int t = 0; t < ti.n_tiles; ++t) {
         const int s = t % KST, use = t / KST, sv = t % VST, usev = t / VST;
         const bool tree = t >= ti.n_pt;
-        const int y = tree ? bh * a.R : bh * a.P + (ti.t_begin + t) * KT;
+        const int y = tree ? bh * a.R : (CAUSAL ? h : bh) * a.P + (ti.t_begin + t) * KT;
         if (use > 0 && !wait_parity(&k_empty[s], (use - 1) & 1, a.err, ERR_KEMPTY)) break;
         mbar_arrive_expect_tx(&k_full[s], TILE);
         load_kv_tile(tree ? tm.tk : tm.kc, smem + SM_K + s * TILE, y, &k_full[s], policy);
@@ -533,7 +551,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const int node = vrow ? row / a.G : 0;
     const int hq = h * a.G + (vrow ? row % a.G : 0);
     uint32_t tw[4] = {0u, 0u, 0u, 0u};  // the row's ancestor words over the tree keys
-    if (vrow) {
+    if (vrow && !CAUSAL) {
       const uint64_t* mrow = a.anc_mask + (static_cast<size_t>(b) * a.R + node) * a.W;
       const uint64_t w0 = mrow[0], w1 = a.W > 1 ? mrow[1] : 0ull;
       tw[0] = static_cast<uint32_t>(w0) & low_bits(ti.Rb);
@@ -554,7 +572,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       const int nv = tile_valid(ti, t);
       uint32_t km[4];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) km[i] = !vrow ? 0u : (tree ? tw[i] : low_bits(nv - 32 * i));
+      for (int i = 0; i < 4; ++i)
+        km[i] = !vrow ? 0u
+                      : (CAUSAL ? low_bits(min(nv, node + 1 - (ti.t_begin + t) * KT) - 32 * i)
+                                  : (tree ? tw[i] : low_bits(nv - 32 * i)));
       const bool full = __all_sync(0xffffffffu, (km[0] & km[1] & km[2] & km[3]) == 0xffffffffu);
       const uint32_t sc = lb + col_s(wg);
       // keys 64..127 stay in registers from the max to the exponentials; keys 0..63
@@ -644,10 +665,54 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 #pragma unroll
       for (int k = 0; k < 64; ++k) o[k] = 0.f;
     }
+    float M_out = M, L_out = L;
+    if (CAUSAL && b > 0) {
+      // step b's own predecessors at this position, (i, node) for i = 1..b: one more
+      // key each, folded into the row's softmax (streaming: new max, rescale, add).  The
+      // two warpgroups each hold 64 of the 128 dims: partial dot products meet in shared
+      // memory (the Q area, unused by now)
+      float* s_dot = reinterpret_cast<float*>(smem + SM_Q + 2048);  // [2][128]
+      const uint16_t* qrow = a.qg + (static_cast<size_t>(b * a.R + node) * a.Hq + hq) * 128 + 64 * wg;
+      for (int i = 1; i <= b; ++i) {
+        const size_t kvrow = ((static_cast<size_t>(i) * a.Hkv + h) * a.P + node) * 128 + 64 * wg;
+        float part = 0.f;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const uint4 u = *reinterpret_cast<const uint4*>(a.kb + kvrow + 8 * k);
+          const uint4 qq = *reinterpret_cast<const uint4*>(qrow + 8 * k);
+          const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+          const uint32_t q4[4] = {qq.x, qq.y, qq.z, qq.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            part = fmaf(__uint_as_float(q4[e] << 16), __uint_as_float(w4[e] << 16), part);
+            part = fmaf(__uint_as_float(q4[e] & 0xffff0000u), __uint_as_float(w4[e] & 0xffff0000u), part);
+          }
+        }
+        s_dot[wg * 128 + r_local] = part;
+        bar_sync(1, 256);
+        const float sc = s_dot[r_local] + s_dot[128 + r_local];  // the same sum in both halves
+        bar_sync(1, 256);
+        const float m_new = fmaxf(M_out, sc);
+        const float a_old = M_out == -INFINITY ? 0.f : ex2((M_out - m_new) * sl2);
+        const float a_new = ex2((sc - m_new) * sl2);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const uint4 u = *reinterpret_cast<const uint4*>(a.vb + kvrow + 8 * k);
+          const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            o[8 * k + 2 * e] = fmaf(o[8 * k + 2 * e], a_old, a_new * __uint_as_float(w4[e] << 16));
+            o[8 * k + 2 * e + 1] = fmaf(o[8 * k + 2 * e + 1], a_old, a_new * __uint_as_float(w4[e] & 0xffff0000u));
+          }
+        }
+        L_out = L_out * a_old + a_new;
+        M_out = m_new;
+      }
+    }
     const size_t prow = (static_cast<size_t>(bh) * a.splits + split) * a.rows_pad + rb * 128 + r_local;
     if (a.splits == 1) {
       if (vrow && all_done) {
-        const float inv = L > 0.f ? 1.f / L : 0.f;
+        const float inv = L_out > 0.f ? 1.f / L_out : 0.f;
         const size_t orow = (static_cast<size_t>(b * a.R + node) * a.Hq + hq) * 128 + 64 * wg;
         if (a.out_f32) {
           float4* dst = reinterpret_cast<float4*>(static_cast<float*>(a.out) + orow);
@@ -667,7 +732,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             dst[k] = make_uint4(w[0], w[1], w[2], w[3]);
           }
         }
-        if (a.lse && wg == 0) a.lse[static_cast<size_t>(b * a.R + node) * a.Hq + hq] = a.scale * M + logf(L);
+        if (a.lse && wg == 0)
+          a.lse[static_cast<size_t>(b * a.R + node) * a.Hq + hq] = a.scale * M_out + logf(L_out);
       }
     } else if (all_done) {
       // partial O of the M-tile (128 rows, contiguous in the workspace) staged in the
@@ -777,14 +843,15 @@ bool make_tmap(CUtensorMap* m, CUtensorMapDataType dt, const void* base, int ran
 }
 
 // One-time per-device kernel attribute: the dynamic shared memory.
-template <bool PRECISE>
+template <bool PRECISE, bool CAUSAL>
 cudaError_t configure_tc() {
   static unsigned long long configured = 0;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 64 && (__atomic_load_n(&configured, __ATOMIC_ACQUIRE) & (1ull << dev))) return cudaSuccess;
-  e = cudaFuncSetAttribute(tree_attn_tc_kernel<PRECISE>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+  e = cudaFuncSetAttribute(tree_attn_tc_kernel<PRECISE, CAUSAL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           SMEM_BYTES);
   if (e != cudaSuccess) return e;
   if (dev < 64) __atomic_fetch_or(&configured, 1ull << dev, __ATOMIC_RELEASE);
   return cudaSuccess;
@@ -793,9 +860,9 @@ cudaError_t configure_tc() {
 // Cooperative launch when the CTAs of a split group wait on one another (a.coop):
 // the driver then guarantees that the whole grid is resident at once, or fails the
 // launch.
-template <bool PRECISE>
+template <bool PRECISE, bool CAUSAL = false>
 cudaError_t launch_tc(const Tmaps& tm, const TcArgs& a, dim3 grid, cudaStream_t s) {
-  cudaError_t e = configure_tc<PRECISE>();
+  cudaError_t e = configure_tc<PRECISE, CAUSAL>();
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
@@ -814,7 +881,7 @@ cudaError_t launch_tc(const Tmaps& tm, const TcArgs& a, dim3 grid, cudaStream_t 
   }
   cfg.attrs = attr;
   cfg.numAttrs = n;
-  e = cudaLaunchKernelEx(&cfg, tree_attn_tc_kernel<PRECISE>, tm, a);
+  e = cudaLaunchKernelEx(&cfg, tree_attn_tc_kernel<PRECISE, CAUSAL>, tm, a);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
@@ -878,6 +945,8 @@ cudaError_t launch_tree_attn_tc(const AttnPlan& p, const void* q, const void* k_
   a.coop = p.coop ? 1 : 0;
   a.tps = p.tps;
   a.lpt = p.lpt ? 1 : 0;
+  a.causal = 0;
+  a.qg = a.kb = a.vb = nullptr;
   a.cnt = p.coop ? reinterpret_cast<int*>(w + p.off_cnt) : nullptr;
   a.n_groups = p.B * p.Hkv * p.row_blocks;
   // the failure test hook: the group waits for one split that does not exist and gives
@@ -893,6 +962,55 @@ cudaError_t launch_tree_attn_tc(const AttnPlan& p, const void* q, const void* k_
   if (e != cudaSuccess || !partials || p.coop) return e;
   return launch_tree_attn_combine(p, seq_len, n_nodes, out, lse, static_cast<const float*>(a.part_o), a.part_ml, s,
                                   true);
+}
+
+cudaError_t launch_ttt_attn_tc(int steps, int S, int Hq, int Hkv, float scale, bool out_f32, const void* q,
+                               const void* k_trunk, const void* v_trunk, const void* k_branch, const void* v_branch,
+                               void* out, float* lse, void* ws, cudaStream_t s) {
+  const int G = Hq / Hkv;
+  Tmaps tm;
+  const cuuint64_t D = 128;
+  {
+    const cuuint64_t dims[3] = {D, static_cast<cuuint64_t>(Hq), static_cast<cuuint64_t>(steps) * S};
+    const cuuint64_t strides[2] = {D * 2, static_cast<cuuint64_t>(Hq) * D * 2};
+    const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(G), static_cast<cuuint32_t>(128 / G)};
+    if (!make_tmap(&tm.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, q, 3, dims, strides, box)) return cudaErrorInvalidValue;
+  }
+  {
+    const cuuint64_t dims[2] = {D, static_cast<cuuint64_t>(Hkv) * S};
+    const cuuint64_t strides[1] = {D * 2};
+    const cuuint32_t box[2] = {64, 128};
+    if (!make_tmap(&tm.kc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, k_trunk, 2, dims, strides, box)) return cudaErrorInvalidValue;
+    if (!make_tmap(&tm.vc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, v_trunk, 2, dims, strides, box)) return cudaErrorInvalidValue;
+  }
+  tm.tk = tm.kc;  // no tree tile in this mode
+  tm.tv = tm.vc;
+  memset(&tm.po, 0, sizeof(tm.po));
+  TcArgs a;
+  memset(&a, 0, sizeof(a));
+  a.out = out;
+  a.lse = lse;
+  a.err = static_cast<int*>(ws);
+  a.B = steps;
+  a.R = S;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.G = G;
+  a.P = S;
+  a.W = 1;
+  a.splits = 1;
+  const int row_blocks = (S * G + 127) / 128;
+  a.rows_pad = row_blocks * 128;
+  a.out_f32 = out_f32 ? 1 : 0;
+  a.group_need = 1;
+  a.group_limit_ns = 2000000000ull;
+  a.scale = scale;
+  a.scale_log2 = scale * kLog2e;
+  a.causal = 1;
+  a.qg = static_cast<const uint16_t*>(q);
+  a.kb = static_cast<const uint16_t*>(k_branch);
+  a.vb = static_cast<const uint16_t*>(v_branch);
+  return launch_tc<true, true>(tm, a, dim3(row_blocks, 1, steps * Hkv), s);
 }
 
 }  // namespace eagle

@@ -119,7 +119,7 @@ enum {
 enum { EAGLE_ENGINE_AUTO = 0, EAGLE_ENGINE_MMA_SYNC = 1 };
 
 /* Workspace kinds for eagle_workspace_size() */
-enum { EAGLE_WS_TREE_BUILD = 1, EAGLE_WS_TREE_ATTN = 2, EAGLE_WS_ACCEPT = 3 };
+enum { EAGLE_WS_TREE_BUILD = 1, EAGLE_WS_TREE_ATTN = 2, EAGLE_WS_ACCEPT = 3, EAGLE_WS_TTT_ATTN = 4 };
 
 /* ---------------------------------------------------------------- tree build */
 typedef struct {
@@ -299,6 +299,41 @@ int eagle_accept(const eagle_accept_desc* d, const void* target_logits, const vo
 int eagle_accept_noalloc(const eagle_accept_desc* d, const void* target_logits, const void* draft_logits,
                          const int32_t* tree_tokens, const int32_t* tree_parent, const float* u_accept,
                          const float* u_final, const eagle_accept_out* out, void* stream);
+
+/* ---------------------------------------------------------------- training-time-test attention */
+/* The attention of EAGLE-3's training-time test (EAGLE-3 visual reading, "训练时的
+ * Attention Mask 设计"; Didi EAGLE-3 article, sections 5.2-5.3): the draft model is
+ * trained on its own k-step rollouts, and TTT step j's prediction at position t attends
+ * causally to the original sequence (trunk keys t' <= t) and, through the diagonal
+ * mask, only to its own predecessors at the same position in the earlier steps (branch
+ * keys (i, t), 1 <= i <= j), all under one softmax:
+ *     out = softmax(scale * q [K_trunk(<= t); K_branch(1..j, t)]^T) [V_trunk(<= t); V_branch(1..j, t)]
+ *     lse = ln sum exp(...)
+ * The trunk runs on the tensor cores (the causal keys, tile by tile, with the tree
+ * attention kernel's machinery); the j branch keys of a row are a few dot products
+ * folded into the row's softmax at the end (the streaming-softmax fusion of trunk and
+ * branch).  bf16 inputs, fp32 accumulation, P split into two bf16 terms in the PV
+ * product (as EAGLE_ATTN_PRECISE).
+ *   q [k][S][Hq][128]; k_trunk, v_trunk [Hkv][S][128] (the original sequence's keys,
+ *   shared by every step); k_branch, v_branch [k][Hkv][S][128] (step i's predictions'
+ *   keys; step 0's entries are not read); out [k][S][Hq][128] (bf16 or fp32 by
+ *   out_dtype); lse [k][S][Hq] fp32, may be NULL.
+ * ws: eagle_workspace_size(EAGLE_WS_TTT_ATTN, d) bytes, zero-filled; its first 4 bytes
+ * are an error word that a bounded wait ORs a bit into when it gives up (2 s).
+ * Unsupported: head_dim != 128, 128 % (Hq / Hkv) != 0, Hq % Hkv != 0. */
+typedef struct {
+  int32_t steps;       /* k >= 1 */
+  int32_t seq;         /* S >= 1 */
+  int32_t n_q_heads;   /* Hq */
+  int32_t n_kv_heads;  /* Hkv */
+  int32_t head_dim;    /* 128 */
+  float scale;         /* usually 1/sqrt(128) */
+  int32_t out_dtype;   /* EAGLE_BF16 or EAGLE_F32 */
+} eagle_ttt_desc;
+
+int eagle_ttt_attn(const eagle_ttt_desc* d, const void* q, const void* k_trunk, const void* v_trunk,
+                   const void* k_branch, const void* v_branch, void* out, float* lse, void* ws, size_t ws_bytes,
+                   void* stream);
 
 /* ---------------------------------------------------------------- LM-head statistics */
 /* What acceptance needs from the target model's distribution at every tree node,
