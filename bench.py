@@ -382,6 +382,7 @@ def run_ours(args):
                 "us_per_launch": round(attn_ms * 1e3, 2)}
     tree_build = time_tree_build(st, stream, max(20, args.steps // 2))
     lmhead = time_lmhead(st, stream, max(10, args.steps // 4), peak)
+    ttt = time_ttt(stream, 5) if args.config in ("llama8b", "vicuna7b") else {"skipped": "run with the 8B workloads"}
     step_bytes = kv_total + float(np.mean([st.logit_bytes_visited(a) for a in n_acc_all]))
     step_frac = step_bytes / (ms_per_step / 1e3) / 1e9 / peak
 
@@ -396,7 +397,7 @@ def run_ours(args):
                        "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU"},
             "step_roofline_frac": round(step_frac, 4), "step_algorithmic_bytes": int(step_bytes),
             "mean_accept_length": round(float(np.mean(n_acc_all + 1)), 4), "step_variants": int(n_var),
-            "roofline": roofline, "tree_build": tree_build, "lmhead_stats": lmhead,
+            "roofline": roofline, "tree_build": tree_build, "lmhead_stats": lmhead, "ttt_attention": ttt,
             "e2e": e2e,
             "gpu_launches": int(launches_per_step * args.steps), "clocks": clocks,
             "setup_s": round(t_setup, 1)}
@@ -486,6 +487,47 @@ def time_lmhead(st, stream, reps: int, peak: float):
     del head
     torch.cuda.empty_cache()
     return out
+
+
+def time_ttt(stream, reps: int):
+    """EAGLE-3 training-time-test attention (eagle_ttt_attn) for an 8B-shaped draft layer
+    in training: 32 q / 8 kv heads x 128, sequence 4096, 7 TTT steps, bf16 N(0, 1)
+    inputs; timed apart from the verify step.  Its work is the causal trunk's products,
+    2 * 128 * S (S + 1) flops per (step, query head) (QK^T and PV, the causal half), so
+    its roofline is the tensor pipe (measured bf16 peak)."""
+    import torch
+    from eagle_speculative_decoding_tree_gb300 import binding as B
+    K, S, Hq, Hkv, D = 7, 4096, 32, 8, 128
+    g = torch.Generator(device="cuda").manual_seed(0xEA61E7)
+    mk = lambda *shape: torch.randn(*shape, device="cuda", generator=g).to(torch.bfloat16)
+    q, kt, vt, kb, vb = mk(K, S, Hq, D), mk(Hkv, S, D), mk(Hkv, S, D), mk(K, Hkv, S, D), mk(K, Hkv, S, D)
+    out = torch.empty(K, S, Hq, D, dtype=torch.bfloat16, device="cuda")
+    desc = B.TttDesc(K, S, Hq, Hkv, D, 1.0 / math.sqrt(D), B.EAGLE_BF16)
+    ws = torch.zeros(B.workspace_size(B.EAGLE_WS_TTT_ATTN, desc), dtype=torch.uint8, device="cuda")
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            B.eagle_ttt_attn(desc, q, kt, vt, kb, vb, out, None, ws, stream)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(reps):
+            B.eagle_ttt_attn(desc, q, kt, vt, kb, vb, out, None, ws, stream)
+        e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / reps
+    flops = K * Hq * 2.0 * D * S * (S + 1)
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            tpeak = float(json.load(f)["bf16_tflops"])
+    except Exception:
+        tpeak = 1900.0
+    tf = flops / (ms / 1e3) / 1e12
+    res = {"shape": f"{Hq}q/{Hkv}kv x {D}, sequence {S}, {K} TTT steps", "ms_per_call": round(ms, 3),
+           "bound": "tensor", "achieved": round(tf, 1), "peak": tpeak, "unit": "TFLOP/s", "frac": round(tf / tpeak, 4),
+           "algorithmic_flops": flops, "error_word": int(ws[:4].view(torch.int32).item()),
+           "note": "timed apart from the verify step; P enters PV as two bf16 terms (1.5x the MMAs of the flops counted)"}
+    del q, kt, vt, kb, vb, out
+    torch.cuda.empty_cache()
+    return res
 
 
 def e2e_run(st, stream, args, ws):
