@@ -38,7 +38,7 @@ int num_sms() {
 int check_tree_desc(const eagle_tree_desc* d) {
   if (!d) return EAGLE_ERR_INVALID_ARG;
   if (d->batch < 1 || d->vocab < 1) return EAGLE_ERR_INVALID_ARG;
-  if (!dtype_ok(d->dtype) || d->vocab > kMaxVocabTiles * kVocabChunk) return EAGLE_ERR_UNSUPPORTED;
+  if (!dtype_ok(d->dtype) || d->vocab > kMaxTreeChunks * kVocabChunk) return EAGLE_ERR_UNSUPPORTED;
   if (d->mode == EAGLE_TREE_DYNAMIC) {
     if (d->depth < 1 || d->top_k < 1 || d->total_tokens < 1) return EAGLE_ERR_INVALID_ARG;
     if (d->depth > kMaxDepth || d->top_k > kMaxTopK || d->top_k > d->vocab) return EAGLE_ERR_UNSUPPORTED;

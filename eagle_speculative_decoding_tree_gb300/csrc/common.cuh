@@ -16,6 +16,7 @@ constexpr int kMaxTopK = 16;      // children per frontier node
 constexpr int kMaxDepth = 16;     // draft levels
 constexpr int kMaxPool = 2048;    // dynamic-tree candidate pool per request
 constexpr int kVocabChunk = 4096; // elements of a logit row per CTA in the vocabulary passes
+constexpr int kMaxTreeChunks = 128; // tree build: vocabulary <= 128 * 4096 = 524288 tokens
 constexpr int kMaxVocabTiles = 512;  // vocabulary <= 512 * 4096 = 2M tokens
 constexpr float kLog2e = 1.4426950408889634f;
 

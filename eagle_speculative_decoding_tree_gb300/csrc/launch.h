@@ -28,7 +28,7 @@ struct TreeBuildPlan {
   StaticShape shape;
   // workspace carve-up (byte offsets)
   size_t off_pool_tok, off_pool_par, off_pool_score, off_pool_depth, off_state, off_front,
-      off_part, off_node_tok, off_node_score, total;
+      off_part, off_node_tok, off_node_score, off_ticket, off_front_score, off_best_score, off_best_idx, total;
 };
 void plan_tree_build(const eagle_tree_desc* d, TreeBuildPlan* p);
 int frontier_rows(const TreeBuildPlan& p, int level);

@@ -13,14 +13,19 @@
 // best tokens in rank order (greedy) or i.i.d. inverse-CDF draws from
 // softmax(row / T) (non-greedy).
 //
-// Kernels
-//   tree_chunk_kernel   one CTA per (request x frontier row, 4096-token chunk): the
-//                       chunk max, sum exp (T = 1 and T) and the chunk's top-16 by
-//                       (logit desc, id asc), from one read of the logits held in
-//                       registers (16 per thread).
-//   tree_select_kernel  one CTA per request: merges the chunk results per row,
-//                       extends the pool, picks the frontier (bitonic sort in shared
-//                       memory) and, at the last level, emits the tree arrays.
+// One launch per level: tree_level_kernel, one CTA per (request x frontier row,
+// 4096-token chunk).
+//   chunk pass    every CTA: the chunk max, sum exp(x - m) (and sum exp((x - m) / T)
+//                 for draws) and the chunk's best kc by (logit desc, id asc), from one
+//                 read of the logits held in registers (16 per thread).
+//   row finisher  the last CTA of a row to finish (an atomic ticket): merges the row's
+//                 chunk records (M, ln Z, top-k or draws) and adds its candidates to the
+//                 pool (dynamic) or its children to the shape (static).
+//   request       the last row finisher of a request (a second ticket): picks the
+//                 next frontier (rank counting) and, at the last level, the best N of
+//                 the pool (bitonic sort in shared memory) and the tree arrays.
+// No CTA waits for another; the tickets return to zero for the next level, and level 1
+// clears them with a memset first.
 //
 // Precision: chunk sums are compensated fp32, merged as float-float (about 48
 // significant bits on the fp32 pipe; this GPU's fp64 pipe is narrow), and ln Z is a
@@ -41,6 +46,7 @@ constexpr int K = kMaxTopK;
 constexpr int kPer = kVocabChunk / kThreads;  // logits per thread in the chunk pass
 constexpr float kIcdfNearEps = 1e-7f;
 static_assert(kPer == K, "the chunk pass sorts one thread's logits as a K-entry list");
+static_assert(K * K <= kThreads, "a level's dynamic candidates are one per thread of the request's finisher");
 
 struct __align__(16) ChunkPart {
   float tv[K];    // top-K logits of the chunk, best first
@@ -64,12 +70,6 @@ struct BuildArgs {
 
 __device__ __forceinline__ ChunkPart* parts(const TreeBuildPlan& p, uint8_t* ws) {
   return reinterpret_cast<ChunkPart*>(ws + p.off_part);
-}
-
-// Order of (value, id) pairs: best first.  Two float-float values compare as reals.
-__device__ __forceinline__ bool ff_eq(ff a, ff b) { return a.hi == b.hi && a.lo == b.lo; }
-__device__ __forceinline__ bool before_ff(ff va, int ia, ff vb, int ib) {
-  return ff_gt(va, vb) || (ff_eq(va, vb) && ia < ib);
 }
 
 // (value desc, id asc) order without short-circuit evaluation (no branches).
@@ -188,8 +188,10 @@ __device__ __forceinline__ void load_chunk(const void* logits, size_t row, int l
 }
 
 // ------------------------------------------------------------------ chunk pass
+// One CTA's (frontier row, chunk) record: the chunk max, sum exp(x - m) (and, for draws,
+// sum exp((x - m) / T)) and the chunk's best kc by (logit desc, id asc).
 template <bool TOPK, bool BF16>
-__global__ void __launch_bounds__(kThreads, 2) tree_chunk_kernel(const TreeBuildPlan p, const BuildArgs a) {
+__device__ __forceinline__ void chunk_pass(const TreeBuildPlan& p, const BuildArgs& a) {
   const int bf = blockIdx.x, c = blockIdx.y;
   const int b = bf / a.F, f = bf % a.F;
   const int lo = c * kVocabChunk;
@@ -224,11 +226,11 @@ __global__ void __launch_bounds__(kThreads, 2) tree_chunk_kernel(const TreeBuild
 #pragma unroll
     for (int e = 0; e < kPer; ++e) {
       s1.add(expf(x[e] - BM));
-      sT.add(expf((x[e] - BM) * invT));
+      if constexpr (!TOPK) sT.add(expf((x[e] - BM) * invT));  // the mass at T only feeds draws
     }
   }
   const ff d1 = warp_sum_ff(csum_ff(s1));
-  const ff dT = warp_sum_ff(csum_ff(sT));
+  const ff dT = TOPK ? d1 : warp_sum_ff(csum_ff(sT));
   if (lane == 0) {
     ss1[warp] = d1;
     ssT[warp] = dT;
@@ -360,30 +362,6 @@ __global__ void __launch_bounds__(kThreads, 2) tree_chunk_kernel(const TreeBuild
 }
 
 // ------------------------------------------------------------------ select helpers
-// Block bitonic sort of n2 (power of two) entries, best first by (key desc, idx asc).
-__device__ void bitonic_sort(ff* key, int* idx, int n2) {
-  for (int k = 2; k <= n2; k <<= 1) {
-    for (int j = k >> 1; j > 0; j >>= 1) {
-      for (int i = threadIdx.x; i < n2; i += blockDim.x) {
-        const int ixj = i ^ j;
-        if (ixj > i) {
-          const bool up = (i & k) == 0;
-          const ff ki = key[i], kj = key[ixj];
-          const int ii = idx[i], ij = idx[ixj];
-          const bool sw = up ? before_ff(kj, ij, ki, ii) : before_ff(ki, ii, kj, ij);
-          if (sw) {
-            key[i] = kj;
-            key[ixj] = ki;
-            idx[i] = ij;
-            idx[ixj] = ii;
-          }
-        }
-      }
-      __syncthreads();
-    }
-  }
-}
-
 // Exclusive ranks, in index order, of the entries of fr[0, n) that are non-zero:
 // fr[i] becomes that rank, or -1 for a zero entry.  Block-wide; ends synchronised.
 __device__ void block_flag_ranks(int* fr, int n, int* s_cnt) {
@@ -408,22 +386,27 @@ __device__ void block_flag_ranks(int* fr, int n, int* s_cnt) {
 }
 
 // Float-float constants split on the host: hi = the nearest float, lo = the rest.
-constexpr float split_hi(double d) { return static_cast<float>(d); }
-constexpr float split_lo(double d) { return static_cast<float>(d - static_cast<double>(static_cast<float>(d))); }
+__host__ __device__ constexpr float split_hi(double d) { return static_cast<float>(d); }
+__host__ __device__ constexpr float split_lo(double d) {
+  return static_cast<float>(d - static_cast<double>(static_cast<float>(d)));
+}
 constexpr double kLn2 = 0.693147180559945309417232121458;
-__constant__ float kLogSeries[9][2] = {
-    {split_hi(1.0), split_lo(1.0)},           {split_hi(1.0 / 3), split_lo(1.0 / 3)},
-    {split_hi(1.0 / 5), split_lo(1.0 / 5)},   {split_hi(1.0 / 7), split_lo(1.0 / 7)},
-    {split_hi(1.0 / 9), split_lo(1.0 / 9)},   {split_hi(1.0 / 11), split_lo(1.0 / 11)},
-    {split_hi(1.0 / 13), split_lo(1.0 / 13)}, {split_hi(1.0 / 15), split_lo(1.0 / 15)},
-    {split_hi(1.0 / 17), split_lo(1.0 / 17)}};
-__constant__ float kLn2Split[2] = {split_hi(kLn2), split_lo(kLn2)};
+
 
 // ln z for a float-float z > 0 (finite, normal), as float-float, on the fp32 pipe.
 // z = 2^k w with w in [1/sqrt 2, sqrt 2); ln z = k ln 2 + ln w and, with
 // t = (w - 1) / (w + 1) (|t| < 0.172), ln w = 2 atanh t = 2 (t + t^3/3 + t^5/5 + ...);
 // the series stops after t^17 (remainder below 1e-15 of ln w).
 __device__ __forceinline__ ff ff_log(ff z) {
+  // compile-time constants: they become instruction immediates, so the logarithm reads
+  // no constant memory (whose first touch on an SM costs a round trip to L2)
+  constexpr float kLogSeries[9][2] = {
+      {split_hi(1.0), split_lo(1.0)},           {split_hi(1.0 / 3), split_lo(1.0 / 3)},
+      {split_hi(1.0 / 5), split_lo(1.0 / 5)},   {split_hi(1.0 / 7), split_lo(1.0 / 7)},
+      {split_hi(1.0 / 9), split_lo(1.0 / 9)},   {split_hi(1.0 / 11), split_lo(1.0 / 11)},
+      {split_hi(1.0 / 13), split_lo(1.0 / 13)}, {split_hi(1.0 / 15), split_lo(1.0 / 15)},
+      {split_hi(1.0 / 17), split_lo(1.0 / 17)}};
+  constexpr float kLn2Split[2] = {split_hi(kLn2), split_lo(kLn2)};
   int e;
   float w_hi = frexpf(z.hi, &e);  // z.hi = w_hi 2^e, w_hi in [0.5, 1)
   int k = e;
@@ -679,210 +662,158 @@ __device__ int warp_draw(const void* logits, size_t row, int dtype, int V, const
   return tok;
 }
 
-__global__ void __launch_bounds__(kThreads, 1) tree_select_kernel(const TreeBuildPlan p, const BuildArgs a) {
-  const int b = blockIdx.x;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  uint8_t* ws = a.ws;
-  int32_t* state = reinterpret_cast<int32_t*>(ws + p.off_state) + b * 4;  // [0] n_pool, [1] near
-  const ChunkPart* cps = parts(p, ws) + static_cast<size_t>(b) * p.f_max * p.n_chunks;
-  const float invT = 1.f / (p.temperature > 0.f ? p.temperature : 1.f);
+// ------------------------------------------------------------------ the level's finishers
+// The CTAs of a level finish in any order.  The last chunk CTA of a frontier row (an
+// atomic ticket per row) merges that row's chunk records; the last row to finish in a
+// request (a ticket per request) selects the request's next frontier and, at the last
+// level, writes the tree.  Nobody waits for anybody: a CTA that is not last returns.
+// Records written in the same launch by other CTAs are read from L2 (ld.global.cg)
+// after the ticket, never through this SM's L1.
 
-  __shared__ ff skey[kMaxPool];
-  __shared__ int sidx[kMaxPool];
-  __shared__ int srow[kMaxPool];
-  __shared__ int stok[NW][K];
-  __shared__ float sval[NW][K];
-  __shared__ int s_cnt[NW];
-  __shared__ int s_near;
-  __shared__ int spar[kMaxRows];
+// Pool entries before level `level` of a dynamic tree: level 1 adds k, every later
+// level k * k.
+__device__ __forceinline__ int pool_base(const TreeBuildPlan& p, int level) {
+  return level == 1 ? 0 : p.k + (level - 2) * p.k * p.k;
+}
 
-  if (threadIdx.x == 0) {
-    if (a.level == 1) {
-      state[0] = 0;
-      state[1] = 0;
-    }
-    s_near = 0;
-  }
+// Workspace views of one request.
+struct ReqView {
+  int32_t* state;   // [1] near-ties so far (zeroed before level 1)
+  int32_t* ptok;    // dynamic pool: token, parent pool index, score, depth
+  int32_t* ppar;
+  ff* psc;
+  int32_t* pdep;
+  int32_t* front;   // pool index of each frontier slot
+  ff* fsc;          // and its score
+  int32_t* ntok;    // static shape: node tokens and scores
+  ff* nsc;
+};
+
+__device__ __forceinline__ ReqView req_view(const TreeBuildPlan& p, uint8_t* ws, int b) {
+  ReqView v;
+  v.state = reinterpret_cast<int32_t*>(ws + p.off_state) + b * 4;
+  const size_t pc = static_cast<size_t>(b) * p.pool_cap;
+  v.ptok = reinterpret_cast<int32_t*>(ws + p.off_pool_tok) + pc;
+  v.ppar = reinterpret_cast<int32_t*>(ws + p.off_pool_par) + pc;
+  v.psc = reinterpret_cast<ff*>(ws + p.off_pool_score) + pc;
+  v.pdep = reinterpret_cast<int32_t*>(ws + p.off_pool_depth) + pc;
+  v.front = reinterpret_cast<int32_t*>(ws + p.off_front) + static_cast<size_t>(b) * K;
+  v.fsc = reinterpret_cast<ff*>(ws + p.off_front_score) + static_cast<size_t>(b) * K;
+  v.ntok = reinterpret_cast<int32_t*>(ws + p.off_node_tok) + static_cast<size_t>(b) * p.R;
+  v.nsc = reinterpret_cast<ff*>(ws + p.off_node_score) + static_cast<size_t>(b) * p.R;
+  return v;
+}
+
+// Device-scope acquire-release fetch-and-add (a ticket).
+__device__ __forceinline__ int atom_add_acq_rel(int* ptr, int v) {
+  int old;
+  asm volatile("atom.add.acq_rel.gpu.global.s32 %0, [%1], %2;" : "=r"(old) : "l"(ptr), "r"(v) : "memory");
+  return old;
+}
+
+__device__ __forceinline__ ff ldcg_ff(const ff* q) {
+  const float2 v = __ldcg(reinterpret_cast<const float2*>(q));
+  return ff{v.x, v.y};
+}
+
+// The finishers' shared memory: a row's chunk records while a row is merged, then the
+// request's selection arrays.
+constexpr int kFinParts = kMaxTreeChunks * static_cast<int>(sizeof(ChunkPart));
+constexpr int kFinSelect = (2 * kThreads + 2 * kMaxRows) * 8 + (kThreads + 2 * kMaxRows + kMaxPool) * 4;
+constexpr int kFinBytes = kFinParts > kFinSelect ? kFinParts : kFinSelect;
+
+// Copies the row's chunk records from L2 into shared memory (the whole CTA).
+__device__ void stage_parts(const ChunkPart* g, ChunkPart* sp, int n_chunks) {
+  const uint4* src = reinterpret_cast<const uint4*>(g);
+  uint4* dst = reinterpret_cast<uint4*>(sp);
+  const int n = n_chunks * static_cast<int>(sizeof(ChunkPart) / 16);
+  for (int i = threadIdx.x; i < n; i += kThreads) dst[i] = __ldcg(src + i);
   __syncthreads();
+}
 
-  if (p.mode == EAGLE_TREE_DYNAMIC) {
-    int32_t* ptok = reinterpret_cast<int32_t*>(ws + p.off_pool_tok) + static_cast<size_t>(b) * p.pool_cap;
-    int32_t* ppar = reinterpret_cast<int32_t*>(ws + p.off_pool_par) + static_cast<size_t>(b) * p.pool_cap;
-    ff* psc = reinterpret_cast<ff*>(ws + p.off_pool_score) + static_cast<size_t>(b) * p.pool_cap;
-    int32_t* pdep = reinterpret_cast<int32_t*>(ws + p.off_pool_depth) + static_cast<size_t>(b) * p.pool_cap;
-    int32_t* front = reinterpret_cast<int32_t*>(ws + p.off_front) + static_cast<size_t>(b) * K;
-    const int base = state[0];
-    const int k = p.k;
-    // extend the pool: one warp per frontier row
-    for (int f = warp; f < a.F; f += NW) {
-      const ChunkPart* cp = cps + static_cast<size_t>(f) * p.n_chunks;
-      const RowStats rs = row_stats(cp, p.n_chunks, invT);
-      merge_topk(cp, p.n_chunks, k, stok[warp], sval[warp]);
-      const int pidx = (a.level == 1) ? -1 : front[f];
-      const ff spar_score = (pidx < 0) ? ff_make(0.f) : psc[pidx];
-      if (lane < k) {
-        const int i = base + f * k + lane;
-        ptok[i] = stok[warp][lane];
-        ppar[i] = pidx;
-        psc[i] = ff_add(spar_score, log_q(sval[warp][lane], rs));
-        pdep[i] = a.level;
-      }
-      __syncwarp();
-    }
-    __syncthreads();
-    const int n_new = a.F * k;
-    // next frontier: best k of the new candidates, kept in pool order.  A candidate's
-    // rank is the number of candidates before it by (score desc, pool index asc).
-    for (int j = threadIdx.x; j < n_new; j += kThreads) skey[j] = psc[base + j];
-    __syncthreads();
-    for (int j = threadIdx.x; j < n_new; j += kThreads) {
-      const ff kj = skey[j];
-      int r = 0;
-      for (int i = 0; i < n_new; ++i) r += before_ff(skey[i], i, kj, j) ? 1 : 0;
-      if (r == k - 1 || r == k) sidx[r - (k - 1)] = j;  // the two candidates at the boundary
-      srow[j] = r < k ? 1 : 0;
-    }
-    __syncthreads();
-    // a near-tie at the boundary, unless it is an exact tie between siblings (same
-    // parent, same logit), which both sides break by pool index
-    if (threadIdx.x == 0 && n_new > k) {
-      const ff ka = skey[sidx[0]], kb = skey[sidx[1]];
-      if (ff_float(ff_sub(ka, kb)) < kNearTieEps && !(ff_eq(ka, kb) && ppar[base + sidx[0]] == ppar[base + sidx[1]]))
-        s_near += 1;
-    }
-    block_flag_ranks(srow, n_new, s_cnt);
-    for (int j = threadIdx.x; j < n_new; j += kThreads) {
-      const int slot = srow[j];
-      if (slot < 0) continue;
-      front[slot] = base + j;
-      a.out.frontier_tok[static_cast<size_t>(b) * p.f_max + slot] = ptok[base + j];
-      a.out.frontier_slot[static_cast<size_t>(b) * p.f_max + slot] = j / k;
-    }
-    __syncthreads();
-    if (threadIdx.x == 0) {
-      state[0] = base + n_new;
-      state[1] += s_near;
-      s_near = 0;
-    }
-    __syncthreads();
-    if (a.level != p.depth) return;
-
-    // ---- last level: best N of the pool, rows in pool order
-    const int np = base + n_new;
-    const int N = p.N;
-    int n2 = 1;
-    while (n2 < np) n2 <<= 1;
-    for (int j = threadIdx.x; j < n2; j += kThreads) {
-      skey[j] = j < np ? psc[j] : ff_make(-INFINITY);
-      sidx[j] = j < np ? j : INT_MAX;
-    }
-    __syncthreads();
-    bitonic_sort(skey, sidx, n2);
-    if (threadIdx.x == 0 && np > N && ff_float(ff_sub(skey[N - 1], skey[N])) < kNearTieEps &&
-        !(ff_eq(skey[N - 1], skey[N]) && ppar[sidx[N - 1]] == ppar[sidx[N]]))
-      state[1] += 1;
-    for (int j = threadIdx.x; j < np; j += kThreads) srow[j] = 0;
-    __syncthreads();
-    for (int j = threadIdx.x; j < N; j += kThreads) srow[sidx[j]] = 1;
-    __syncthreads();
-    block_flag_ranks(srow, np, s_cnt);  // row of a selected pool entry = its rank + 1
-    const size_t ob = static_cast<size_t>(b) * p.R;
-    const int L = a.seq_len[b];
-    for (int j = threadIdx.x; j < np; j += kThreads) {
-      if (srow[j] < 0) continue;
-      const int r = srow[j] + 1;
-      const int pp = ppar[j];
-      const int pr = (pp < 0) ? 0 : (srow[pp] >= 0 ? srow[pp] + 1 : 0);
-      spar[r] = pr;
-      a.out.tokens[ob + r] = ptok[j];
-      a.out.parent[ob + r] = pr;
-      a.out.depth[ob + r] = pdep[j];
-      a.out.pos_id[ob + r] = L + pdep[j];
-      a.out.score[ob + r] = ff_float(psc[j]);
-    }
-    if (threadIdx.x == 0) {
-      spar[0] = -1;
-      a.out.tokens[ob] = a.root_tok[b];
-      a.out.parent[ob] = -1;
-      a.out.depth[ob] = 0;
-      a.out.pos_id[ob] = L;
-      a.out.score[ob] = 0.f;
-    }
-    __syncthreads();
-  } else {
-    // ---- static shape
-    int32_t* ntok = reinterpret_cast<int32_t*>(ws + p.off_node_tok) + static_cast<size_t>(b) * p.R;
-    ff* nsc = reinterpret_cast<ff*>(ws + p.off_node_score) + static_cast<size_t>(b) * p.R;
-    const bool sampled = p.mode == EAGLE_TREE_STATIC_SAMPLED;
-    if (a.level == 1 && threadIdx.x == 0) {
-      ntok[0] = a.root_tok[b];
-      nsc[0] = ff_make(0.f);
-    }
-    __syncthreads();
-    // frontier row f = the f-th node of depth level-1; one warp per row
-    int near_local = 0;
-    for (int f = warp; f < a.F; f += NW) {
-      int n = -1;
-      for (int i = 0; i < p.R; ++i)
-        if (p.shape.depth[i] == a.level - 1 && p.shape.lrank[i] == f) {
-          n = i;
-          break;
-        }
-      if (n < 0) continue;
-      int kids = 0;
-      for (int i = n + 1; i < p.R; ++i) kids += (p.shape.parent[i] == n);
-      if (kids == 0) continue;
-      const ChunkPart* cp = cps + static_cast<size_t>(f) * p.n_chunks;
-      const RowStats rs = row_stats(cp, p.n_chunks, invT);
-      const size_t row = (static_cast<size_t>(b) * a.F + f) * p.V;
-      if (!sampled) merge_topk(cp, p.n_chunks, kids, stok[warp], sval[warp]);
-      int j = 0;
-      for (int ch = n + 1; ch < p.R; ++ch) {
-        if (p.shape.parent[ch] != n) continue;
-        int tok;
-        if (!sampled) {
-          tok = stok[warp][j];
-        } else {
-          int nr = 0;
-          tok = warp_draw(a.logits, row, p.dtype, p.V, cp, p.n_chunks, rs.M, invT, rs.WT,
-                          a.u_draft[static_cast<size_t>(b) * p.R + ch], &nr);
-          near_local += nr;
-        }
-        if (lane == 0) {
-          ntok[ch] = tok;
-          nsc[ch] = ff_add(nsc[n], log_q(load_elem(a.logits, row + tok, p.dtype), rs));
-        }
-        ++j;
-      }
-      __syncwarp();
-    }
-    if (lane == 0 && near_local) atomicAdd(&s_near, near_local);
-    __syncthreads();
-    // next frontier: the nodes of depth `level` in index order, with their parent's
-    // row in this level's input (the parent's rank within its depth)
-    for (int i = threadIdx.x; i < p.R; i += kThreads) {
-      if (p.shape.depth[i] != a.level) continue;
-      const int slot = p.shape.lrank[i];
-      a.out.frontier_tok[static_cast<size_t>(b) * p.f_max + slot] = ntok[i];
-      a.out.frontier_slot[static_cast<size_t>(b) * p.f_max + slot] = p.shape.lrank[p.shape.parent[i]];
-    }
-    if (threadIdx.x == 0) state[1] += s_near;
-    __syncthreads();
-    if (a.level != p.depth) return;
-    const size_t ob = static_cast<size_t>(b) * p.R;
-    const int L = a.seq_len[b];
-    for (int i = threadIdx.x; i < p.R; i += kThreads) {
-      spar[i] = p.shape.parent[i];
-      a.out.tokens[ob + i] = (i == 0) ? a.root_tok[b] : ntok[i];
-      a.out.parent[ob + i] = p.shape.parent[i];
-      a.out.depth[ob + i] = p.shape.depth[i];
-      a.out.pos_id[ob + i] = L + p.shape.depth[i];
-      a.out.score[ob + i] = ff_float(nsc[i]);
-    }
-    __syncthreads();
+// Dynamic tree, frontier row f of request b: the row's statistics (warp 0) and top-k
+// (warp 1) from its chunk records, then its k candidates join the pool with
+// score s_parent + ln q(t).
+__device__ __forceinline__ void finish_row_dynamic(const TreeBuildPlan& p, const BuildArgs& a, int b, int f,
+                                                uint8_t* s_fin) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  __shared__ int stok[K];
+  __shared__ float sval[K];
+  ChunkPart* sp = reinterpret_cast<ChunkPart*>(s_fin);
+  const ReqView v = req_view(p, a.ws, b);
+  // the parent (written by the previous level), loaded while the records are staged
+  const int pidx = (a.level == 1) ? -1 : __ldcg(v.front + f);
+  const ff sp_score = (a.level == 1) ? ff_make(0.f) : ldcg_ff(v.fsc + f);
+  stage_parts(parts(p, a.ws) + (static_cast<size_t>(b) * p.f_max + f) * p.n_chunks, sp, p.n_chunks);
+  RowStats rs;
+  if (warp == 0) rs = row_stats(sp, p.n_chunks, 1.f);
+  if (warp == 1) merge_topk(sp, p.n_chunks, p.k, stok, sval);
+  __syncthreads();
+  if (warp == 0 && lane < p.k) {
+    const int i = pool_base(p, a.level) + f * p.k + lane;
+    v.ptok[i] = stok[lane];
+    v.ppar[i] = pidx;
+    v.psc[i] = ff_add(sp_score, log_q(sval[lane], rs));
+    v.pdep[i] = a.level;
   }
-  // ancestor masks: row i has bits i and those of its ancestors (each row walks up
-  // the parent chain; parents come first, so at most R steps)
+}
+
+// Static shape, frontier row f (the f-th node n of depth level - 1): the children of n
+// are its best tokens in rank order (top-k) or draws from softmax(row / T), one warp per
+// child; node scores are s_n + ln q(t) at T = 1.
+__device__ __forceinline__ void finish_row_static(const TreeBuildPlan& p, const BuildArgs& a, int b, int f,
+                                               uint8_t* s_fin) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const bool sampled = p.mode == EAGLE_TREE_STATIC_SAMPLED;
+  const float invT = 1.f / (p.temperature > 0.f ? p.temperature : 1.f);
+  __shared__ int stok[K];
+  __shared__ float sval[K];
+  __shared__ RowStats s_rs;
+  int n = -1;
+  for (int i = 0; i < p.R; ++i)
+    if (p.shape.depth[i] == a.level - 1 && p.shape.lrank[i] == f) {
+      n = i;
+      break;
+    }
+  int kids = 0;
+  for (int i = n + 1; n >= 0 && i < p.R; ++i) kids += (p.shape.parent[i] == n);
+  if (kids == 0) return;  // uniform over the CTA
+  ChunkPart* sp = reinterpret_cast<ChunkPart*>(s_fin);
+  stage_parts(parts(p, a.ws) + (static_cast<size_t>(b) * p.f_max + f) * p.n_chunks, sp, p.n_chunks);
+  const ReqView v = req_view(p, a.ws, b);
+  if (warp == 0) {
+    const RowStats rs = row_stats(sp, p.n_chunks, invT);
+    if (lane == 0) s_rs = rs;
+  }
+  if (warp == 1 && !sampled) merge_topk(sp, p.n_chunks, kids, stok, sval);
+  __syncthreads();
+  const RowStats rs = s_rs;
+  const size_t row = (static_cast<size_t>(b) * a.F + f) * p.V;
+  const ff s_par = (n == 0) ? ff_make(0.f) : ldcg_ff(v.nsc + n);
+  int near_local = 0, j = 0;
+  for (int ch = n + 1; ch < p.R; ++ch) {
+    if (p.shape.parent[ch] != n) continue;
+    if ((j++ % NW) != warp) continue;
+    int tok;
+    if (!sampled) {
+      tok = stok[j - 1];
+    } else {
+      int nr = 0;
+      tok = warp_draw(a.logits, row, p.dtype, p.V, sp, p.n_chunks, rs.M, invT, rs.WT,
+                      a.u_draft[static_cast<size_t>(b) * p.R + ch], &nr);
+      near_local += nr;
+    }
+    if (lane == 0) {
+      v.ntok[ch] = tok;
+      v.nsc[ch] = ff_add(s_par, log_q(load_elem(a.logits, row + tok, p.dtype), rs));
+    }
+  }
+  if (lane == 0 && near_local) atomicAdd(v.state + 1, near_local);
+}
+
+// Ancestor masks: row i has bits i and those of its ancestors (each row walks up the
+// parent chain; parents come first, so at most R steps).
+__device__ void write_masks(const TreeBuildPlan& p, const BuildArgs& a, int b, const int* spar) {
   const size_t mb = static_cast<size_t>(b) * p.R;
   for (int i = threadIdx.x; i < p.R; i += kThreads) {
     uint64_t w0 = 0, w1 = 0;
@@ -897,7 +828,249 @@ __global__ void __launch_bounds__(kThreads, 1) tree_select_kernel(const TreeBuil
     a.out.anc_mask[(mb + i) * p.W] = w0;
     if (p.W > 1) a.out.anc_mask[(mb + i) * p.W + 1] = w1;
   }
-  if (threadIdx.x == 0) a.out.near_tie[b] = state[1];
+}
+
+// The order of pool entries as one 64-bit key: (score desc) as the float-float pair's
+// order-preserving images, high part first (the pairs are normalised, so this is the
+// order of their values); ties go to the lower pool index.
+__device__ __forceinline__ uint64_t score_key(ff s) {
+  return (static_cast<uint64_t>(ord32(s.hi)) << 32) | ord32(s.lo);
+}
+
+__device__ __forceinline__ ff key_score(uint64_t key) {
+  return ff{unord32(static_cast<uint32_t>(key >> 32)), unord32(static_cast<uint32_t>(key))};
+}
+
+// Leading entries of a descending list (key, index) that come before (x, ix).
+__device__ __forceinline__ int count_before(const uint64_t* key, const int* idx, int n, uint64_t x, int ix) {
+  int lo = 0, hi = n;
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (key[mid] > x || (key[mid] == x && idx[mid] < ix))
+      lo = mid + 1;
+    else
+      hi = mid;
+  }
+  return lo;
+}
+
+// Dynamic tree, request b, after all its rows: the next frontier is the best k of the
+// level's F k candidates (kept in pool order).  The request also keeps, from level to
+// level, the best N + 1 entries of the pool so far as a sorted list (the level's
+// candidates, ranked, are merged into it), so that after the last level the best N of
+// the pool, in pool order, form the tree without sorting the whole pool.
+__device__ __forceinline__ void finish_request_dynamic(const TreeBuildPlan& p, const BuildArgs& a, int b,
+                                                       uint8_t* s_fin) {
+  // shared memory: the level's candidates, the incoming and outgoing best lists, flags
+  uint64_t* ck = reinterpret_cast<uint64_t*>(s_fin);      // [256] candidate keys, by candidate
+  uint64_t* bk = ck + kThreads;                            // [256] candidate keys, by rank
+  uint64_t* lk = bk + kThreads;                            // [128] best list in
+  uint64_t* nk = lk + kMaxRows;                            // [128] best list out
+  int* bi = reinterpret_cast<int*>(nk + kMaxRows);         // [256] pool index, by rank
+  int* li = bi + kThreads;                                 // [128]
+  int* ni = li + kMaxRows;                                 // [128]
+  int* srow = ni + kMaxRows;                               // [kMaxPool] flags / parents
+  __shared__ int s_cnt[NW];
+  __shared__ int s_bnd[2];
+  __shared__ int spar[kMaxRows];
+  const ReqView v = req_view(p, a.ws, b);
+  ff* best_sc = reinterpret_cast<ff*>(a.ws + p.off_best_score) + static_cast<size_t>(b) * kMaxRows;
+  int32_t* best_ix = reinterpret_cast<int32_t*>(a.ws + p.off_best_idx) + static_cast<size_t>(b) * kMaxRows;
+  const int base = pool_base(p, a.level);
+  const int k = p.k;
+  const int n_new = a.F * k;  // <= 256 = kThreads: one candidate per thread
+  const int M = p.N + 1;      // the best list: the N kept and the first dropped
+  const int nA = base < M ? base : M;
+  const int nL = (base + n_new) < M ? base + n_new : M;
+  const int j = threadIdx.x;
+  // every load of the level at once: the candidates (written by the row finishers) and
+  // the best list (written by the previous level)
+  ff kj = ff_make(-INFINITY);
+  int tj = 0, pj = 0;
+  if (j < n_new) {
+    kj = ldcg_ff(v.psc + base + j);
+    tj = __ldcg(v.ptok + base + j);
+    pj = __ldcg(v.ppar + base + j);
+  }
+  ff la = ff_make(-INFINITY);
+  int lix = 0;
+  if (j < nA) {
+    la = ldcg_ff(best_sc + j);
+    lix = __ldcg(best_ix + j);
+    lk[j] = score_key(la);
+    li[j] = lix;
+  }
+  const uint64_t kkey = score_key(kj);
+  if (j < n_new) {
+    ck[j] = kkey;
+    srow[j] = pj;
+  }
+  __syncthreads();
+  // a candidate's rank among the level's: the candidates before it by (score desc,
+  // pool index asc)
+  int r = n_new;
+  if (j < n_new) {
+    r = 0;
+    int i = 0;
+    for (; i + 4 <= n_new; i += 4) {
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const uint64_t ki = ck[i + u];
+        r += (ki > kkey || (ki == kkey && i + u < j)) ? 1 : 0;
+      }
+    }
+    for (; i < n_new; ++i) r += (ck[i] > kkey || (ck[i] == kkey && i < j)) ? 1 : 0;
+    bk[r] = kkey;
+    bi[r] = base + j;
+    if (r == k - 1 || r == k) s_bnd[r - (k - 1)] = j;  // the two candidates at the boundary
+  }
+  __syncthreads();
+  // a near-tie at the frontier boundary, unless it is an exact tie between siblings (same
+  // parent, same logit), which both sides break by pool index
+  if (threadIdx.x == 0 && n_new > k) {
+    const int ja = s_bnd[0], jb = s_bnd[1];
+    if (ff_float(ff_sub(key_score(ck[ja]), key_score(ck[jb]))) < kNearTieEps &&
+        !(ck[ja] == ck[jb] && srow[ja] == srow[jb]))
+      atomicAdd(v.state + 1, 1);
+  }
+  // the merged best list: an entry's position is its rank in its own list plus the
+  // entries of the other list before it
+  if (j < nA) {
+    const int pos = j + count_before(bk, bi, n_new, lk[j], lix);
+    if (pos < M) {
+      nk[pos] = lk[j];
+      ni[pos] = lix;
+      best_sc[pos] = la;
+      best_ix[pos] = lix;
+    }
+  }
+  if (j < n_new) {
+    const int pos = r + count_before(lk, li, nA, kkey, base + j);
+    if (pos < M) {
+      nk[pos] = kkey;
+      ni[pos] = base + j;
+      best_sc[pos] = kj;
+      best_ix[pos] = base + j;
+    }
+  }
+  __syncthreads();
+  if (j < n_new) srow[j] = r < k ? 1 : 0;
+  block_flag_ranks(srow, n_new, s_cnt);
+  if (j < n_new && srow[j] >= 0) {
+    const int slot = srow[j];
+    v.front[slot] = base + j;
+    v.fsc[slot] = kj;
+    a.out.frontier_tok[static_cast<size_t>(b) * p.f_max + slot] = tj;
+    a.out.frontier_slot[static_cast<size_t>(b) * p.f_max + slot] = j / k;
+  }
+  __syncthreads();
+  if (a.level != p.depth) return;
+
+  // ---- last level: the best N of the pool, rows in pool order
+  const int np = base + n_new;
+  const int N = p.N;
+  if (threadIdx.x == 0 && np > N) {  // the selection boundary: the N-th and the first dropped
+    const int ia = ni[N - 1], ib = ni[N];
+    if (ff_float(ff_sub(key_score(nk[N - 1]), key_score(nk[N]))) < kNearTieEps &&
+        !(nk[N - 1] == nk[N] && __ldcg(v.ppar + ia) == __ldcg(v.ppar + ib)))
+      atomicAdd(v.state + 1, 1);
+  }
+  for (int jj = threadIdx.x; jj < np; jj += kThreads) srow[jj] = 0;
+  __syncthreads();
+  for (int jj = threadIdx.x; jj < N && jj < nL; jj += kThreads) srow[ni[jj]] = 1;
+  __syncthreads();
+  block_flag_ranks(srow, np, s_cnt);  // row of a selected pool entry = its rank + 1
+  const size_t ob = static_cast<size_t>(b) * p.R;
+  const int L = a.seq_len[b];
+  for (int jj = threadIdx.x; jj < np; jj += kThreads) {
+    if (srow[jj] < 0) continue;
+    const int pp = __ldcg(v.ppar + jj), dep = __ldcg(v.pdep + jj), tok = __ldcg(v.ptok + jj);
+    const ff sc = ldcg_ff(v.psc + jj);
+    const int rr = srow[jj] + 1;
+    const int pr = (pp < 0) ? 0 : (srow[pp] >= 0 ? srow[pp] + 1 : 0);
+    spar[rr] = pr;
+    a.out.tokens[ob + rr] = tok;
+    a.out.parent[ob + rr] = pr;
+    a.out.depth[ob + rr] = dep;
+    a.out.pos_id[ob + rr] = L + dep;
+    a.out.score[ob + rr] = ff_float(sc);
+  }
+  if (threadIdx.x == 0) {
+    spar[0] = -1;
+    a.out.tokens[ob] = a.root_tok[b];
+    a.out.parent[ob] = -1;
+    a.out.depth[ob] = 0;
+    a.out.pos_id[ob] = L;
+    a.out.score[ob] = 0.f;
+  }
+  __syncthreads();
+  write_masks(p, a, b, spar);
+  __syncthreads();
+  if (threadIdx.x == 0) a.out.near_tie[b] = atomicAdd(v.state + 1, 0);
+}
+
+// Static shape, request b, after all its rows: the next frontier is the nodes of depth
+// `level` in index order; after the last level the tree arrays.
+__device__ __forceinline__ void finish_request_static(const TreeBuildPlan& p, const BuildArgs& a, int b) {
+  __shared__ int spar[kMaxRows];
+  const ReqView v = req_view(p, a.ws, b);
+  for (int i = threadIdx.x; i < p.R; i += kThreads) {
+    if (p.shape.depth[i] != a.level) continue;
+    const int slot = p.shape.lrank[i];
+    a.out.frontier_tok[static_cast<size_t>(b) * p.f_max + slot] = __ldcg(v.ntok + i);
+    a.out.frontier_slot[static_cast<size_t>(b) * p.f_max + slot] = p.shape.lrank[p.shape.parent[i]];
+  }
+  if (a.level != p.depth) return;
+  const size_t ob = static_cast<size_t>(b) * p.R;
+  const int L = a.seq_len[b];
+  for (int i = threadIdx.x; i < p.R; i += kThreads) {
+    spar[i] = p.shape.parent[i];
+    a.out.tokens[ob + i] = (i == 0) ? a.root_tok[b] : __ldcg(v.ntok + i);
+    a.out.parent[ob + i] = p.shape.parent[i];
+    a.out.depth[ob + i] = p.shape.depth[i];
+    a.out.pos_id[ob + i] = L + p.shape.depth[i];
+    a.out.score[ob + i] = (i == 0) ? 0.f : ff_float(ldcg_ff(v.nsc + i));
+  }
+  __syncthreads();
+  write_masks(p, a, b, spar);
+  if (threadIdx.x == 0) a.out.near_tie[b] = atomicAdd(v.state + 1, 0);
+}
+
+// ------------------------------------------------------------------ one draft level
+// One CTA per (request x frontier row, 4096-token chunk): the chunk pass, then the
+// tickets: the row's last chunk CTA merges the row, the request's last row selects.
+template <bool TOPK, bool BF16>
+__global__ void __launch_bounds__(kThreads, 2)
+    tree_level_kernel(const TreeBuildPlan p, const BuildArgs a) {
+  __shared__ __align__(16) uint8_t s_fin[kFinBytes];
+  __shared__ int s_ticket;
+  chunk_pass<TOPK, BF16>(p, a);
+  const int b = blockIdx.x / a.F, f = blockIdx.x % a.F;
+  int* row_ticket = reinterpret_cast<int*>(a.ws + p.off_ticket) + b * p.f_max + f;
+  int* req_ticket = reinterpret_cast<int*>(a.ws + p.off_ticket) + p.B * p.f_max + b;
+  // the ticket: the barrier orders the CTA's record writes before thread 0's atomic,
+  // whose release makes them visible with it at device scope and whose acquire orders
+  // the last CTA's reads of the other CTAs' records after it
+  __syncthreads();
+  if (threadIdx.x == 0) s_ticket = atom_add_acq_rel(row_ticket, 1);
+  __syncthreads();
+  if (s_ticket != p.n_chunks - 1) return;
+  if (p.mode == EAGLE_TREE_DYNAMIC)
+    finish_row_dynamic(p, a, b, f, s_fin);
+  else
+    finish_row_static(p, a, b, f, s_fin);
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    *row_ticket = 0;  // ready for the next level
+    s_ticket = atom_add_acq_rel(req_ticket, 1);
+  }
+  __syncthreads();
+  if (s_ticket != a.F - 1) return;
+  if (p.mode == EAGLE_TREE_DYNAMIC)
+    finish_request_dynamic(p, a, b, s_fin);
+  else
+    finish_request_static(p, a, b);
+  if (threadIdx.x == 0) *req_ticket = 0;
 }
 
 }  // namespace
@@ -962,10 +1135,18 @@ void plan_tree_build(const eagle_tree_desc* d, TreeBuildPlan* p) {
   off = align256(off + cap * sizeof(ff));
   p->off_pool_depth = off;
   off = align256(off + cap * 4);
-  p->off_state = off;
-  off = align256(off + static_cast<size_t>(p->B) * 4 * 4);
+  p->off_state = off;  // state [B][4], then the row tickets [B][f_max] and request tickets [B]
+  off += static_cast<size_t>(p->B) * 4 * 4;
+  p->off_ticket = off;
+  off = align256(off + static_cast<size_t>(p->B) * (p->f_max + 1) * 4);
   p->off_front = off;
   off = align256(off + static_cast<size_t>(p->B) * K * 4);
+  p->off_front_score = off;
+  off = align256(off + static_cast<size_t>(p->B) * K * sizeof(ff));
+  p->off_best_score = off;  // the best N + 1 of the pool so far, per request
+  off = align256(off + static_cast<size_t>(p->B) * kMaxRows * sizeof(ff));
+  p->off_best_idx = off;
+  off = align256(off + static_cast<size_t>(p->B) * kMaxRows * 4);
   p->off_part = off;
   off = align256(off + static_cast<size_t>(p->B) * p->f_max * p->n_chunks * sizeof(ChunkPart));
   p->off_node_tok = off;
@@ -995,22 +1176,24 @@ cudaError_t launch_tree_build(const TreeBuildPlan& p, int level, const void* log
   a.out = out;
   a.level = level;
   a.F = frontier_rows(p, level);
+  if (level == 1) {  // a new build: zero the per-request state and the tickets
+    const cudaError_t e = cudaMemsetAsync(a.ws + p.off_state, 0,
+                                          p.off_ticket - p.off_state + static_cast<size_t>(p.B) * (p.f_max + 1) * 4, s);
+    if (e != cudaSuccess) return e;
+  }
   dim3 grid(p.B * a.F, p.n_chunks);
   const bool bf16 = p.dtype != EAGLE_F32;
   if (p.mode == EAGLE_TREE_STATIC_SAMPLED) {
     if (bf16)
-      tree_chunk_kernel<false, true><<<grid, kThreads, 0, s>>>(p, a);
+      tree_level_kernel<false, true><<<grid, kThreads, 0, s>>>(p, a);
     else
-      tree_chunk_kernel<false, false><<<grid, kThreads, 0, s>>>(p, a);
+      tree_level_kernel<false, false><<<grid, kThreads, 0, s>>>(p, a);
   } else {
     if (bf16)
-      tree_chunk_kernel<true, true><<<grid, kThreads, 0, s>>>(p, a);
+      tree_level_kernel<true, true><<<grid, kThreads, 0, s>>>(p, a);
     else
-      tree_chunk_kernel<true, false><<<grid, kThreads, 0, s>>>(p, a);
+      tree_level_kernel<true, false><<<grid, kThreads, 0, s>>>(p, a);
   }
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  tree_select_kernel<<<p.B, kThreads, 0, s>>>(p, a);
   return cudaGetLastError();
 }
 

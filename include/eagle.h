@@ -124,7 +124,7 @@ enum { EAGLE_WS_TREE_BUILD = 1, EAGLE_WS_TREE_ATTN = 2, EAGLE_WS_ACCEPT = 3, EAG
 /* ---------------------------------------------------------------- tree build */
 typedef struct {
   int32_t batch;              /* B >= 1 */
-  int32_t vocab;              /* V >= 1 */
+  int32_t vocab;              /* 1 <= V <= 524288 (128 chunks of 4096 tokens) */
   int32_t mode;               /* EAGLE_TREE_* */
   int32_t depth;              /* draft levels D, 1..16 (dynamic), or the static shape's depth */
   int32_t top_k;              /* dynamic: children per frontier node and frontier width, 1..16 */
@@ -168,10 +168,14 @@ int eagle_tree_max_frontier(const eagle_tree_desc* d);
  *                    the last level).
  *   ws               scratch of eagle_workspace_size(EAGLE_WS_TREE_BUILD, d) bytes.
  *                    It carries the candidate pool from level to level: pass the
- *                    same ws, untouched, to levels 1..depth of one build.
+ *                    same ws, untouched, to levels 1..depth of one build.  Level 1
+ *                    clears its counters (one memset on the stream), so it need not be
+ *                    zero-filled.
  * After each level frontier_tok / frontier_slot name the next level's rows.  The
  * last level writes the tree.  Ties inside a row go to the lower token id;
- * scores are compared in fp32 with the pool index breaking ties. */
+ * cumulative scores are float-float (about 48 bits) with the pool index breaking
+ * ties.  One kernel launch per level (after level 1's memset): the last CTA to
+ * finish a frontier row merges that row, and the last row of a request selects. */
 int eagle_tree_build(const eagle_tree_desc* d, int level, const void* frontier_logits,
                      const float* u_draft, const int32_t* root_tok, const int32_t* seq_len,
                      void* ws, size_t ws_bytes, const eagle_tree* out, void* stream);

@@ -129,6 +129,8 @@ def test_tree_build_validation(lib):
     assert _call_build(lib, dyn(total_tokens=128)) == B.EAGLE_ERR_UNSUPPORTED
     assert _call_build(lib, dyn(depth=2, top_k=3, total_tokens=13)) == B.EAGLE_ERR_INVALID_ARG  # pool is 12
     assert _call_build(lib, dyn(top_k=16, depth=10)) == B.EAGLE_ERR_UNSUPPORTED  # pool > 2048
+    assert B.workspace_size(B.EAGLE_WS_TREE_BUILD, dyn(vocab=128 * 4096)) > 0  # largest vocabulary
+    assert _call_build(lib, dyn(vocab=128 * 4096 + 1)) == B.EAGLE_ERR_UNSUPPORTED
     need = B.workspace_size(B.EAGLE_WS_TREE_BUILD, dyn())
     assert need > 0
     assert _call_build(lib, dyn(), ws_bytes=need - 1) == B.EAGLE_ERR_WORKSPACE
