@@ -22,8 +22,9 @@
 //                 chunk records (M, ln Z, top-k or draws) and adds its candidates to the
 //                 pool (dynamic) or its children to the shape (static).
 //   request       the last row finisher of a request (a second ticket): picks the
-//                 next frontier (rank counting) and, at the last level, the best N of
-//                 the pool (bitonic sort in shared memory) and the tree arrays.
+//                 next frontier (rank counting), merges the level's ranked candidates
+//                 into the request's sorted list of the best N + 1 so far, and after the
+//                 last level writes the tree from that list's first N.
 // No CTA waits for another; the tickets return to zero for the next level, and level 1
 // clears them with a memset first.
 //
