@@ -382,6 +382,7 @@ def run_ours(args):
                 "us_per_launch": round(attn_ms * 1e3, 2)}
     tree_build = time_tree_build(st, stream, max(20, args.steps // 2))
     lmhead = time_lmhead(st, stream, max(10, args.steps // 4), peak)
+    tree_head = time_tree_head(st, stream, max(5, args.steps // 8), peak)
     ttt = time_ttt(stream, 5) if args.config in ("llama8b", "vicuna7b") else {"skipped": "run with the 8B workloads"}
     step_bytes = kv_total + float(np.mean([st.logit_bytes_visited(a) for a in n_acc_all]))
     step_frac = step_bytes / (ms_per_step / 1e3) / 1e9 / peak
@@ -397,8 +398,8 @@ def run_ours(args):
                        "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU"},
             "step_roofline_frac": round(step_frac, 4), "step_algorithmic_bytes": int(step_bytes),
             "mean_accept_length": round(float(np.mean(n_acc_all + 1)), 4), "step_variants": int(n_var),
-            "roofline": roofline, "tree_build": tree_build, "lmhead_stats": lmhead, "ttt_attention": ttt,
-            "e2e": e2e,
+            "roofline": roofline, "tree_build": tree_build, "tree_build_head": tree_head, "lmhead_stats": lmhead,
+            "ttt_attention": ttt, "e2e": e2e,
             "gpu_launches": int(launches_per_step * args.steps), "clocks": clocks,
             "setup_s": round(t_setup, 1)}
     if need_host:
@@ -484,6 +485,59 @@ def time_lmhead(st, stream, reps: int, peak: float):
     out = {"us_per_call": round(us, 2), "rows": M, "hidden": h, "vocab": V, "algorithmic_bytes": int(byt),
            "gbs": round(byt / us / 1e3, 1), "frac": round(byt / us / 1e3 / peak, 4), "status": int(status.item()),
            "note": "timed apart from the verify step (not in value): head bytes read once per call"}
+    del head
+    torch.cuda.empty_cache()
+    return out
+
+
+def time_tree_head(st, stream, reps: int, peak: float):
+    """The draft-tree build from the draft's hidden states (eagle_tree_build_head: the
+    draft LM head fused with tree expansion), timed apart from the verify step: every
+    level's frontier hidden states (4096 wide, N(0, 1)) against a random bf16 head of the
+    workload's vocabulary (N(0, 1/4096)), all levels replayed from a CUDA graph.  Each
+    level reads the head once, so the roofline is the levels' head bytes over the time."""
+    import torch
+    from eagle_speculative_decoding_tree_gb300 import binding as B, synth
+    from eagle_speculative_decoding_tree_gb300.step import GpuTreeBuilder
+    w = st.w
+    h, V = 4096, w.vocab
+    if w.tree_mode == "static_sampled" or w.dtype != "bf16":
+        return {"skipped": "sampled trees draw from the logits; bf16 workloads only"}
+    bld = GpuTreeBuilder(w, st.B)
+    if st.B * bld.desc.top_k > 128:
+        return {"skipped": "more than 128 frontier rows"}
+    g = np.random.default_rng(0xEA61E000 + w.config_id)
+    head = (torch.randn(V, h, device="cuda", generator=torch.Generator(device="cuda").manual_seed(w.config_id))
+            / 64.0).to(torch.bfloat16)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    bld.set_context(np.zeros(st.B, np.int32), np.asarray(st.seq_len0, np.int32))
+    F, rows = 1, 0
+    for level in range(1, bld.depth + 1):
+        hid = synth.bf16_bits(g.normal(0, 1, (st.B, F, h)).astype(np.float32))
+        tok, _ = bld.expand_head(level, hid, head, status)
+        rows += st.B * F
+        F = tok.shape[1]
+    gr = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        bld.replay_head(head, status, stream)
+        stream.synchronize()
+        with torch.cuda.graph(gr, stream=stream):
+            bld.replay_head(head, status, stream)
+        for _ in range(3):
+            gr.replay()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(reps):
+            gr.replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    us = e0.elapsed_time(e1) * 1e3 / reps
+    levels = bld.depth
+    byt = levels * V * h * 2 + rows * h * 2
+    out = {"us_per_tree": round(us, 2), "levels": levels, "launches_per_tree": 2 * levels, "hidden": h, "vocab": V,
+           "algorithmic_bytes": int(byt), "gbs": round(byt / us / 1e3, 1), "frac": round(byt / us / 1e3 / peak, 4),
+           "status": int(status.item()),
+           "note": "timed apart from the verify step (not in value): the draft head read once per level"}
     del head
     torch.cuda.empty_cache()
     return out

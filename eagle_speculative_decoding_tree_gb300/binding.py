@@ -32,7 +32,7 @@ EXPORTED_SYMBOLS = ("eagle_tree_build", "eagle_tree_attn", "eagle_accept", "eagl
                     "eagle_workspace_size", "eagle_status_string", "eagle_version",
                     "eagle_tree_frontier_rows", "eagle_tree_max_frontier", "eagle_last_cuda_error",
                     "eagle_last_cuda_error_string", "eagle_tree_attn_plan", "eagle_accept_noalloc",
-                    "eagle_selftest_ff_log", "eagle_lmhead_stats", "eagle_ttt_attn")
+                    "eagle_selftest_ff_log", "eagle_lmhead_stats", "eagle_ttt_attn", "eagle_tree_build_head")
 
 
 class TreeDesc(ctypes.Structure):
@@ -113,6 +113,8 @@ def load() -> ctypes.CDLL:
         L.eagle_selftest_ff_log.argtypes = [vp, vp, vp, vp, i32, vp]
         L.eagle_lmhead_stats.argtypes = [ctypes.POINTER(LmHeadDesc), vp, vp, vp, vp, vp, vp, vp, vp]
         L.eagle_ttt_attn.argtypes = [ctypes.POINTER(TttDesc), vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+        L.eagle_tree_build_head.argtypes = [ctypes.POINTER(TreeDesc), i32, vp, vp, i32, vp, vp, vp, sz,
+                                            ctypes.POINTER(TreeOut), vp, vp]
         L.eagle_workspace_size.argtypes = [i32, vp]
         L.eagle_workspace_size.restype = sz
         L.eagle_status_string.argtypes = [i32]
@@ -124,7 +126,7 @@ def load() -> ctypes.CDLL:
         L.eagle_tree_max_frontier.argtypes = [ctypes.POINTER(TreeDesc)]
         L.eagle_tree_attn_plan.argtypes = [ctypes.POINTER(AttnDesc), ctypes.POINTER(ctypes.c_int32),
                                            ctypes.POINTER(ctypes.c_int32)]
-        for f in (L.eagle_tree_build, L.eagle_tree_attn, L.eagle_accept, L.eagle_kv_commit,
+        for f in (L.eagle_tree_build, L.eagle_tree_build_head, L.eagle_tree_attn, L.eagle_accept, L.eagle_kv_commit,
                   L.eagle_tree_frontier_rows, L.eagle_tree_max_frontier, L.eagle_tree_attn_plan,
                   L.eagle_accept_noalloc):
             f.restype = ctypes.c_int
@@ -267,6 +269,19 @@ def eagle_tree_build(desc: TreeDesc, level: int, frontier_logits: torch.Tensor, 
         _ptr(u_draft, torch.float32, "u_draft"), _ptr(root_tok, torch.int32, "root_tok"),
         _ptr(seq_len, torch.int32, "seq_len"), _ptr(ws, name="ws"), ws.numel() * ws.element_size(),
         ctypes.byref(o), _stream(stream)))
+
+
+def eagle_tree_build_head(desc: TreeDesc, level: int, hidden: torch.Tensor, head_weight: torch.Tensor,
+                          root_tok: torch.Tensor, seq_len: torch.Tensor, ws: torch.Tensor, out: TreeBuffers,
+                          status: torch.Tensor, stream=None) -> None:
+    """One draft level from the frontier rows' hidden states [B][F][h] and the LM head
+    [V][h], both bf16 (see eagle.h: eagle_tree_build_head)."""
+    o = out.c_struct()
+    _check("eagle_tree_build_head", load().eagle_tree_build_head(
+        ctypes.byref(desc), level, _ptr(hidden, torch.bfloat16, "hidden"),
+        _ptr(head_weight, torch.bfloat16, "head_weight"), int(hidden.shape[-1]), _ptr(root_tok, torch.int32, "root_tok"),
+        _ptr(seq_len, torch.int32, "seq_len"), _ptr(ws, name="ws"), ws.numel() * ws.element_size(), ctypes.byref(o),
+        _ptr(status, torch.int32, "status"), _stream(stream)))
 
 
 def eagle_tree_attn(desc: AttnDesc, q, k_cache, v_cache, tree_k, tree_v, seq_len, anc_mask, out,

@@ -208,6 +208,29 @@ int eagle_tree_build(const eagle_tree_desc* d, int level, const void* frontier_l
                            static_cast<cudaStream_t>(stream)));
 }
 
+int eagle_tree_build_head(const eagle_tree_desc* d, int level, const void* hidden, const void* head_weight,
+                          int32_t hidden_dim, const int32_t* root_tok, const int32_t* seq_len, void* ws,
+                          size_t ws_bytes, const eagle_tree* out, uint32_t* status, void* stream) {
+  int rc = check_tree_desc(d);
+  if (rc != EAGLE_OK) return rc;
+  if (d->mode == EAGLE_TREE_STATIC_SAMPLED) return EAGLE_ERR_UNSUPPORTED;  // draws read the logits
+  TreeBuildPlan p;
+  plan_tree_build(d, &p);
+  if (level < 1 || level > p.depth) return EAGLE_ERR_INVALID_ARG;
+  if (hidden_dim < 64 || hidden_dim % 64 != 0) return hidden_dim < 1 ? EAGLE_ERR_INVALID_ARG : EAGLE_ERR_UNSUPPORTED;
+  if (static_cast<long long>(d->batch) * p.f_max > 128) return EAGLE_ERR_UNSUPPORTED;  // one M-tile of rows
+  if (!hidden || !head_weight || !root_tok || !seq_len || !out || !status) return EAGLE_ERR_INVALID_ARG;
+  if (!out->tokens || !out->parent || !out->depth || !out->pos_id || !out->anc_mask || !out->score ||
+      !out->frontier_tok || !out->frontier_slot || !out->near_tie)
+    return EAGLE_ERR_INVALID_ARG;
+  if (!aligned(hidden, 16) || !aligned(head_weight, 16) || !aligned(ws, 16) || !aligned(out->anc_mask, 8) ||
+      !aligned(status, 4))
+    return EAGLE_ERR_ALIGNMENT;
+  if (!ws || ws_bytes < p.total) return EAGLE_ERR_WORKSPACE;
+  return cuda_status(launch_tree_build_head(p, level, hidden, head_weight, hidden_dim, root_tok, seq_len, ws, *out,
+                                            status, static_cast<cudaStream_t>(stream)));
+}
+
 int eagle_tree_attn(const eagle_attn_desc* d, const void* q, const void* k_cache, const void* v_cache,
                     const void* tree_k, const void* tree_v, const int32_t* seq_len, const int32_t* n_nodes,
                     const uint64_t* anc_mask, void* out, float* lse, void* ws, size_t ws_bytes, void* stream) {

@@ -32,6 +32,12 @@ struct TreeBuildPlan {
 };
 void plan_tree_build(const eagle_tree_desc* d, TreeBuildPlan* p);
 int frontier_rows(const TreeBuildPlan& p, int level);
+// One tree level from the draft model's hidden states of the frontier rows and its LM
+// head (dynamic and static top-k trees): the head kernel writes the rows' records, the
+// finishers select as from logits.
+cudaError_t launch_tree_build_head(const TreeBuildPlan& plan, int level, const void* hidden, const void* weight,
+                                   int hidden_dim, const int32_t* root_tok, const int32_t* seq_len, void* ws,
+                                   const eagle_tree& out, uint32_t* status, cudaStream_t s);
 cudaError_t launch_tree_build(const TreeBuildPlan& p, int level, const void* logits, const float* u_draft,
                               const int32_t* root_tok, const int32_t* seq_len, void* ws, const eagle_tree& out,
                               cudaStream_t s);
@@ -95,6 +101,28 @@ cudaError_t launch_accept(const AcceptPlan& p, const void* target, const void* d
 
 // ------------------------------------------------------------------ LM-head statistics
 int lmhead_tiles(int vocab);
+
+// A tree-build vocabulary record of one frontier row: the best 16 (value desc, id asc)
+// of the tokens it covers, sum exp(x - m) and sum exp((x - m) / T) as float-float pairs,
+// and the max m.  Written by the tree build's chunk pass (one 4096-token chunk) or by the
+// LM-head kernel (the tiles one persistent CTA covered).
+struct TreeChunkRecord {
+  float tv[16];
+  int ti[16];
+  float s1_hi, s1_lo, sT_hi, sT_lo;
+  float m;
+  float pad[3];
+};
+static_assert(sizeof(TreeChunkRecord) == 160, "tree chunk records are 160 bytes");
+
+// Records per frontier row when the tree build reads the draft LM head (one per
+// persistent CTA of the head kernel).
+constexpr int kHeadRecords = 144;
+
+// Draft LM head for a tree level: for hidden rows r = b F + f (M = B F <= 128), the
+// record of row r for CTA c goes to trec[(b f_max + f) n_rec + c], c < n_rec.
+cudaError_t launch_lmhead_tree_records(int M, int h, int V, int F, int f_max, int n_rec, const void* hidden,
+                                       const void* weight, TreeChunkRecord* trec, uint32_t* status, cudaStream_t s);
 cudaError_t launch_lmhead_stats(int M, int h, int V, int R, float temperature, const void* hidden, const void* weight,
                                 const int32_t* tokens, const int32_t* parent, eagle_vocab_record* rec, float* child,
                                 uint32_t* status, int num_sms, cudaStream_t s);

@@ -52,7 +52,10 @@ struct LmArgs {
   float* child;           // [M] nullable
   uint32_t* status;
   int M, h, V, R, n_tiles;
+  int h_bytes;  // bytes of one H slice: its box has M rows rounded up to 8
   float invT;
+  TreeChunkRecord* trec;  // tree-build records (nullable): one per (row, CTA)
+  int F, f_max;
 };
 
 struct LmMaps {
@@ -66,6 +69,7 @@ __device__ __forceinline__ bool lm_wait(uint64_t* bar, uint32_t parity, uint32_t
   return false;
 }
 
+template <bool TREC>
 __global__ void __launch_bounds__(NTHREADS, 1) lmhead_stats_kernel(const __grid_constant__ LmMaps tm,
                                                                   const LmArgs a) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -119,7 +123,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) lmhead_stats_kernel(const __grid_
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(&full[s], STAGE);
+          mbar_arrive_expect_tx(&full[s], a.h_bytes + SLICE);
           tma_load_2d(smem + s * STAGE, &tm.H, k * KS, 0, &full[s]);
           tma_load_2d_hint(smem + s * STAGE + SLICE, &tm.W, k * KS, t * NT, &full[s], once);
         }
@@ -157,6 +161,101 @@ __global__ void __launch_bounds__(NTHREADS, 1) lmhead_stats_kernel(const __grid_
         }
         if (ok) mma_commit(&d_full[buf]);
       }
+    }
+  } else if constexpr (TREC) {
+    // ------------------------------------------------------------ epilogue, tree records
+    // this row's running max, float-float sum exp(x - max) and best 16 (value desc, id
+    // asc) over the CTA's tiles, 32 columns at a time; tiles and columns come in
+    // increasing vocabulary order, so an equal value never displaces a lower id
+    const int r = warp * 32 + lane;  // hidden row = TMEM lane
+    const uint32_t lb = tb + (static_cast<uint32_t>(warp * 32) << 16);
+    float run_m = -INFINITY;
+    ff run_s = ff_make(0.f);
+    float tv[16];
+    int ti[16];
+#pragma unroll
+    for (int q = 0; q < 16; ++q) {
+      tv[q] = -INFINITY;
+      ti[q] = INT_MAX;
+    }
+    for (int j = 0; j < n_my; ++j) {
+      const int t = blockIdx.x + j * gridDim.x;
+      const int buf = j & 1;
+      const bool got = __all_sync(0xffffffffu, lm_wait(&d_full[buf], (j >> 1) & 1, a.status));
+      if (!got) break;
+      tc_fence_after();
+      // the whole accumulator first, so that the MMA may reuse it while this tile is
+      // folded in
+      float x[NT];
+#pragma unroll
+      for (int c = 0; c < NT / 32; ++c) {
+        uint32_t v[32];
+        tmem_ld32(lb + buf * NT + 32 * c, v);
+        tmem_ld_wait();
+#pragma unroll
+        for (int e = 0; e < 32; ++e) x[32 * c + e] = __uint_as_float(v[e]);
+      }
+      tc_fence_before();
+      mbar_arrive(&d_empty[buf]);
+      if (r >= a.M) continue;
+      const int base = t * NT;
+      const int nv = min(NT, a.V - base);
+#pragma unroll
+      for (int c = 0; c < NT / 32; ++c) {
+        const int lim = nv - 32 * c;  // valid columns of this slice
+        float cm = -INFINITY;
+#pragma unroll
+        for (int e = 0; e < 32; ++e)
+          if (e < lim) cm = fmaxf(cm, x[32 * c + e]);
+        if (cm == -INFINITY) continue;
+        if (cm > run_m) {
+          run_s = (run_m == -INFINITY) ? ff_make(0.f) : ff_mul(run_s, expf(run_m - cm));
+          run_m = cm;
+        }
+        CSum acc;
+        uint32_t cand = 0u;
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          if (e < lim) {
+            acc.add(expf(x[32 * c + e] - run_m));
+            cand |= (x[32 * c + e] > tv[15]) ? (1u << e) : 0u;
+          }
+        }
+        run_s = ff_add(run_s, csum_ff(acc));
+        while (cand) {  // rare after the first tiles: insert into the sorted list
+          const int e = __ffs(cand) - 1;
+          cand &= cand - 1u;
+          float val = 0.f;
+#pragma unroll
+          for (int q = 0; q < 32; ++q) val = (q == e) ? x[32 * c + q] : val;
+          if (!(val > tv[15])) continue;  // the list has moved on since the mask
+          const int id = base + 32 * c + e;
+#pragma unroll
+          for (int q = 15; q > 0; --q) {
+            const bool sh = val > tv[q - 1];
+            const bool at = !sh && val > tv[q];
+            tv[q] = sh ? tv[q - 1] : (at ? val : tv[q]);
+            ti[q] = sh ? ti[q - 1] : (at ? id : ti[q]);
+          }
+          if (val > tv[0]) {
+            tv[0] = val;
+            ti[0] = id;
+          }
+        }
+      }
+    }
+    if (r < a.M) {
+      const int b = r / a.F, f = r % a.F;
+      TreeChunkRecord* o = a.trec + (static_cast<size_t>(b) * a.f_max + f) * gridDim.x + blockIdx.x;
+      float4* ov = reinterpret_cast<float4*>(o->tv);
+      int4* oi = reinterpret_cast<int4*>(o->ti);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        ov[q] = make_float4(tv[4 * q], tv[4 * q + 1], tv[4 * q + 2], tv[4 * q + 3]);
+        oi[q] = make_int4(ti[4 * q], ti[4 * q + 1], ti[4 * q + 2], ti[4 * q + 3]);
+      }
+      *reinterpret_cast<float4*>(&o->s1_hi) = make_float4(run_s.hi, run_s.lo, run_s.hi, run_s.lo);
+      o->m = run_m;
     }
   } else {
     // ------------------------------------------------------------ epilogue, warps 0-3
@@ -241,12 +340,14 @@ PFN_cuTensorMapEncodeTiled_v12000 lm_encode_fn() {
   return fn;
 }
 
-bool lm_tmap(CUtensorMap* m, const void* base, int rows, int h) {
+// box_rows: the H slices cover only the M rows (rounded up to 8): a box that is mostly
+// out of bounds slowed the loads; the accumulator rows past them are never read.
+bool lm_tmap(CUtensorMap* m, const void* base, int rows, int h, int box_rows = 128) {
   auto fn = lm_encode_fn();
   if (!fn) return false;
   const cuuint64_t dims[2] = {static_cast<cuuint64_t>(h), static_cast<cuuint64_t>(rows)};
   const cuuint64_t strides[1] = {static_cast<cuuint64_t>(h) * 2};
-  const cuuint32_t box[2] = {KS, 128};
+  const cuuint32_t box[2] = {KS, static_cast<cuuint32_t>(box_rows)};
   const cuuint32_t es[2] = {1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -261,7 +362,8 @@ cudaError_t launch_lmhead_stats(int M, int h, int V, int R, float temperature, c
                                 const int32_t* tokens, const int32_t* parent, eagle_vocab_record* rec, float* child,
                                 uint32_t* status, int num_sms, cudaStream_t s) {
   LmMaps tm;
-  if (!lm_tmap(&tm.H, hidden, M, h) || !lm_tmap(&tm.W, weight, V, h)) return cudaErrorInvalidValue;
+  const int hrows = (M + 7) / 8 * 8;
+  if (!lm_tmap(&tm.H, hidden, M, h, hrows) || !lm_tmap(&tm.W, weight, V, h)) return cudaErrorInvalidValue;
   LmArgs a;
   a.tokens = tokens;
   a.parent = parent;
@@ -273,18 +375,56 @@ cudaError_t launch_lmhead_stats(int M, int h, int V, int R, float temperature, c
   a.V = V;
   a.R = R;
   a.n_tiles = lmhead_tiles(V);
+  a.h_bytes = hrows * KS * 2;
   a.invT = 1.f / (temperature > 0.f ? temperature : 1.f);
+  a.trec = nullptr;
+  a.F = 1;
+  a.f_max = 1;
   static unsigned long long configured = 0;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev >= 64 || !(__atomic_load_n(&configured, __ATOMIC_ACQUIRE) & (1ull << dev))) {
-    e = cudaFuncSetAttribute(lmhead_stats_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    e = cudaFuncSetAttribute(lmhead_stats_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
     if (e != cudaSuccess) return e;
     if (dev < 64) __atomic_fetch_or(&configured, 1ull << dev, __ATOMIC_RELEASE);
   }
   const int grid = a.n_tiles < num_sms ? a.n_tiles : num_sms;
-  lmhead_stats_kernel<<<grid, NTHREADS, SMEM_BYTES, s>>>(tm, a);
+  lmhead_stats_kernel<false><<<grid, NTHREADS, SMEM_BYTES, s>>>(tm, a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_lmhead_tree_records(int M, int h, int V, int F, int f_max, int n_rec, const void* hidden,
+                                       const void* weight, TreeChunkRecord* trec, uint32_t* status, cudaStream_t s) {
+  LmMaps tm;
+  const int hrows = (M + 7) / 8 * 8;
+  if (!lm_tmap(&tm.H, hidden, M, h, hrows) || !lm_tmap(&tm.W, weight, V, h)) return cudaErrorInvalidValue;
+  LmArgs a;
+  a.tokens = nullptr;
+  a.parent = nullptr;
+  a.rec = nullptr;
+  a.child = nullptr;
+  a.status = status;
+  a.M = M;
+  a.h = h;
+  a.V = V;
+  a.R = 0;
+  a.n_tiles = lmhead_tiles(V);
+  a.h_bytes = hrows * KS * 2;
+  a.invT = 1.f;  // the tree ranks at T = 1
+  a.trec = trec;
+  a.F = F;
+  a.f_max = f_max;
+  static unsigned long long configured = 0;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev >= 64 || !(__atomic_load_n(&configured, __ATOMIC_ACQUIRE) & (1ull << dev))) {
+    e = cudaFuncSetAttribute(lmhead_stats_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    if (dev < 64) __atomic_fetch_or(&configured, 1ull << dev, __ATOMIC_RELEASE);
+  }
+  lmhead_stats_kernel<true><<<n_rec, NTHREADS, SMEM_BYTES, s>>>(tm, a);
   return cudaGetLastError();
 }
 

@@ -34,6 +34,7 @@
 // agree with an fp64 computation unless two scores at a boundary are within 1e-5
 // (reported as a near-tie).
 #include <limits.h>
+#include <stddef.h>
 
 #include "common.cuh"
 #include "launch.h"
@@ -58,6 +59,10 @@ struct __align__(16) ChunkPart {
   float pad[3];
 };
 static_assert(sizeof(ChunkPart) % 16 == 0, "chunk lists are read as 16-byte vectors");
+static_assert(sizeof(ChunkPart) == sizeof(TreeChunkRecord) && offsetof(ChunkPart, s1) == offsetof(TreeChunkRecord, s1_hi) &&
+                  offsetof(ChunkPart, sT) == offsetof(TreeChunkRecord, sT_hi) && offsetof(ChunkPart, m) == offsetof(TreeChunkRecord, m),
+              "the LM-head kernel writes chunk records in this layout");
+static_assert(kHeadRecords <= 160, "a warp merges at most 160 chunk lists");
 
 struct BuildArgs {
   const void* logits;
@@ -507,12 +512,12 @@ __device__ void merge_topk(const ChunkPart* cp, int n_chunks, int cnt, int* tok,
     __syncwarp();
     return;
   }
-  int head[4] = {0, 0, 0, 0};  // per owned chunk (lane, lane+32, ...)
+  int head[5] = {0, 0, 0, 0, 0};  // per owned chunk (lane, lane+32, ...): up to 160 chunks
   for (int r = 0; r < cnt; ++r) {
     float bv = -INFINITY;
     int bi = INT_MAX, bslot = -1;
 #pragma unroll
-    for (int s = 0; s < 4; ++s) {
+    for (int s = 0; s < 5; ++s) {
       const int c = lane + 32 * s;
       if (c < n_chunks && head[s] < K) {
         const float v = cp[c].tv[head[s]];
@@ -719,7 +724,7 @@ __device__ __forceinline__ ff ldcg_ff(const ff* q) {
 
 // The finishers' shared memory: a row's chunk records while a row is merged, then the
 // request's selection arrays.
-constexpr int kFinParts = kMaxTreeChunks * static_cast<int>(sizeof(ChunkPart));
+constexpr int kFinParts = (kMaxTreeChunks > kHeadRecords ? kMaxTreeChunks : kHeadRecords) * static_cast<int>(sizeof(ChunkPart));
 constexpr int kFinSelect = (2 * kThreads + 2 * kMaxRows) * 8 + (kThreads + 2 * kMaxRows + kMaxPool) * 4;
 constexpr int kFinBytes = kFinParts > kFinSelect ? kFinParts : kFinSelect;
 
@@ -796,17 +801,20 @@ __device__ __forceinline__ void finish_row_static(const TreeBuildPlan& p, const 
     if (p.shape.parent[ch] != n) continue;
     if ((j++ % NW) != warp) continue;
     int tok;
+    float x;  // the token's logit
     if (!sampled) {
       tok = stok[j - 1];
+      x = sval[j - 1];
     } else {
       int nr = 0;
       tok = warp_draw(a.logits, row, p.dtype, p.V, sp, p.n_chunks, rs.M, invT, rs.WT,
                       a.u_draft[static_cast<size_t>(b) * p.R + ch], &nr);
       near_local += nr;
+      x = load_elem(a.logits, row + tok, p.dtype);
     }
     if (lane == 0) {
       v.ntok[ch] = tok;
-      v.nsc[ch] = ff_add(s_par, log_q(load_elem(a.logits, row + tok, p.dtype), rs));
+      v.nsc[ch] = ff_add(s_par, log_q(x, rs));
     }
   }
   if (lane == 0 && near_local) atomicAdd(v.state + 1, near_local);
@@ -1037,6 +1045,24 @@ __device__ __forceinline__ void finish_request_static(const TreeBuildPlan& p, co
   if (threadIdx.x == 0) a.out.near_tie[b] = atomicAdd(v.state + 1, 0);
 }
 
+// A frontier row's finisher, then (by the request ticket) the request's.
+__device__ __forceinline__ void finish_row_and_request(const TreeBuildPlan& p, const BuildArgs& a, int b, int f,
+                                                       uint8_t* s_fin, int* req_ticket, int* s_ticket) {
+  if (p.mode == EAGLE_TREE_DYNAMIC)
+    finish_row_dynamic(p, a, b, f, s_fin);
+  else
+    finish_row_static(p, a, b, f, s_fin);
+  __syncthreads();
+  if (threadIdx.x == 0) *s_ticket = atom_add_acq_rel(req_ticket, 1);
+  __syncthreads();
+  if (*s_ticket != a.F - 1) return;
+  if (p.mode == EAGLE_TREE_DYNAMIC)
+    finish_request_dynamic(p, a, b, s_fin);
+  else
+    finish_request_static(p, a, b);
+  if (threadIdx.x == 0) *req_ticket = 0;  // ready for the next level
+}
+
 // ------------------------------------------------------------------ one draft level
 // One CTA per (request x frontier row, 4096-token chunk): the chunk pass, then the
 // tickets: the row's last chunk CTA merges the row, the request's last row selects.
@@ -1056,22 +1082,18 @@ __global__ void __launch_bounds__(kThreads, 2)
   if (threadIdx.x == 0) s_ticket = atom_add_acq_rel(row_ticket, 1);
   __syncthreads();
   if (s_ticket != p.n_chunks - 1) return;
-  if (p.mode == EAGLE_TREE_DYNAMIC)
-    finish_row_dynamic(p, a, b, f, s_fin);
-  else
-    finish_row_static(p, a, b, f, s_fin);
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    *row_ticket = 0;  // ready for the next level
-    s_ticket = atom_add_acq_rel(req_ticket, 1);
-  }
-  __syncthreads();
-  if (s_ticket != a.F - 1) return;
-  if (p.mode == EAGLE_TREE_DYNAMIC)
-    finish_request_dynamic(p, a, b, s_fin);
-  else
-    finish_request_static(p, a, b);
-  if (threadIdx.x == 0) *req_ticket = 0;
+  if (threadIdx.x == 0) *row_ticket = 0;  // ready for the next level
+  finish_row_and_request(p, a, b, f, s_fin, req_ticket, &s_ticket);
+}
+
+// The finishers of a level whose records the LM-head kernel wrote (kHeadRecords per
+// row): one CTA per (request, frontier row) merges its row, the request's last selects.
+__global__ void __launch_bounds__(kThreads, 1) tree_head_finish_kernel(const TreeBuildPlan p, const BuildArgs a) {
+  __shared__ __align__(16) uint8_t s_fin[kFinBytes];
+  __shared__ int s_ticket;
+  const int b = blockIdx.x / a.F, f = blockIdx.x % a.F;
+  int* req_ticket = reinterpret_cast<int*>(a.ws + p.off_ticket) + p.B * p.f_max + b;
+  finish_row_and_request(p, a, b, f, s_fin, req_ticket, &s_ticket);
 }
 
 }  // namespace
@@ -1148,8 +1170,9 @@ void plan_tree_build(const eagle_tree_desc* d, TreeBuildPlan* p) {
   off = align256(off + static_cast<size_t>(p->B) * kMaxRows * sizeof(ff));
   p->off_best_idx = off;
   off = align256(off + static_cast<size_t>(p->B) * kMaxRows * 4);
-  p->off_part = off;
-  off = align256(off + static_cast<size_t>(p->B) * p->f_max * p->n_chunks * sizeof(ChunkPart));
+  p->off_part = off;  // room for the chunk pass's records or the LM head's, whichever is more
+  const int n_rec = p->n_chunks > kHeadRecords ? p->n_chunks : kHeadRecords;
+  off = align256(off + static_cast<size_t>(p->B) * p->f_max * n_rec * sizeof(ChunkPart));
   p->off_node_tok = off;
   off = align256(off + static_cast<size_t>(p->B) * p->R * 4);
   p->off_node_score = off;
@@ -1195,6 +1218,32 @@ cudaError_t launch_tree_build(const TreeBuildPlan& p, int level, const void* log
     else
       tree_level_kernel<true, false><<<grid, kThreads, 0, s>>>(p, a);
   }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_tree_build_head(const TreeBuildPlan& plan, int level, const void* hidden, const void* weight,
+                                   int hidden_dim, const int32_t* root_tok, const int32_t* seq_len, void* ws,
+                                   const eagle_tree& out, uint32_t* status, cudaStream_t s) {
+  TreeBuildPlan p = plan;
+  p.n_chunks = kHeadRecords;  // the finishers read the head kernel's records
+  BuildArgs a;
+  a.logits = nullptr;
+  a.u_draft = nullptr;
+  a.root_tok = root_tok;
+  a.seq_len = seq_len;
+  a.ws = static_cast<uint8_t*>(ws);
+  a.out = out;
+  a.level = level;
+  a.F = frontier_rows(p, level);
+  if (level == 1) {
+    const cudaError_t e = cudaMemsetAsync(a.ws + p.off_state, 0,
+                                          p.off_ticket - p.off_state + static_cast<size_t>(p.B) * (p.f_max + 1) * 4, s);
+    if (e != cudaSuccess) return e;
+  }
+  cudaError_t e = launch_lmhead_tree_records(p.B * a.F, hidden_dim, p.V, a.F, p.f_max, kHeadRecords, hidden, weight,
+                                             reinterpret_cast<TreeChunkRecord*>(a.ws + p.off_part), status, s);
+  if (e != cudaSuccess) return e;
+  tree_head_finish_kernel<<<p.B * a.F, kThreads, 0, s>>>(p, a);
   return cudaGetLastError();
 }
 

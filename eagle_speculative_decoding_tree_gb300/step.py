@@ -68,6 +68,9 @@ class GpuTreeBuilder:
         ud = None if u_draft is None else torch.from_numpy(np.asarray(u_draft, np.float32)).to(self.device)
         B.eagle_tree_build(self.desc, level, lg, ud, self.root_tok, self.seq_len, self.ws, self.out)
         self.levels = [lv for lv in self.levels if lv[0] < level] + [(level, lg, ud)]
+        return self._frontier(level)
+
+    def _frontier(self, level: int):
         if self.w.tree_mode == "dynamic":
             F = self.w.top_k
         else:  # the nodes created at this level (depth == level), in row order
@@ -76,14 +79,30 @@ class GpuTreeBuilder:
             for i in range(1, len(par)):
                 dep[i] = dep[par[i]] + 1
             F = int((dep == level).sum())
-        tok = self.out.frontier_tok[:, :F].cpu().numpy()
-        slot = self.out.frontier_slot[:, :F].cpu().numpy()
-        return tok, slot
+        return self.out.frontier_tok[:, :F].cpu().numpy(), self.out.frontier_slot[:, :F].cpu().numpy()
+
+    def expand_head(self, level: int, hidden: np.ndarray, head_weight: torch.Tensor, status: torch.Tensor):
+        """One level from the frontier rows' hidden states (bf16 bits [B][F][h]) and the
+        draft LM head (device bf16 [V][h]) through eagle_tree_build_head."""
+        if self.root_tok is None:
+            self.set_context(np.zeros(self.batch, np.int32), np.zeros(self.batch, np.int32))
+        hd = torch.from_numpy(np.ascontiguousarray(hidden).view(np.int16)).to(self.device).view(torch.bfloat16)
+        B.eagle_tree_build_head(self.desc, level, hd, head_weight, self.root_tok, self.seq_len, self.ws, self.out,
+                                status)
+        self.head_levels = [lv for lv in getattr(self, "head_levels", []) if lv[0] < level] + [(level, hd)]
+        return self._frontier(level)
 
     def replay(self, stream=None):
         """Enqueue the whole build again (every level, inputs already on the device)."""
         for level, lg, ud in self.levels:
             B.eagle_tree_build(self.desc, level, lg, ud, self.root_tok, self.seq_len, self.ws, self.out, stream)
+
+    def replay_head(self, head_weight: torch.Tensor, status: torch.Tensor, stream=None):
+        """Enqueue the whole build from hidden states again (every level's hidden states
+        already on the device)."""
+        for level, hd in self.head_levels:
+            B.eagle_tree_build_head(self.desc, level, hd, head_weight, self.root_tok, self.seq_len, self.ws,
+                                    self.out, status, stream)
 
     def finalize(self, root_tok: np.ndarray, seq_len: np.ndarray):
         o = self.out

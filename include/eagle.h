@@ -180,6 +180,28 @@ int eagle_tree_build(const eagle_tree_desc* d, int level, const void* frontier_l
                      const float* u_draft, const int32_t* root_tok, const int32_t* seq_len,
                      void* ws, size_t ws_bytes, const eagle_tree* out, void* stream);
 
+/* One draft level of the tree build from the draft model's hidden states instead of its
+ * logits: the draft LM head fused with tree expansion (EAGLE review, section 3.1: the
+ * draft maps its predicted feature to tokens through the frozen LM head; EAGLE-3 visual
+ * reading, "EAGLE-2": the dynamic tree keeps the most confident candidates).  For each
+ * frontier row, logits x = hidden W^T (bf16 x bf16, fp32 accumulation, on the tensor
+ * cores) are reduced to the row's softmax statistics (T = 1) and its best tokens by
+ * (logit desc, id asc) without being written; the level then selects exactly as
+ * eagle_tree_build does from logits with those values.
+ *   hidden       [B][F][hidden_dim] bf16 DEVICE: the draft's last hidden states of the
+ *                frontier rows, in eagle_tree.frontier_tok order (level 1: the root).
+ *   head_weight  [V][hidden_dim] bf16 DEVICE, row-major (the frozen LM head).
+ *   status       DEVICE uint32: EAGLE_STATUS_TIMEOUT is ORed in when a bounded wait of
+ *                the head kernel gives up (2 s); the caller clears it.
+ *   ws, out      as eagle_tree_build (the same workspace size; level 1 clears its
+ *                counters).  Levels from logits and from hidden states may be mixed.
+ * Modes: EAGLE_TREE_DYNAMIC and EAGLE_TREE_STATIC_TOPK (STATIC_SAMPLED draws need the
+ * logits: EAGLE_ERR_UNSUPPORTED).  Unsupported: hidden_dim not a multiple of 64,
+ * B x (widest frontier) > 128.  Near-ties as eagle_tree_build. */
+int eagle_tree_build_head(const eagle_tree_desc* d, int level, const void* hidden, const void* head_weight,
+                          int32_t hidden_dim, const int32_t* root_tok, const int32_t* seq_len, void* ws,
+                          size_t ws_bytes, const eagle_tree* out, uint32_t* status, void* stream);
+
 /* ---------------------------------------------------------------- tree attention */
 typedef struct {
   int32_t batch;       /* B */

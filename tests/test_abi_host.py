@@ -143,6 +143,29 @@ def test_tree_build_validation(lib):
     assert _call_build(lib, st([-1, 0, 1], temperature=0.0), u=A) == B.EAGLE_ERR_INVALID_ARG
 
 
+def _call_build_head(lib, desc, level=1, hidden_dim=4096, ws_bytes=1 << 40, status=A):
+    o = B.TreeOut(*([A] * 9))
+    lib.eagle_tree_build_head.argtypes = [ctypes.POINTER(B.TreeDesc), ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p,
+                                          ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                          ctypes.c_size_t, ctypes.POINTER(B.TreeOut), ctypes.c_void_p, ctypes.c_void_p]
+    return lib.eagle_tree_build_head(ctypes.byref(desc), level, A, A, hidden_dim, A, A, A, ws_bytes, ctypes.byref(o),
+                                     status, None)
+
+
+def test_tree_build_head_validation(lib):
+    dyn = lambda **kw: B.tree_desc(**{**dict(batch=1, vocab=128256, mode=B.EAGLE_TREE_DYNAMIC, depth=7, top_k=8,
+                                              total_tokens=60), **kw})
+    assert _call_build_head(lib, dyn(), level=0) == B.EAGLE_ERR_INVALID_ARG
+    assert _call_build_head(lib, dyn(), hidden_dim=0) == B.EAGLE_ERR_INVALID_ARG
+    assert _call_build_head(lib, dyn(), hidden_dim=96) == B.EAGLE_ERR_UNSUPPORTED  # not a multiple of 64
+    assert _call_build_head(lib, dyn(batch=17)) == B.EAGLE_ERR_UNSUPPORTED  # 17 x 8 rows > 128
+    assert _call_build_head(lib, dyn(), status=None) == B.EAGLE_ERR_INVALID_ARG
+    need = B.workspace_size(B.EAGLE_WS_TREE_BUILD, dyn())
+    assert _call_build_head(lib, dyn(), ws_bytes=need - 1) == B.EAGLE_ERR_WORKSPACE
+    sampled = B.tree_desc(1, 1000, B.EAGLE_TREE_STATIC_SAMPLED, 3, static_parent=[-1, 0, 0, 1], temperature=1.0)
+    assert _call_build_head(lib, sampled) == B.EAGLE_ERR_UNSUPPORTED  # draws read the logits
+
+
 def test_tree_frontier_rows(lib):
     d = B.tree_desc(1, 1000, B.EAGLE_TREE_STATIC_SAMPLED, 3, static_parent=[-1, 0, 0, 0, 0, 1, 1, 2, 3, 5, 5])
     assert [B.tree_frontier_rows(d, l) for l in (1, 2, 3)] == [1, 4, 4]
