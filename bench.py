@@ -380,6 +380,7 @@ def run_ours(args):
                 "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
                 else "fallback 6.8 TB/s", "traffic": traffic, "algorithmic_bytes_per_launch": bytes_layer,
                 "us_per_launch": round(attn_ms * 1e3, 2)}
+    accept_t, commit_t = time_accept_commit(st, stream, n_var, n_acc_all, max(5, args.steps // 16), peak)
     tree_build = time_tree_build(st, stream, max(20, args.steps // 2))
     lmhead = time_lmhead(st, stream, max(10, args.steps // 4), peak)
     tree_head = time_tree_head(st, stream, max(5, args.steps // 8), peak)
@@ -398,7 +399,8 @@ def run_ours(args):
                        "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU"},
             "step_roofline_frac": round(step_frac, 4), "step_algorithmic_bytes": int(step_bytes),
             "mean_accept_length": round(float(np.mean(n_acc_all + 1)), 4), "step_variants": int(n_var),
-            "roofline": roofline, "tree_build": tree_build, "tree_build_head": tree_head, "lmhead_stats": lmhead,
+            "roofline": roofline, "accept": accept_t, "commit": commit_t, "tree_build": tree_build,
+            "tree_build_head": tree_head, "lmhead_stats": lmhead,
             "ttt_attention": ttt, "e2e": e2e,
             "gpu_launches": int(launches_per_step * args.steps), "clocks": clocks,
             "setup_s": round(t_setup, 1)}
@@ -417,6 +419,65 @@ def run_ours(args):
         dist.destroy_process_group()
     if rank == 0:
         print(json.dumps(line), flush=True)
+
+
+def time_accept_commit(st, stream, n_var: int, n_acc_all, reps: int, peak: float):
+    """Acceptance and commit, each timed alone over the step variants (graphs replayed in
+    turn), against the bytes each must move: acceptance reads the target rows its walk
+    visits (n_acc + 1 per request; their draft rows too for drawn proposals), the commit
+    reads and writes the accepted path's K/V rows of every layer (n_acc + 1 rows per
+    request, K and V)."""
+    import torch
+    ga, gc = [], []
+    with torch.cuda.stream(stream):
+        for k in range(n_var):
+            st.use_variant(k)
+            st.reset()
+            st.accept(stream)
+            st.commit(stream)
+            stream.synchronize()
+            g1, g2 = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g1, stream=stream):
+                st.accept(stream)
+            with torch.cuda.graph(g2, stream=stream):
+                st.reset()
+                st.commit(stream)
+            ga.append(g1)
+            gc.append(g2)
+        st.use_variant(0)
+
+        def timed(gs):
+            for g in gs:
+                g.replay()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(reps):
+                for g in gs:
+                    g.replay()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            return e0.elapsed_time(e1) * 1e3 / (reps * len(gs))
+
+        us_acc = timed(ga)
+        # a commit moves the rows its own acceptance accepted: each variant's commit is
+        # timed after that variant's acceptance
+        us_com = 0.0
+        for k in range(n_var):
+            ga[k].replay()
+            us_com += timed([gc[k]]) / n_var
+        # leave the accept outputs of variant 0 in place for later users of the step
+        ga[0].replay()
+        stream.synchronize()
+    acc_bytes = float(np.mean([st.logit_bytes_visited(a) for a in n_acc_all]))
+    esz = 4 if st.w.dtype == "f32" else 2
+    rows = float(np.mean([np.sum(a + 1) for a in n_acc_all]))
+    com_bytes = rows * st.L * st.w.n_kv_heads * st.w.head_dim * esz * 2 * 2
+    return ({"us_per_step": round(us_acc, 2), "algorithmic_bytes": int(acc_bytes),
+             "gbs": round(acc_bytes / us_acc / 1e3, 1), "frac": round(acc_bytes / us_acc / 1e3 / peak, 4),
+             "bound": "latency (one group barrier per visited node)"},
+            {"us_per_step": round(us_com, 2), "algorithmic_bytes": int(com_bytes),
+             "gbs": round(com_bytes / us_com / 1e3, 1), "frac": round(com_bytes / us_com / 1e3 / peak, 4),
+             "bound": "launch latency (two kernels, a 4-byte seq_len reset in the graph)"})
 
 
 def time_tree_build(st, stream, reps: int):
