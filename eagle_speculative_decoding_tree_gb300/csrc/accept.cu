@@ -759,12 +759,18 @@ __device__ ff sum_records(const RowPart* rp, int C, ff* red) {
   return t;
 }
 
+// The walk's mode is a template argument (greedy, point-mass or drawn proposals), so that
+// each launch carries only its own path: the walk runs most of its code once per launch,
+// from a cold instruction cache, and a smaller kernel misses less.
+enum { kWalkGreedy = 0, kWalkDelta = 1, kWalkSampled = 2 };
+
+template <int MODE>
 __global__ void __launch_bounds__(kThreads, 2) accept_coop_kernel(const AcceptPlan p, const CoopArgs ca) {
   const WalkArgs& a = ca.w;
   const int b = blockIdx.y, cta = blockIdx.x, cpr = ca.cpr;
   const int R = p.R, V = p.V, C = p.n_chunks;
-  const bool greedy = !(p.temperature > 0.f);
-  const bool sampled = !greedy && p.proposal == EAGLE_PROPOSAL_SAMPLED;
+  constexpr bool greedy = MODE == kWalkGreedy;
+  constexpr bool sampled = MODE == kWalkSampled;
   const float invT = 1.f / (greedy ? 1.f : p.temperature);
   const int maxp = p.max_depth + 1;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -1161,11 +1167,17 @@ int coop_capacity() {
     return 0;
   }
   if (dev < 64 && (__atomic_load_n(&known, __ATOMIC_ACQUIRE) & (1ull << dev))) return cached[dev];
-  int per_sm = 0, sms = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, accept_coop_kernel, kThreads, 0) != cudaSuccess ||
+  int per_sm = 0, sms = 0, o1 = 0, o2 = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, accept_coop_kernel<kWalkGreedy>, kThreads, 0) !=
+          cudaSuccess ||
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o1, accept_coop_kernel<kWalkDelta>, kThreads, 0) != cudaSuccess ||
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o2, accept_coop_kernel<kWalkSampled>, kThreads, 0) !=
+          cudaSuccess ||
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
     per_sm = sms = 0;
   }
+  per_sm = per_sm < o1 ? per_sm : o1;  // the co-resident grid of the smallest occupancy
+  per_sm = per_sm < o2 ? per_sm : o2;
   (void)cudaGetLastError();
   const int n = per_sm * sms;
   if (dev < 64) {
@@ -1227,7 +1239,12 @@ cudaError_t launch_accept(const AcceptPlan& p, const void* target, const void* d
     attr[0].val.cooperative = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, accept_coop_kernel, p, ca);
+    if (!(p.temperature > 0.f))
+      e = cudaLaunchKernelEx(&cfg, accept_coop_kernel<kWalkGreedy>, p, ca);
+    else if (p.proposal == EAGLE_PROPOSAL_SAMPLED)
+      e = cudaLaunchKernelEx(&cfg, accept_coop_kernel<kWalkSampled>, p, ca);
+    else
+      e = cudaLaunchKernelEx(&cfg, accept_coop_kernel<kWalkDelta>, p, ca);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
   }

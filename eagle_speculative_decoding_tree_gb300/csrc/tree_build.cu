@@ -1045,10 +1045,13 @@ __device__ __forceinline__ void finish_request_static(const TreeBuildPlan& p, co
   if (threadIdx.x == 0) a.out.near_tie[b] = atomicAdd(v.state + 1, 0);
 }
 
-// A frontier row's finisher, then (by the request ticket) the request's.
+// A frontier row's finisher, then (by the request ticket) the request's.  The tree mode
+// is a template argument: the finishers run once per level from a cold instruction
+// cache, so each kernel carries only its own mode's code.
+template <bool DYN>
 __device__ __forceinline__ void finish_row_and_request(const TreeBuildPlan& p, const BuildArgs& a, int b, int f,
                                                        uint8_t* s_fin, int* req_ticket, int* s_ticket) {
-  if (p.mode == EAGLE_TREE_DYNAMIC)
+  if constexpr (DYN)
     finish_row_dynamic(p, a, b, f, s_fin);
   else
     finish_row_static(p, a, b, f, s_fin);
@@ -1056,7 +1059,7 @@ __device__ __forceinline__ void finish_row_and_request(const TreeBuildPlan& p, c
   if (threadIdx.x == 0) *s_ticket = atom_add_acq_rel(req_ticket, 1);
   __syncthreads();
   if (*s_ticket != a.F - 1) return;
-  if (p.mode == EAGLE_TREE_DYNAMIC)
+  if constexpr (DYN)
     finish_request_dynamic(p, a, b, s_fin);
   else
     finish_request_static(p, a, b);
@@ -1066,7 +1069,7 @@ __device__ __forceinline__ void finish_row_and_request(const TreeBuildPlan& p, c
 // ------------------------------------------------------------------ one draft level
 // One CTA per (request x frontier row, 4096-token chunk): the chunk pass, then the
 // tickets: the row's last chunk CTA merges the row, the request's last row selects.
-template <bool TOPK, bool BF16>
+template <bool TOPK, bool BF16, bool DYN>
 __global__ void __launch_bounds__(kThreads, 2)
     tree_level_kernel(const TreeBuildPlan p, const BuildArgs a) {
   __shared__ __align__(16) uint8_t s_fin[kFinBytes];
@@ -1083,17 +1086,18 @@ __global__ void __launch_bounds__(kThreads, 2)
   __syncthreads();
   if (s_ticket != p.n_chunks - 1) return;
   if (threadIdx.x == 0) *row_ticket = 0;  // ready for the next level
-  finish_row_and_request(p, a, b, f, s_fin, req_ticket, &s_ticket);
+  finish_row_and_request<DYN>(p, a, b, f, s_fin, req_ticket, &s_ticket);
 }
 
 // The finishers of a level whose records the LM-head kernel wrote (kHeadRecords per
 // row): one CTA per (request, frontier row) merges its row, the request's last selects.
+template <bool DYN>
 __global__ void __launch_bounds__(kThreads, 1) tree_head_finish_kernel(const TreeBuildPlan p, const BuildArgs a) {
   __shared__ __align__(16) uint8_t s_fin[kFinBytes];
   __shared__ int s_ticket;
   const int b = blockIdx.x / a.F, f = blockIdx.x % a.F;
   int* req_ticket = reinterpret_cast<int*>(a.ws + p.off_ticket) + p.B * p.f_max + b;
-  finish_row_and_request(p, a, b, f, s_fin, req_ticket, &s_ticket);
+  finish_row_and_request<DYN>(p, a, b, f, s_fin, req_ticket, &s_ticket);
 }
 
 }  // namespace
@@ -1209,14 +1213,19 @@ cudaError_t launch_tree_build(const TreeBuildPlan& p, int level, const void* log
   const bool bf16 = p.dtype != EAGLE_F32;
   if (p.mode == EAGLE_TREE_STATIC_SAMPLED) {
     if (bf16)
-      tree_level_kernel<false, true><<<grid, kThreads, 0, s>>>(p, a);
+      tree_level_kernel<false, true, false><<<grid, kThreads, 0, s>>>(p, a);
     else
-      tree_level_kernel<false, false><<<grid, kThreads, 0, s>>>(p, a);
+      tree_level_kernel<false, false, false><<<grid, kThreads, 0, s>>>(p, a);
+  } else if (p.mode == EAGLE_TREE_DYNAMIC) {
+    if (bf16)
+      tree_level_kernel<true, true, true><<<grid, kThreads, 0, s>>>(p, a);
+    else
+      tree_level_kernel<true, false, true><<<grid, kThreads, 0, s>>>(p, a);
   } else {
     if (bf16)
-      tree_level_kernel<true, true><<<grid, kThreads, 0, s>>>(p, a);
+      tree_level_kernel<true, true, false><<<grid, kThreads, 0, s>>>(p, a);
     else
-      tree_level_kernel<true, false><<<grid, kThreads, 0, s>>>(p, a);
+      tree_level_kernel<true, false, false><<<grid, kThreads, 0, s>>>(p, a);
   }
   return cudaGetLastError();
 }
@@ -1243,7 +1252,10 @@ cudaError_t launch_tree_build_head(const TreeBuildPlan& plan, int level, const v
   cudaError_t e = launch_lmhead_tree_records(p.B * a.F, hidden_dim, p.V, a.F, p.f_max, kHeadRecords, hidden, weight,
                                              reinterpret_cast<TreeChunkRecord*>(a.ws + p.off_part), status, s);
   if (e != cudaSuccess) return e;
-  tree_head_finish_kernel<<<p.B * a.F, kThreads, 0, s>>>(p, a);
+  if (p.mode == EAGLE_TREE_DYNAMIC)
+    tree_head_finish_kernel<true><<<p.B * a.F, kThreads, 0, s>>>(p, a);
+  else
+    tree_head_finish_kernel<false><<<p.B * a.F, kThreads, 0, s>>>(p, a);
   return cudaGetLastError();
 }
 
