@@ -810,10 +810,15 @@ __global__ void __launch_bounds__(kThreads, 2) accept_coop_kernel(const AcceptPl
   const bool keep = cpr == C;
   const int own_lo = cta * kVocabChunk;
 
+  // the request's tree and uniforms, once: later levels read them from shared memory
+  __shared__ float s_ua[kMaxRows];
+  __shared__ float s_uf;
   for (int c = threadIdx.x; c < R; c += kThreads) {
     s_par[c] = a.parent[static_cast<size_t>(b) * R + c];
     s_tokr[c] = a.tokens[static_cast<size_t>(b) * R + c];
+    s_ua[c] = a.u_accept[static_cast<size_t>(b) * R + c];
   }
+  if (threadIdx.x == 0) s_uf = a.u_final[b];
   if (threadIdx.x == 0) {
     s_len = 1;
     s_path[0] = 0;
@@ -860,7 +865,7 @@ __global__ void __launch_bounds__(kThreads, 2) accept_coop_kernel(const AcceptPl
     for (int i = threadIdx.x; i < s_nk; i += kThreads) {
       const int c = s_kids[i];
       const int d = tok[c];
-      s_uk[i] = a.u_accept[row_base + c];
+      s_uk[i] = s_ua[c];
       s_xk[i] = (!greedy && !sampled && d >= 0 && d < V) ? load_elem(a.target, xrow + d, p.dtype) : 0.f;
     }
     // this CTA's slice of the node's target (and draft) row, exchanged with the group
@@ -936,8 +941,55 @@ __global__ void __launch_bounds__(kThreads, 2) accept_coop_kernel(const AcceptPl
       }
       __syncthreads();
     } else if (!sampled) {
-      // point-mass proposals: p_res(d) = p(d) / (1 - mass of the rejected tokens)
-      if (threadIdx.x == 0) {
+      // point-mass proposals: p_res(d) = p(d) / (1 - mass of the rejected tokens).  Child
+      // i is tested only when every earlier child was rejected, so its residual mass is
+      // 1 minus the masses of the distinct valid tokens before it: one lane per child, an
+      // exclusive scan of those masses, and the first child whose test passes is the one
+      // accepted (a node has at most 16 children; more take the serial loop)
+      const int nk = s_nk;
+      if (nk <= 32 && warp == 0) {
+        const float invZ = 1.f / ff_float(s_Zt);
+        const bool valid = lane < nk;
+        const int c = valid ? s_kids[lane] : 0;
+        const int d = valid ? tok[c] : -1;
+        const bool bad = valid && (d < 0 || d >= V);
+        bool dup = false;  // an earlier valid child with the same token (its mass is gone)
+        for (int j = 0; j < lane && j < nk; ++j) {
+          const int dj = tok[s_kids[j]];
+          dup |= (dj >= 0 && dj < V && dj == d);
+        }
+        const bool live = valid && !bad && !dup;
+        const float pd = live ? s_wk[lane] * invZ : 0.f;
+        ff incl = ff_make(pd);
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const ff t = ff_shfl_up(incl, o);
+          if (lane >= o) incl = ff_add(incl, t);
+        }
+        const ff rejmass = ff_sub(incl, ff_make(pd));  // exclusive: the children before this one
+        const float denom = ff_float(ff_sub(ff_make(1.f), rejmass));
+        const float ratio = denom > 0.f ? __fdividef(pd, denom) : 0.f;
+        const float u = valid ? s_uk[lane] : 2.f;
+        const bool tested = valid && !bad;
+        const unsigned acc = __ballot_sync(0xffffffffu, tested && u < ratio);
+        const int first = acc ? __ffs(acc) - 1 : 32;  // children after it are never tested
+        const bool seen = lane <= first;
+        const bool near = __any_sync(0xffffffffu, seen && tested && fabsf(u - ratio) < kNearTieEps);
+        const bool anybad = __any_sync(0xffffffffu, seen && bad && lane != first);
+        // the rejected tokens and their weights, in child order, when none is accepted
+        const unsigned rj = __ballot_sync(0xffffffffu, live && lane < first);
+        if (live && lane < first) {
+          const int slot = __popc(rj & ((1u << lane) - 1u));
+          s_rej[slot] = d;
+          s_rejw[slot] = s_wk[lane];
+        }
+        if (lane == 0) {
+          if (near) s_near = 1;
+          if (anybad) s_status |= EAGLE_STATUS_BAD_TOKEN;
+          s_nrej = __popc(rj);
+          if (first < 32) s_next = s_kids[first];
+        }
+      } else if (nk > 32 && threadIdx.x == 0) {
         const float invZ = 1.f / ff_float(s_Zt);
         ff rejmass = ff_make(0.f);
         for (int i = 0; i < s_nk; ++i) {
@@ -1030,7 +1082,7 @@ __global__ void __launch_bounds__(kThreads, 2) accept_coop_kernel(const AcceptPl
     // ---- draw the emitted token from the (residual) target distribution: the chunk
     // masses (the group's slice passes for a drawn-proposal residual), the chunk holding
     // the crossing, then that chunk element by element in the CTA that owns it
-    const float u = a.u_final[b];
+    const float u = s_uf;
     const bool residual = sampled && s_nz > 0;
     const int nz = s_nz, nrej = s_nrej;
     if (residual) {
