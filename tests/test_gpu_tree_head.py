@@ -43,7 +43,7 @@ def _kept_per_row(w, level, F):
     return np.array([(par == n).sum() for n in nodes])
 
 
-def build_head_both(w, batch, h, seed, label):
+def build_head_both(w, batch, h, seed, label, logits_levels=()):
     g = np.random.default_rng(seed)
     V = w.vocab
     Wb = _bits(g.normal(0, 1 / np.sqrt(h), (V, h)))
@@ -70,8 +70,13 @@ def build_head_both(w, batch, h, seed, label):
             if 0 < kf < V:
                 gap |= (srt[:, f, kf - 1] - srt[:, f, kf]) < 1e-4
         excluded |= gap
-        gt, gs = gpu.expand_head(level, H, Wd, status)
-        ot, os_ = ora.expand(level, lo.astype(np.float32))
+        if level in logits_levels:  # this level from the logits themselves (fp32 rows)
+            lg = lo.astype(np.float32)
+            gt, gs = gpu.expand(level, lg)
+            ot, os_ = ora.expand(level, lg)
+        else:
+            gt, gs = gpu.expand_head(level, H, Wd, status)
+            ot, os_ = ora.expand(level, lo.astype(np.float32))
         excluded |= ora.t.near_tie > 0
         for b in np.nonzero(~excluded)[0]:
             assert np.array_equal(gt[b], ot[b]), (level, b, gt[b], ot[b])
@@ -113,3 +118,10 @@ def test_tree_head_llama8b_draft_shape():
     """A LLaMA-3.1-8B-shaped draft head (vocab 128256, hidden 4096) over the llama8b
     workload's dynamic tree (depth 7, top-8, 60 drafts)."""
     build_head_both(W["llama8b"], 1, 4096, seed=14, label="tree from head llama8b")
+
+
+def test_tree_levels_from_logits_and_from_the_head_mix():
+    """Level 1 from the logits (eagle_tree_build), the later levels from hidden states
+    (eagle_tree_build_head) in the same workspace."""
+    w = W["vicuna7b"].with_(vocab=7000, top_k=6, depth=4, total_tokens=20, dtype="f32")
+    build_head_both(w, 8, 128, seed=15, label="tree from logits then head", logits_levels=(1,))
